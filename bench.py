@@ -1,0 +1,393 @@
+"""Benchmark of the fused causal-conv1d + KDA verify decode on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--variant auto|small_batch|large_batch]
+
+One step = one kda_conv_verify call over the whole workload (default: the
+large-batch verify, N=256 sequences, T=4 tokens, H=HV=32, K=V=128, bf16
+activations, fp32 state, softplus gate).  `value` is verify head-steps/s
+(N*T*HV per call) timed with CUDA events on the launching stream with the
+inputs resident in HBM; `e2e` is the same metric through the same public call
+with the inputs copied in from pinned host memory and every output copied
+back inside the timed region.  `roofline` compares the algorithmic bytes of
+one launch divided by its measured duration with the measured HBM copy
+bandwidth.  `cpu_baseline` times the CPU oracle on a bounded sample of the
+same workload on the host cores.
+
+Under torchrun every rank runs its own copy of the workload on its own GPU
+(weak scaling, no collective on the data path); the time is the maximum over
+ranks.  `--impl reference` times the CPU oracle as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify head-steps/s (N·T·HV) and achieved HBM GB/s vs GB300 peak, 1 GPU"
+UNIT = "head-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="large_bf16_n256_t4_h32")
+    ap.add_argument("--variant", default="auto")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def workload(name):
+    from linear_attention_speculative_gb300 import workloads as wk
+    if name in wk.WORKLOADS:
+        return wk.WORKLOADS[name]
+    for w in wk.sweep():
+        if w.name == name:
+            return w
+    raise SystemExit(f"unknown workload {name}")
+
+
+def measured_hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_src_hash():
+    d = os.path.join(ROOT, "linear_attention_speculative_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(wl_name):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    or None when absent or taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"ncu_{wl_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_src_sha256:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_src_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling in the background."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.t_on = None
+        self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark_on(self):
+        self.t_on = time.time()
+
+    def mark_off(self):
+        self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [s for t, s in self.samples
+                if self.t_on is not None and self.t_on - 0.1 <= t <= (self.t_off or t) + 0.1]
+        if not rows:
+            rows = [s for _, s in self.samples]
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(wl, inputs_cpu, max_seconds=30.0):
+    """Time the CPU oracle as it stands on a bounded sample of the workload,
+    one sequence per thread at a time, on all host cores."""
+    import oracle
+    cores = os.cpu_count() or 1
+    s = wl.shape
+    per_seq = s.T * s.HV
+    # one sequence costs ~1e-3 s per head-step on one core; aim at ~20 s of CPU work
+    n_seq = max(cores, min(s.N, int(20.0 / (per_seq * 1.0e-3))))
+    n_seq = min(s.N, (n_seq + cores - 1) // cores * cores)
+    seqs = list(range(n_seq))
+    sub = {k: (v[seqs] if v is not None and k in ("mixed_qkv", "conv_state", "a", "b", "S0") else v)
+           for k, v in inputs_cpu.items()}
+    # bf16/fp32 -> fp64 conversion of the inputs happens outside the timed region
+    sub = {k: (oracle._f64(v) if v is not None else None) for k, v in sub.items()}
+    t0 = time.perf_counter()
+    oracle.verify(sub, wl.gate, threads=cores)
+    dt = time.perf_counter() - t0
+    hs = n_seq * per_seq
+    return {"value": hs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n_seq} of {s.N} sequences of {wl.name} ({hs} head-steps), fp64 C oracle, "
+                      f"{cores} threads, {dt:.2f} s wall"}
+
+
+def run_reference(args, wl):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    from linear_attention_speculative_gb300 import workloads as wk
+    inputs = wk.make_inputs(wl)
+    cores = os.cpu_count() or 1
+    s = wl.shape
+    seqs = list(range(min(s.N, cores)))
+    sub = {k: (v[seqs] if v is not None and k in ("mixed_qkv", "conv_state", "a", "b", "S0") else v)
+           for k, v in inputs.items()}
+    oracle.build()
+    sub = {k: (oracle._f64(v) if v is not None else None) for k, v in sub.items()}
+    for _ in range(args.warmup):
+        oracle.verify(sub, wl.gate, threads=cores)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.verify(sub, wl.gate, threads=cores)
+    dt = time.perf_counter() - t0
+    hs = len(seqs) * s.T * s.HV
+    value = hs * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "K": s.K,
+                   "V": s.V, "act": s.act, "gate": wl.gate,
+                   "sample_per_step": f"{len(seqs)} sequences ({hs} head-steps)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{len(seqs)} of {s.N} sequences per step, {cores} threads"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, wl):
+    import torch
+    from linear_attention_speculative_gb300 import kda
+    from linear_attention_speculative_gb300 import workloads as wk
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    s = wl.shape
+    inputs_cpu = wk.make_inputs(wl)
+    inp = {k: (v.to(dev) if v is not None else None) for k, v in inputs_cpu.items()}
+    shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
+    ws = kda.alloc_workspace(shape, dev)
+    out = {k: v.to(dev) for k, v in wk.empty_outputs(wl).items()}
+    stream = torch.cuda.current_stream(dev)
+    alg_bytes = s.algorithmic_bytes()
+    flush_l2 = alg_bytes < 2 * L2_BYTES
+    flush_buf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush_l2 else None
+
+    def step(x=inp):
+        kda.conv_verify(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"], x["dt_bias"],
+                        x["a"], x["b"], x["S0"], wl.gate, out["o"], out["inter_ssm"],
+                        out["conv_snapshots"], ws, stream=stream, variant=args.variant,
+                        shape=shape)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    barrier()
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+        time.sleep(0.3)
+    K = args.steps
+    barrier()
+    clocks.mark_on()
+    if flush_l2:
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(K):
+            flush_buf.fill_(float(i))  # evict the previous step's lines from L2
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        barrier()
+        kernel_ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    else:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(K):
+            step()
+        e1.record(stream)
+        barrier()
+        kernel_ms = e0.elapsed_time(e1)
+    clocks.mark_off()
+    t_max = torch.tensor([kernel_ms], device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    kernel_ms = float(t_max.item())
+    ms_per_step = kernel_ms / K
+    value = world * s.head_steps * K / (kernel_ms / 1e3)
+
+    # end to end: pinned host inputs in, every output back, through the same call
+    E = max(1, min(args.e2e_steps, K))
+    host_in = {k: (v.pin_memory() if v is not None else None) for k, v in inputs_cpu.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+    host_cs = torch.empty(inp["conv_state"].shape, dtype=inp["conv_state"].dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values()) + \
+        host_cs.numel() * host_cs.element_size()
+
+    def e2e_step():
+        for k, v in host_in.items():
+            if v is not None:
+                inp[k].copy_(v, non_blocking=True)
+        step()
+        for k, v in host_out.items():
+            v.copy_(out[k], non_blocking=True)
+        host_cs.copy_(inp["conv_state"], non_blocking=True)
+
+    e2e_step()
+    barrier()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    f1.record(stream)
+    barrier()
+    e2e_ms = f0.elapsed_time(f1)
+    t_e2e = torch.tensor([e2e_ms], device=dev)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
+    e2e_value = world * s.head_steps * E / (float(t_e2e.item()) / 1e3)
+
+    if rank == 0:
+        clocks.stop()
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    peak, peak_src = measured_hbm_peak()
+    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+    plan = kda.make_plan(shape, torch.cuda.get_device_properties(dev).multi_processor_count,
+                         args.variant)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "K": s.K,
+                   "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
+                   "variant": {1: "small_batch", 2: "large_batch"}[plan.variant],
+                   "grid": plan.grid, "warps_per_cta": plan.warps,
+                   "l2": ("L2 flushed between steps (256 MB write)" if flush_l2 else
+                          f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB moved per step"),
+                   "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(wl.name),
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
+                     "kernel": "kda_verify_kernel"},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": E},
+        "gpu_launches": K,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, inputs_cpu)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse()
+    wl = workload(args.workload)
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * kda_verify.h -- C ABI of the fused causal-conv1d + Kimi Delta Attention
+ * (gated delta rule) multi-token-prediction verify decode for GB300 (sm_103a).
+ *
+ * Operation ("[KDA] Fuse causal conv1d into MTP verify decode", cuLA pull
+ * request 107: description section and both commit messages).  For every
+ * sequence n and value head hv, with q/k head h = hv / (HV/H):
+ *
+ *   1. width-4 depthwise causal conv1d over [conv_state || T new tokens] of
+ *      the packed pre-convolution mixed_qkv, then SiLU, on the q, k and v
+ *      channels;
+ *   2. q and k L2-normalised over K (eps = 1e-6 inside the root), q scaled
+ *      by K^-1/2;
+ *   3. the gate: softplus form g = -exp(A_log[hv]) * softplus(a + dt_bias),
+ *      softplus linear above 20 (a real branch, as the review of that page
+ *      requires), or the safe form g = min(a, 0); beta = sigmoid(b);
+ *   4. the gated delta rule, token by token, on the fp32 K x V state:
+ *        S <- diag(exp g) S ;  S <- S + beta k (v - S^T k)^T ;  o = S^T q ;
+ *   5. outputs: o, the state after every token (inter_ssm), the raw conv
+ *      window after every token (conv_snapshots), and conv_state rolled in
+ *      place to the last W-1 raw inputs.  The persistent state S0 is read only.
+ *
+ * Layouts: every tensor is dense, row-major, contiguous; "act" is the
+ * activation type of the call (fp32 or bf16); dim = 2*H*K + HV*V and the
+ * channels of mixed_qkv / conv_w / conv_state / conv_snapshots are ordered
+ * q (H heads x K) | k (H x K) | v (HV x V).  conv_w tap W-1 multiplies the
+ * newest token; conv_state index 0 is the oldest raw input.
+ *
+ * Ownership: the caller allocates every buffer (device memory) and keeps
+ * ownership; the library allocates nothing and keeps no pointer after a call
+ * returns.  Calls are asynchronous on `stream` (NULL = legacy default
+ * stream); no call synchronises except kda_read_status.
+ *
+ * Errors: 0 on success; a negative KDA_ERR_* code when the arguments are
+ * rejected on the host (nothing is launched, no buffer is touched); a
+ * positive value is a cudaError_t reported by the launch.
+ */
+#ifndef KDA_VERIFY_H
+#define KDA_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle type as cudaStream_t. */
+typedef struct CUstream_st* kda_stream_t;
+
+typedef enum { KDA_GATE_SOFTPLUS = 0, KDA_GATE_SAFE = 1 } kda_gate_mode;
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Kernel variants.  AUTO picks from N*HV, T and the SM count. */
+typedef enum {
+  KDA_VARIANT_AUTO = 0,
+  KDA_VARIANT_SMALL_BATCH = 1, /* one CTA per (sequence, v-head, v-tile) */
+  KDA_VARIANT_LARGE_BATCH = 2  /* persistent CTAs over whole (sequence, v-head) units,
+                                  next state tile prefetched by TMA */
+} kda_variant;
+
+/* Problem shape.  Supported: T in [1, KDA_MAX_T] (N == 0 is a no-op),
+ * H >= 1, HV a multiple of H, W == 4, K and V in {32, 64, 128}. */
+typedef struct {
+  int N, T, H, HV, K, V, W;
+  kda_dtype act;
+} kda_shape;
+
+#define KDA_MAX_T 16
+
+/* Error codes (negative: rejected on the host, nothing launched). */
+#define KDA_OK 0
+#define KDA_ERR_NULL (-1)        /* a required pointer is NULL */
+#define KDA_ERR_SHAPE (-2)       /* unsupported or inconsistent shape */
+#define KDA_ERR_DTYPE (-3)       /* unknown activation type */
+#define KDA_ERR_MISALIGNED (-4)  /* a pointer is not 16-byte aligned */
+#define KDA_ERR_ALIAS (-5)       /* an output overlaps an input or another output */
+#define KDA_ERR_WORKSPACE (-6)   /* workspace missing or smaller than kda_workspace_bytes */
+#define KDA_ERR_GATE (-7)        /* unknown gate mode, or softplus without A_log/dt_bias */
+#define KDA_ERR_VARIANT (-8)     /* unknown variant */
+#define KDA_ERR_DEVICE (-9)      /* device query or driver entry point failed */
+
+/* Device status bits, written into the workspace by a kernel that gave up a
+ * bounded wait (the kernel then returns without hanging the GPU). */
+#define KDA_STATUS_OK 0
+#define KDA_STATUS_TMA_TIMEOUT 1
+
+/* The fused verify decode.
+ *   s              problem shape (host pointer, read during the call only)
+ *   mixed_qkv      act  [N, T, dim]      packed pre-conv q|k|v, read
+ *   conv_w         act  [dim, W]         read
+ *   conv_state     act  [N, dim, W-1]    IN/OUT: rolled in place to the last
+ *                                        W-1 raw inputs of each channel
+ *   A_log          f32  [HV]             softplus gate only (NULL for safe)
+ *   dt_bias        f32  [HV, K]          softplus gate only (NULL for safe)
+ *   a              act  [N, T, HV, K]    gate input; safe gate: the log-decay
+ *   b              act  [N, T, HV]       beta logit
+ *   S0             f32  [N, HV, K, V]    persistent state, read only
+ *   gate_mode      KDA_GATE_SOFTPLUS or KDA_GATE_SAFE
+ *   o              act  [N, T, HV, V]    OUT
+ *   inter_ssm      f32  [N, T, HV, K, V] OUT: S after token t
+ *   conv_snapshots act  [N, T, dim, W-1] OUT: raw conv window after token t
+ *                                        (the W-1 newest raw inputs)
+ *   workspace      device scratch of >= kda_workspace_bytes(s) bytes, zeroed
+ *                  once before its first use; every launch leaves it zeroed
+ *                  again.  One workspace per stream: two launches that run
+ *                  concurrently must not share one.
+ *   workspace_bytes  size of `workspace`
+ * All device pointers must be 16-byte aligned.  Outputs must not overlap
+ * inputs or each other; conv_state is the only in-place buffer. */
+int kda_conv_verify(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                    void* conv_state, const float* A_log, const float* dt_bias,
+                    const void* a, const void* b, const float* S0, kda_gate_mode gate_mode,
+                    void* o, float* inter_ssm, void* conv_snapshots, void* workspace,
+                    size_t workspace_bytes, kda_stream_t stream);
+
+/* Same as kda_conv_verify with an explicit variant (AUTO = the dispatcher's
+ * choice).  Every variant produces bit-identical outputs. */
+int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                            void* conv_state, const float* A_log, const float* dt_bias,
+                            const void* a, const void* b, const float* S0,
+                            kda_gate_mode gate_mode, void* o, float* inter_ssm,
+                            void* conv_snapshots, void* workspace, size_t workspace_bytes,
+                            kda_variant variant, kda_stream_t stream);
+
+/* Bytes of workspace a call with shape `s` needs (arrival counters for the
+ * shared q/k conv_state write-back, N*H int32, plus a status word), rounded
+ * up to 256.  Returns 0 for a NULL shape. */
+size_t kda_workspace_bytes(const kda_shape* s);
+
+/* The launch plan the dispatcher picks; host-only, no CUDA call.
+ *   num_sms   streaming multiprocessors of the device
+ *   variant   requested variant (AUTO lets the dispatcher decide)
+ * Out: chosen variant, v-tile width bv (columns of V per CTA), warps per
+ * CTA, grid size.  Returns 0 or a negative KDA_ERR_* code. */
+typedef struct {
+  int variant;
+  int bv;
+  int warps;
+  int grid;
+  int ctas_per_sm;
+  long long items;
+} kda_plan;
+int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
+
+/* Synchronously read (and clear) the device status word of `workspace` on
+ * `stream`.  *status receives KDA_STATUS_* bits.  Returns 0 or an error. */
+int kda_read_status(const kda_shape* s, void* workspace, int* status, kda_stream_t stream);
+
+/* Human-readable text for a return code (negative KDA_ERR_* or positive
+ * cudaError_t).  Never NULL. */
+const char* kda_strerror(int code);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KDA_VERIFY_H */

@@ -1,0 +1,287 @@
+// kda_api.cu -- the C ABI declared in include/kda_verify.h: argument
+// validation, the small/large-batch dispatcher, the TMA descriptor of the
+// state tensor, and the launch.  Host code only; kernels live in
+// kda_kernel.cuh and are instantiated in kda_inst_*.cu.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "kda_launch.cuh"
+#include "../../include/kda_verify.h"
+
+namespace {
+
+using kda::LaunchCfg;
+using kda::Params;
+
+constexpr int kSmemPerSm = 233472;  // bytes of shared memory per SM (228 KB)
+constexpr int kSmemReservedPerCta = 1024;
+
+bool supported_dim(int x) { return x == 32 || x == 64 || x == 128; }
+
+int check_shape(const kda_shape* s) {
+  if (!s) return KDA_ERR_NULL;
+  if (s->act != KDA_F32 && s->act != KDA_BF16) return KDA_ERR_DTYPE;
+  if (s->N < 0 || s->T < 1 || s->T > KDA_MAX_T) return KDA_ERR_SHAPE;
+  if (s->H < 1 || s->HV < s->H || s->HV % s->H != 0) return KDA_ERR_SHAPE;
+  if (s->W != 4) return KDA_ERR_SHAPE;
+  if (!supported_dim(s->K) || !supported_dim(s->V)) return KDA_ERR_SHAPE;
+  // TMA row coordinate (N*HV*K) and element counts must fit the index types
+  const long long rows = (long long)s->N * s->HV * s->K;
+  if (rows >= (1ll << 31)) return KDA_ERR_SHAPE;
+  return KDA_OK;
+}
+
+size_t act_bytes(const kda_shape* s) { return s->act == KDA_F32 ? 4 : 2; }
+
+int ctas_per_sm_for(int warps, size_t smem) {
+  const int by_regs = 16 / warps;  // launch bounds cap registers at 128/thread
+  const int by_smem = (int)(kSmemPerSm / (smem + kSmemReservedPerCta));
+  return std::max(1, std::min(by_regs, by_smem));
+}
+
+struct Span {
+  uintptr_t lo, hi;
+};
+
+bool overlap(const Span& a, const Span& b) {
+  return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+int num_sms_of_current_device(int* out) {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev < 64 && cache[dev] > 0) {
+    *out = cache[dev];
+    return 0;
+  }
+  int n = 0;
+  e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return (int)e;
+  if (dev < 64) cache[dev] = n;
+  *out = n;
+  return 0;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_version(void) { return 0x000100; }
+
+size_t kda_workspace_bytes(const kda_shape* s) {
+  if (!s) return 0;
+  const size_t counters = (size_t)std::max(0, s->N) * (size_t)std::max(0, s->H);
+  const size_t bytes = (counters + 4) * sizeof(int);  // counters + status word (+pad)
+  return (bytes + 255) / 256 * 256;
+}
+
+int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!out) return KDA_ERR_NULL;
+  if (num_sms < 1) return KDA_ERR_DEVICE;
+  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
+      variant != KDA_VARIANT_LARGE_BATCH)
+    return KDA_ERR_VARIANT;
+  const long long units = (long long)s->N * s->HV;
+  kda_variant v = variant;
+  if (v == KDA_VARIANT_AUTO) {
+    // Large batch once every SM gets at least two whole (n, hv) units; below
+    // that, split V across CTAs to put more SMs to work.
+    v = units >= 2LL * num_sms ? KDA_VARIANT_LARGE_BATCH : KDA_VARIANT_SMALL_BATCH;
+  }
+  std::memset(out, 0, sizeof(*out));
+  out->variant = v;
+  if (v == KDA_VARIANT_LARGE_BATCH) {
+    out->bv = s->V;
+    out->warps = s->V / 16;
+    const size_t smem = kda::smem_bytes(s->T, s->K, out->bv, 2);
+    out->ctas_per_sm = ctas_per_sm_for(out->warps, smem);
+    out->items = units;
+    const long long cap = (long long)num_sms * out->ctas_per_sm;
+    out->grid = (int)std::max(1LL, std::min(units, cap));
+  } else {
+    int bv = 32;
+    if (units * (s->V / 32) < 4LL * num_sms) bv = 16;
+    out->bv = bv;
+    out->warps = bv / 16;
+    const size_t smem = kda::smem_bytes(s->T, s->K, bv, 1);
+    out->ctas_per_sm = ctas_per_sm_for(out->warps, smem);
+    out->items = units * (s->V / bv);
+    out->grid = (int)std::max(1LL, out->items);
+  }
+  if (units == 0) out->grid = 0;
+  return KDA_OK;
+}
+
+int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                            void* conv_state, const float* A_log, const float* dt_bias,
+                            const void* a, const void* b, const float* S0,
+                            kda_gate_mode gate_mode, void* o, float* inter_ssm,
+                            void* conv_snapshots, void* workspace, size_t workspace_bytes,
+                            kda_variant variant, kda_stream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (gate_mode != KDA_GATE_SOFTPLUS && gate_mode != KDA_GATE_SAFE) return KDA_ERR_GATE;
+  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
+      variant != KDA_VARIANT_LARGE_BATCH)
+    return KDA_ERR_VARIANT;
+  if (s->N == 0) return KDA_OK;  // nothing to do
+  if (!mixed_qkv || !conv_w || !conv_state || !a || !b || !S0 || !o || !inter_ssm ||
+      !conv_snapshots)
+    return KDA_ERR_NULL;
+  if (gate_mode == KDA_GATE_SOFTPLUS && (!A_log || !dt_bias)) return KDA_ERR_GATE;
+  if (!workspace || workspace_bytes < kda_workspace_bytes(s)) return KDA_ERR_WORKSPACE;
+
+  const size_t ab = act_bytes(s);
+  const size_t N = s->N, T = s->T, H = s->H, HV = s->HV, K = s->K, V = s->V;
+  const size_t dim = 2 * H * K + HV * V;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al16(mixed_qkv) || !al16(conv_w) || !al16(conv_state) || !al16(a) || !al16(S0) ||
+      !al16(o) || !al16(inter_ssm) || !al16(conv_snapshots) || !al16(workspace) ||
+      (reinterpret_cast<uintptr_t>(b) % ab) != 0)
+    return KDA_ERR_MISALIGNED;
+  if (gate_mode == KDA_GATE_SOFTPLUS && (!al16(A_log) || !al16(dt_bias)))
+    return KDA_ERR_MISALIGNED;
+
+  auto span = [](const void* p, size_t bytes) {
+    Span sp;
+    sp.lo = reinterpret_cast<uintptr_t>(p);
+    sp.hi = sp.lo + (p ? bytes : 0);
+    return sp;
+  };
+  const Span in[] = {
+      span(mixed_qkv, N * T * dim * ab), span(conv_w, dim * 4 * ab),
+      span(gate_mode == KDA_GATE_SOFTPLUS ? A_log : nullptr, HV * 4),
+      span(gate_mode == KDA_GATE_SOFTPLUS ? dt_bias : nullptr, HV * K * 4),
+      span(a, N * T * HV * K * ab), span(b, N * T * HV * ab), span(S0, N * HV * K * V * 4)};
+  const Span wr[] = {span(conv_state, N * dim * 3 * ab), span(o, N * T * HV * V * ab),
+                     span(inter_ssm, N * T * HV * K * V * 4),
+                     span(conv_snapshots, N * T * dim * 3 * ab),
+                     span(workspace, kda_workspace_bytes(s))};
+  for (size_t i = 0; i < sizeof(wr) / sizeof(wr[0]); ++i) {
+    for (const Span& x : in)
+      if (overlap(wr[i], x)) return KDA_ERR_ALIAS;
+    for (size_t j = 0; j < sizeof(wr) / sizeof(wr[0]); ++j)
+      if (j != i && overlap(wr[i], wr[j])) return KDA_ERR_ALIAS;
+  }
+
+  int num_sms = 0;
+  rc = num_sms_of_current_device(&num_sms);
+  if (rc) return rc;
+  kda_plan plan;
+  rc = kda_make_plan(s, num_sms, variant, &plan);
+  if (rc) return rc;
+
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return KDA_ERR_DEVICE;
+  CUtensorMap tmap;
+  std::memset(&tmap, 0, sizeof(tmap));
+  cuuint64_t gdim[2] = {(cuuint64_t)V, (cuuint64_t)(N * HV * K)};
+  cuuint64_t gstride[1] = {(cuuint64_t)(V * sizeof(float))};
+  cuuint32_t box[2] = {(cuuint32_t)plan.bv, (cuuint32_t)K};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(S0), gdim,
+                       gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return KDA_ERR_DEVICE;
+
+  Params p;
+  p.mixed_qkv = mixed_qkv;
+  p.conv_w = conv_w;
+  p.conv_state = conv_state;
+  p.A_log = A_log;
+  p.dt_bias = dt_bias;
+  p.a = a;
+  p.b = b;
+  p.o = o;
+  p.inter_ssm = inter_ssm;
+  p.conv_snapshots = conv_snapshots;
+  p.counters = static_cast<int*>(workspace);
+  p.status = static_cast<int*>(workspace) + N * H;
+  p.num_items = plan.items;
+  p.N = s->N;
+  p.T = s->T;
+  p.H = s->H;
+  p.HV = s->HV;
+  p.V = s->V;
+  p.dim = (int)dim;
+  p.G = s->HV / s->H;
+  p.nvt = s->V / plan.bv;
+  p.gate_mode = gate_mode == KDA_GATE_SOFTPLUS ? 0 : 1;
+
+  LaunchCfg cfg;
+  cfg.K = s->K;
+  cfg.warps = plan.warps;
+  cfg.persist = plan.variant == KDA_VARIANT_LARGE_BATCH;
+  cfg.grid = plan.grid;
+  cfg.smem = kda::smem_bytes(s->T, s->K, plan.bv, cfg.persist ? 2 : 1);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = s->act == KDA_BF16 ? kda::launch_bf16(tmap, p, cfg, st) : kda::launch_f32(tmap, p, cfg, st);
+  if (rc < 0) return KDA_ERR_SHAPE;
+  return rc;
+}
+
+int kda_conv_verify(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                    void* conv_state, const float* A_log, const float* dt_bias, const void* a,
+                    const void* b, const float* S0, kda_gate_mode gate_mode, void* o,
+                    float* inter_ssm, void* conv_snapshots, void* workspace,
+                    size_t workspace_bytes, kda_stream_t stream) {
+  return kda_conv_verify_variant(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0,
+                                 gate_mode, o, inter_ssm, conv_snapshots, workspace,
+                                 workspace_bytes, KDA_VARIANT_AUTO, stream);
+}
+
+int kda_read_status(const kda_shape* s, void* workspace, int* status, kda_stream_t stream) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!workspace || !status) return KDA_ERR_NULL;
+  int* dev_status = static_cast<int*>(workspace) + (size_t)s->N * s->H;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(status, dev_status, sizeof(int), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e == cudaSuccess && *status != 0) e = cudaMemsetAsync(dev_status, 0, sizeof(int), st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  return (int)e;
+}
+
+const char* kda_strerror(int code) {
+  switch (code) {
+    case KDA_OK: return "success";
+    case KDA_ERR_NULL: return "a required pointer is NULL";
+    case KDA_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case KDA_ERR_DTYPE: return "unknown activation dtype";
+    case KDA_ERR_MISALIGNED: return "a pointer is not 16-byte aligned";
+    case KDA_ERR_ALIAS: return "an output buffer overlaps an input or another output";
+    case KDA_ERR_WORKSPACE: return "workspace missing or too small";
+    case KDA_ERR_GATE: return "unknown gate mode, or softplus gate without A_log/dt_bias";
+    case KDA_ERR_VARIANT: return "unknown kernel variant";
+    case KDA_ERR_DEVICE: return "device query or driver entry point failed";
+    default: break;
+  }
+  if (code > 0) return cudaGetErrorString(static_cast<cudaError_t>(code));
+  return "unknown error";
+}
+
+}  // extern "C"

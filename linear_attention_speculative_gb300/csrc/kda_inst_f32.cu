@@ -1,0 +1,8 @@
+// fp32-activation instantiations of the verify-decode kernel.
+#include "kda_launch.cuh"
+
+namespace kda {
+int launch_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
+  return launch_dispatch<float>(tmap, p, cfg, st);
+}
+}  // namespace kda

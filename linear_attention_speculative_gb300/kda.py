@@ -1,0 +1,184 @@
+"""Thin ctypes binding of the C ABI in include/kda_verify.h.
+
+Argument marshalling only: every step of the verify decode runs in the CUDA
+library.  PyTorch supplies device memory and the current stream.  If the
+library is missing the import of this module fails loudly; there is no CPU
+fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+import torch
+
+from . import _build
+
+GATE_SOFTPLUS = 0
+GATE_SAFE = 1
+VARIANT_AUTO = 0
+VARIANT_SMALL_BATCH = 1
+VARIANT_LARGE_BATCH = 2
+VARIANTS = {"auto": VARIANT_AUTO, "small_batch": VARIANT_SMALL_BATCH,
+            "large_batch": VARIANT_LARGE_BATCH}
+F32 = 0
+BF16 = 1
+MAX_T = 16
+
+# The names declared in include/kda_verify.h.
+EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_workspace_bytes",
+            "kda_make_plan", "kda_read_status", "kda_strerror", "kda_version")
+
+
+class KdaShape(ctypes.Structure):
+    _fields_ = [("N", ctypes.c_int), ("T", ctypes.c_int), ("H", ctypes.c_int),
+                ("HV", ctypes.c_int), ("K", ctypes.c_int), ("V", ctypes.c_int),
+                ("W", ctypes.c_int), ("act", ctypes.c_int)]
+
+
+class KdaPlan(ctypes.Structure):
+    _fields_ = [("variant", ctypes.c_int), ("bv", ctypes.c_int), ("warps", ctypes.c_int),
+                ("grid", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
+                ("items", ctypes.c_longlong)]
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, what: str = "kda_conv_verify"):
+        self.code = code
+        super().__init__(f"{what} failed with code {code}: {strerror(code)}")
+
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library not built ({path}); run __graft_entry__.build() "
+                          "or python -m linear_attention_speculative_gb300._build")
+    L = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    sp = ctypes.POINTER(KdaShape)
+    args_common = [sp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, vp, vp, sz]
+    L.kda_conv_verify.restype = ctypes.c_int
+    L.kda_conv_verify.argtypes = args_common + [vp]
+    L.kda_conv_verify_variant.restype = ctypes.c_int
+    L.kda_conv_verify_variant.argtypes = args_common + [ctypes.c_int, vp]
+    L.kda_workspace_bytes.restype = sz
+    L.kda_workspace_bytes.argtypes = [sp]
+    L.kda_make_plan.restype = ctypes.c_int
+    L.kda_make_plan.argtypes = [sp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(KdaPlan)]
+    L.kda_read_status.restype = ctypes.c_int
+    L.kda_read_status.argtypes = [sp, vp, ctypes.POINTER(ctypes.c_int), vp]
+    L.kda_strerror.restype = ctypes.c_char_p
+    L.kda_strerror.argtypes = [ctypes.c_int]
+    L.kda_version.restype = ctypes.c_int
+    L.kda_version.argtypes = []
+    _lib = L
+    return L
+
+
+def lib():
+    return _load()
+
+
+def strerror(code: int) -> str:
+    return lib().kda_strerror(code).decode()
+
+
+def make_shape(N, T, H, HV, K=128, V=128, act="bf16", W=4) -> KdaShape:
+    a = {"bf16": BF16, "f32": F32, torch.bfloat16: BF16, torch.float32: F32}[act]
+    return KdaShape(N, T, H, HV, K, V, W, a)
+
+
+def shape_of(mixed_qkv: torch.Tensor, a: torch.Tensor, S0: torch.Tensor) -> KdaShape:
+    """Infer the problem shape from the tensors (dim = 2HK + HV V)."""
+    N, T, dim = mixed_qkv.shape
+    HV, K = a.shape[2], a.shape[3]
+    V = S0.shape[3]
+    H = (dim - HV * V) // (2 * K)
+    return make_shape(N, T, H, HV, K, V, mixed_qkv.dtype)
+
+
+def workspace_bytes(shape: KdaShape) -> int:
+    return int(lib().kda_workspace_bytes(ctypes.byref(shape)))
+
+
+def alloc_workspace(shape: KdaShape, device) -> torch.Tensor:
+    """A zeroed workspace (the kernel leaves it zeroed after every launch)."""
+    n = max(256, workspace_bytes(shape))
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def make_plan(shape: KdaShape, num_sms: int, variant: str = "auto") -> KdaPlan:
+    plan = KdaPlan()
+    rc = lib().kda_make_plan(ctypes.byref(shape), num_sms, VARIANTS[variant], ctypes.byref(plan))
+    if rc != 0:
+        raise KdaError(rc, "kda_make_plan")
+    return plan
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def conv_verify(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: str,
+                o, inter_ssm, conv_snapshots, workspace, stream=None, variant: str = "auto",
+                shape: Optional[KdaShape] = None) -> None:
+    """Launch the fused verify decode on `stream` (default: current stream).
+
+    Tensors must be contiguous CUDA tensors in the layouts of the header;
+    conv_state is updated in place; o / inter_ssm / conv_snapshots are
+    written.  Raises KdaError on any non-zero return code."""
+    if shape is None:
+        shape = shape_of(mixed_qkv, a, S0)
+    gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
+    rc = lib().kda_conv_verify_variant(
+        ctypes.byref(shape), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_state), _ptr(A_log),
+        _ptr(dt_bias), _ptr(a), _ptr(b), _ptr(S0), gm, _ptr(o), _ptr(inter_ssm),
+        _ptr(conv_snapshots), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        VARIANTS[variant], _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc)
+
+
+def read_status(shape: KdaShape, workspace: torch.Tensor, stream=None) -> int:
+    st = ctypes.c_int(0)
+    rc = lib().kda_read_status(ctypes.byref(shape), _ptr(workspace), ctypes.byref(st),
+                               _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_read_status")
+    return st.value
+
+
+def run(inputs: Dict[str, torch.Tensor], gate: str, variant: str = "auto",
+        workspace: Optional[torch.Tensor] = None, stream=None) -> Dict[str, torch.Tensor]:
+    """Convenience: allocate outputs on the inputs' device and launch.
+    `inputs["conv_state"]` is rolled in place."""
+    x = inputs["mixed_qkv"]
+    shape = shape_of(x, inputs["a"], inputs["S0"])
+    dev = x.device
+    N, T, dim = x.shape
+    HV, K, V = shape.HV, shape.K, shape.V
+    out = {
+        "o": torch.empty((N, T, HV, V), dtype=x.dtype, device=dev),
+        "inter_ssm": torch.empty((N, T, HV, K, V), dtype=torch.float32, device=dev),
+        "conv_snapshots": torch.empty((N, T, dim, 3), dtype=x.dtype, device=dev),
+    }
+    ws = workspace if workspace is not None else alloc_workspace(shape, dev)
+    conv_verify(x, inputs["conv_w"], inputs["conv_state"], inputs.get("A_log"),
+                inputs.get("dt_bias"), inputs["a"], inputs["b"], inputs["S0"], gate,
+                out["o"], out["inter_ssm"], out["conv_snapshots"], ws, stream=stream,
+                variant=variant, shape=shape)
+    return out

@@ -150,6 +150,13 @@ def verify(inputs: Dict, gate: str, seqs: Optional[Iterable[int]] = None,
     conv_state [n,dim,W-1] (the rolled state).
     """
     L = lib()
+    if seqs is not None:
+        # keep only the requested sequences before converting to float64
+        seqs = list(seqs)
+        inputs = dict(inputs)
+        for key in ("mixed_qkv", "conv_state", "a", "b", "S0"):
+            v = inputs[key]
+            inputs[key] = v[seqs] if hasattr(v, "detach") else np.asarray(v)[seqs]
     x = _f64(inputs["mixed_qkv"])
     N, T, dim = x.shape
     w = _f64(inputs["conv_w"])
@@ -164,7 +171,7 @@ def verify(inputs: Dict, gate: str, seqs: Optional[Iterable[int]] = None,
     gm = GATE_SOFTPLUS if gate == "softplus" else GATE_SAFE
     A_log = _f64(inputs.get("A_log")) if gm == GATE_SOFTPLUS else None
     dt_bias = _f64(inputs.get("dt_bias")) if gm == GATE_SOFTPLUS else None
-    seqs = list(range(N)) if seqs is None else list(seqs)
+    seqs = list(range(N))  # positions within the (possibly sliced) inputs
     n = len(seqs)
     out = {
         "o": np.empty((n, T, HV, V)),

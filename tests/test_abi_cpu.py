@@ -1,0 +1,170 @@
+"""The C ABI on the host: the library loads, exports every declared symbol,
+rejects bad arguments before touching the GPU, and plans launches.
+
+No test here launches a kernel: argument checks run before any CUDA call, and
+the pointers below are fake addresses that are never dereferenced."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from linear_attention_speculative_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda_verify.h")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    _build.build()
+    from linear_attention_speculative_gb300 import kda as mod
+    mod.lib()
+    return mod
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(kda_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("kda_conv_verify", "kda_workspace_bytes", "kda_strerror"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(kda):
+    L = ctypes.CDLL(_build.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} declared in kda_verify.h but not exported"
+    assert set(kda.EXPORTED) <= set(declared_functions())
+
+
+def test_version_and_strerror(kda):
+    assert kda.lib().kda_version() == 0x000100
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8, -9, -1234):
+        assert isinstance(kda.strerror(code), str) and kda.strerror(code)
+
+
+def test_workspace_bytes(kda):
+    s = kda.make_shape(256, 4, 32, 32)
+    ws = kda.workspace_bytes(s)
+    assert ws % 256 == 0 and ws >= (256 * 32 + 1) * 4
+    assert kda.lib().kda_workspace_bytes(None) == 0
+
+
+# ---- the dispatcher (host logic only) --------------------------------------
+
+def test_plan_large_batch_for_many_units(kda):
+    p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
+    assert p.variant == kda.VARIANT_LARGE_BATCH
+    assert p.bv == 128 and p.warps == 8 and p.items == 256 * 32
+    assert 1 <= p.grid <= 152 * p.ctas_per_sm
+
+
+def test_plan_small_batch_for_few_units(kda):
+    p = kda.make_plan(kda.make_shape(16, 4, 16, 16), 152)
+    assert p.variant == kda.VARIANT_SMALL_BATCH
+    assert p.items == 16 * 16 * (128 // p.bv)
+    assert p.grid == p.items
+    p1 = kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)
+    assert p1.bv == 16 and p1.warps == 1  # narrowest tiles for the tiniest batch
+
+
+def test_plan_forced_variants_and_small_heads(kda):
+    s = kda.make_shape(8, 2, 2, 4, K=64, V=32)
+    big = kda.make_plan(s, 152, "large_batch")
+    assert big.variant == kda.VARIANT_LARGE_BATCH and big.bv == 32 and big.warps == 2
+    small = kda.make_plan(s, 152, "small_batch")
+    assert small.variant == kda.VARIANT_SMALL_BATCH and small.bv in (16, 32)
+
+
+@pytest.mark.parametrize("bad", [dict(T=0), dict(T=17), dict(W=3), dict(K=96), dict(V=256),
+                                 dict(H=3, HV=4), dict(HV=1, H=2)])
+def test_plan_rejects_bad_shapes(kda, bad):
+    args = dict(N=2, T=2, H=2, HV=2, K=32, V=32, W=4)
+    args.update(bad)
+    s = kda.KdaShape(args["N"], args["T"], args["H"], args["HV"], args["K"], args["V"],
+                     args["W"], kda.BF16)
+    with pytest.raises(kda.KdaError) as e:
+        kda.make_plan(s, 152)
+    assert e.value.code == -2
+
+
+# ---- argument validation with fake (never dereferenced) pointers -----------
+
+def _fake_args(kda, **over):
+    base = 0x7f0000000000
+    names = ["mixed_qkv", "conv_w", "conv_state", "A_log", "dt_bias", "a", "b", "S0", "o",
+             "inter_ssm", "conv_snapshots", "workspace"]
+    ptrs = {n: base + i * (1 << 24) for i, n in enumerate(names)}
+    ptrs.update(over)
+    return ptrs
+
+
+def _call(kda, shape, ptrs, gate=0, ws_bytes=1 << 20, variant=0):
+    L = kda.lib()
+    v = lambda n: ctypes.c_void_p(ptrs[n]) if ptrs[n] is not None else None
+    return L.kda_conv_verify_variant(
+        ctypes.byref(shape), v("mixed_qkv"), v("conv_w"), v("conv_state"), v("A_log"),
+        v("dt_bias"), v("a"), v("b"), v("S0"), gate, v("o"), v("inter_ssm"),
+        v("conv_snapshots"), v("workspace"), ws_bytes, variant, None)
+
+
+def test_rejects_null_pointers(kda):
+    s = kda.make_shape(2, 2, 2, 2, 32, 32)
+    for name in ("mixed_qkv", "conv_w", "conv_state", "a", "b", "S0", "o", "inter_ssm",
+                 "conv_snapshots"):
+        assert _call(kda, s, _fake_args(kda, **{name: None})) == -1, name
+    assert _call(kda, s, _fake_args(kda, workspace=None)) == -6
+    # softplus needs A_log and dt_bias; the safe gate does not
+    assert _call(kda, s, _fake_args(kda, A_log=None)) == -7
+    assert _call(kda, s, _fake_args(kda, A_log=None, dt_bias=None), gate=1) not in (-1, -7)
+
+
+def test_rejects_misaligned_pointers(kda):
+    s = kda.make_shape(2, 2, 2, 2, 32, 32)
+    for name in ("mixed_qkv", "S0", "inter_ssm", "conv_state", "o", "a"):
+        ptrs = _fake_args(kda)
+        ptrs[name] += 8
+        assert _call(kda, s, ptrs) == -4, name
+
+
+def test_rejects_aliasing(kda):
+    s = kda.make_shape(2, 2, 2, 2, 32, 32)
+    ptrs = _fake_args(kda)
+    ptrs["inter_ssm"] = ptrs["S0"] + 4096  # output inside an input
+    assert _call(kda, s, ptrs) == -5
+    ptrs = _fake_args(kda)
+    ptrs["o"] = ptrs["conv_snapshots"]     # two outputs on one buffer
+    assert _call(kda, s, ptrs) == -5
+    ptrs = _fake_args(kda)
+    ptrs["conv_state"] = ptrs["mixed_qkv"] + 64  # in-place buffer inside an input
+    assert _call(kda, s, ptrs) == -5
+
+
+def test_rejects_small_workspace_bad_gate_and_variant(kda):
+    s = kda.make_shape(64, 2, 8, 8, 32, 32)
+    assert _call(kda, s, _fake_args(kda), ws_bytes=16) == -6
+    assert _call(kda, s, _fake_args(kda), gate=7) == -7
+    assert _call(kda, s, _fake_args(kda), variant=9) == -8
+
+
+def test_empty_batch_is_a_noop(kda):
+    s = kda.make_shape(0, 2, 2, 2, 32, 32)
+    nulls = {n: None for n in _fake_args(kda)}
+    assert _call(kda, s, nulls) == 0
+
+
+def test_valid_arguments_reach_the_device_query(kda):
+    # Everything valid: on a machine without a GPU the call stops at the first
+    # CUDA query and reports its error (a positive cudaError_t), no crash.
+    s = kda.make_shape(2, 2, 2, 2, 32, 32)
+    rc = _call(kda, s, _fake_args(kda))
+    import torch
+    if not torch.cuda.is_available():
+        assert rc > 0

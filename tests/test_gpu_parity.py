@@ -1,0 +1,254 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle.
+
+Covers the four fixed workloads (tiny fp32, decode N=16, GVA N=64 with the
+safe gate, large batch N=256 with planted softplus-overflow values) in every
+variant, bit-identity between variants, determinism, the chained-call
+identity, edge shapes (T = 1, 2, 3, 16; K, V in {32, 64, 128}; GVA ratios
+1..8; odd N), CUDA-graph replay, side streams and the self-resetting
+workspace.  The tolerance lives in parity_util.
+"""
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_speculative_gb300 import workloads as wk
+from parity_util import (TOL, assert_parity, conv_window_properties, max_rel_err, rel_rmse,
+                         run_kernel, to_device)
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = ("auto", "small_batch", "large_batch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from linear_attention_speculative_gb300 import kda
+    kda.lib()  # fails loudly if the library is missing
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("wl", [wk.TINY, wk.DECODE], ids=lambda w: w.name)
+def test_parity_full(wl, variant):
+    inp = wk.make_inputs(wl)
+    ref = oracle.verify(inp, wl.gate, threads=8)
+    out, cs = run_kernel(inp, wl.gate, variant)
+    e_o, e_s = assert_parity(out, cs, ref)
+    print(f"{wl.name} {variant}: o max {e_o:.3e} rmse {rel_rmse(out['o'].double().cpu(), ref['o']):.3e}"
+          f"  state max {e_s:.3e}")
+
+
+# Full-size workloads: o / inter_ssm on sampled sequences (first, last, middle,
+# and a seeded random pick), conv outputs on every element by the window
+# property.
+def _sample(N, k=6, seed=0):
+    rng = np.random.default_rng(seed)
+    pick = {0, 1, N // 2, N - 1} | set(int(i) for i in rng.integers(0, N, k))
+    return sorted(pick)
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("wl", [wk.GVA, wk.LARGE], ids=lambda w: w.name)
+def test_parity_full_size_sampled(wl, variant):
+    inp = wk.make_inputs(wl)
+    seqs = _sample(wl.shape.N, seed=wl.seed)
+    ref = oracle.verify(inp, wl.gate, seqs=seqs, threads=8)
+    out, cs = run_kernel(inp, wl.gate, variant)
+    e_o, e_s = assert_parity(out, cs, ref, seqs=seqs)
+    conv_window_properties(inp, out, cs)
+    assert torch.isfinite(out["inter_ssm"]).all() and torch.isfinite(out["o"].float()).all()
+    print(f"{wl.name} {variant}: o max {e_o:.3e} state max {e_s:.3e} on seqs {seqs}")
+
+
+def test_large_workload_takes_the_softplus_overflow_branch():
+    # a = 100 at planted positions: the exp in softplus would overflow fp32;
+    # the real branch keeps everything finite and the decay underflows to 0.
+    wl = wk.LARGE
+    inp = wk.make_inputs(wl)
+    a = inp["a"].float()
+    assert (a == 100.0).sum() > 1000 and (a == 25.0).sum() > 1000
+    seqs = [0, 3]
+    ref = oracle.verify(inp, wl.gate, seqs=seqs)
+    out, cs = run_kernel(inp, wl.gate, "auto")
+    assert_parity(out, cs, ref, seqs=seqs)
+    assert torch.isfinite(out["inter_ssm"][seqs]).all()
+
+
+@pytest.mark.parametrize("wl", [wk.DECODE, wk.GVA,
+                                wk.custom(5, 3, 2, 8, 64, 128, gate="safe", seed=3),
+                                wk.custom(7, 2, 4, 4, 128, 64, seed=4)],
+                         ids=lambda w: w.name)
+def test_variants_bit_identical(wl):
+    inp = wk.make_inputs(wl)
+    outs = {v: run_kernel(inp, wl.gate, v) for v in ("small_batch", "large_batch")}
+    a, b = outs["small_batch"], outs["large_batch"]
+    for key in ("o", "inter_ssm", "conv_snapshots"):
+        assert torch.equal(a[0][key], b[0][key]), key
+    assert torch.equal(a[1], b[1])
+
+
+def test_deterministic_across_repeats():
+    iters = int(os.environ.get("KDA_DET_ITERS", "20"))
+    wl = wk.GVA
+    inp = wk.make_inputs(wl)
+    first = None
+    for v in ("small_batch", "large_batch"):
+        for _ in range(iters):
+            out, cs = run_kernel(inp, wl.gate, v)
+            cur = (out["o"], out["inter_ssm"], out["conv_snapshots"], cs)
+            if first is None:
+                first = cur
+            else:
+                for x, y in zip(first, cur):
+                    assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("variant", ("small_batch", "large_batch"))
+@pytest.mark.parametrize("gate", ("softplus", "safe"))
+def test_chain_of_single_token_calls_is_bit_exact(variant, gate):
+    from linear_attention_speculative_gb300 import kda
+    T = 4
+    wl = wk.custom(6, T, 2, 4, 128, 128, gate=gate, seed=11)
+    inp = to_device(wk.make_inputs(wl))
+    full_cs = inp["conv_state"].clone()
+    full = kda.run(dict(inp, conv_state=full_cs), gate, variant=variant)
+    S = inp["S0"].clone()
+    cs = inp["conv_state"].clone()
+    for t in range(T):
+        step = dict(inp)
+        step["mixed_qkv"] = inp["mixed_qkv"][:, t:t + 1].contiguous()
+        step["a"] = inp["a"][:, t:t + 1].contiguous()
+        step["b"] = inp["b"][:, t:t + 1].contiguous()
+        step["S0"] = S
+        step["conv_state"] = cs
+        out = kda.run(step, gate, variant=variant)
+        assert torch.equal(out["o"][:, 0], full["o"][:, t])
+        assert torch.equal(out["inter_ssm"][:, 0], full["inter_ssm"][:, t])
+        assert torch.equal(out["conv_snapshots"][:, 0], full["conv_snapshots"][:, t])
+        S = out["inter_ssm"][:, 0].contiguous()
+    torch.cuda.synchronize()
+    assert torch.equal(cs, full_cs)
+
+
+EDGE = [
+    # N, T, H, HV, K, V, act, gate
+    (1, 1, 1, 1, 128, 128, "bf16", "softplus"),
+    (3, 2, 2, 2, 128, 128, "bf16", "safe"),
+    (5, 3, 1, 8, 128, 128, "bf16", "softplus"),
+    (2, 16, 2, 4, 128, 128, "bf16", "softplus"),
+    (3, 5, 4, 8, 64, 64, "bf16", "safe"),
+    (4, 4, 2, 2, 32, 32, "bf16", "softplus"),
+    (3, 3, 2, 4, 64, 128, "bf16", "softplus"),
+    (3, 4, 2, 2, 128, 32, "bf16", "safe"),
+    (2, 7, 3, 6, 32, 64, "f32", "softplus"),
+    (9, 2, 1, 2, 128, 128, "f32", "safe"),
+]
+
+
+@pytest.mark.parametrize("variant", VARIANTS)
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}".format(*c))
+def test_edge_shapes(case, variant):
+    N, T, H, HV, K, V, act, gate = case
+    wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=N * 100 + T)
+    inp = wk.make_inputs(wl)
+    ref = oracle.verify(inp, gate)
+    out, cs = run_kernel(inp, gate, variant)
+    assert_parity(out, cs, ref)
+
+
+def test_empty_batch_is_a_noop():
+    from linear_attention_speculative_gb300 import kda
+    wl = wk.custom(0, 2, 2, 2, 128, 128)
+    inp = to_device(wk.make_inputs(wl))
+    out = kda.run(inp, "softplus")
+    torch.cuda.synchronize()
+    assert out["o"].numel() == 0
+
+
+def test_workspace_is_left_zeroed():
+    from linear_attention_speculative_gb300 import kda
+    wl = wk.GVA  # G = 4 readers per q/k group
+    inp = to_device(wk.make_inputs(wl))
+    shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
+    ws = kda.alloc_workspace(shape, "cuda")
+    for v in ("small_batch", "large_batch"):
+        kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate, variant=v, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(ws.count_nonzero()) == 0
+    assert kda.read_status(shape, ws) == 0
+
+
+def test_side_streams_and_separate_workspaces():
+    from linear_attention_speculative_gb300 import kda
+    wl = wk.custom(8, 4, 2, 4, 128, 128, seed=21)
+    inp_cpu = wk.make_inputs(wl)
+    ref, _ = run_kernel(inp_cpu, wl.gate, "auto")
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    results = []
+    for st in streams:
+        with torch.cuda.stream(st):
+            inp = to_device(inp_cpu)
+            results.append((kda.run(inp, wl.gate, stream=st), inp["conv_state"]))
+    torch.cuda.synchronize()
+    for out, cs in results:
+        assert torch.equal(out["inter_ssm"], ref["inter_ssm"])
+        assert torch.equal(out["o"], ref["o"])
+
+
+def test_cuda_graph_replay():
+    from linear_attention_speculative_gb300 import kda
+    wl = wk.custom(4, 3, 2, 4, 128, 128, seed=23)
+    inp_cpu = wk.make_inputs(wl)
+    ref, ref_cs = run_kernel(inp_cpu, wl.gate, "auto")
+    inp = to_device(inp_cpu)
+    cs0 = inp["conv_state"].clone()
+    shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
+    ws = kda.alloc_workspace(shape, "cuda")
+    out = {k: torch.empty_like(v) for k, v in ref.items()}
+
+    def call():
+        kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
+                        inp["dt_bias"], inp["a"], inp["b"], inp["S0"], wl.gate, out["o"],
+                        out["inter_ssm"], out["conv_snapshots"], ws, shape=shape)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call()  # warm-up outside capture (first-use attribute setup)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for _ in range(3):
+        inp["conv_state"].copy_(cs0)
+        out["inter_ssm"].zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out["inter_ssm"], ref["inter_ssm"])
+        assert torch.equal(out["o"], ref["o"])
+        assert torch.equal(inp["conv_state"], ref_cs)
+
+
+def test_rejects_bad_args_on_device():
+    from linear_attention_speculative_gb300 import kda
+    wl = wk.custom(2, 2, 2, 2, 128, 128)
+    inp = to_device(wk.make_inputs(wl))
+    shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
+    ws = kda.alloc_workspace(shape, "cuda")
+    o = torch.empty((2, 2, 2, 128), dtype=torch.bfloat16, device="cuda")
+    st = torch.empty((2, 2, 2, 128, 128), device="cuda")
+    sn = torch.empty((2, 2, shape.HV * 128 + 4 * 128, 3), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kda.KdaError) as e:  # output aliases an input
+        kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
+                        inp["dt_bias"], inp["a"], inp["b"], inp["S0"], "softplus", o,
+                        inp["S0"], sn, ws, shape=shape)
+    assert e.value.code == -5
+    with pytest.raises(kda.KdaError) as e:  # misaligned state pointer
+        kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
+                        inp["dt_bias"], inp["a"], inp["b"], inp["S0"].view(-1)[1:], "softplus",
+                        o, st, sn, ws, shape=shape)
+    assert e.value.code == -4
