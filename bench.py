@@ -50,6 +50,14 @@ def parse():
     ap.add_argument("--variant", default="auto")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--scaling", default="weak", choices=["weak", "strong"],
+                    help="weak: every rank runs the whole workload; strong: the ranks split "
+                         "its sequences")
+    ap.add_argument("--N", type=int, default=0,
+                    help="override the number of sequences (small profiling cases)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every point of the T x N x heads x gate sweep in both variants")
+    ap.add_argument("--sweep-out", default="")
     return ap.parse_args()
 
 
@@ -233,9 +241,12 @@ def run_reference(args, wl):
 
 
 def run_ours(args, wl):
+    import dataclasses
+
     import torch
     from linear_attention_speculative_gb300 import kda
     from linear_attention_speculative_gb300 import workloads as wk
+    from linear_attention_speculative_gb300.replicas import max_over_ranks, shard
 
     rank, world, local = dist_env()
     if world > 1:
@@ -243,8 +254,16 @@ def run_ours(args, wl):
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    s = wl.shape
     inputs_cpu = wk.make_inputs(wl)
+    global_head_steps = wl.shape.head_steps * (world if args.scaling == "weak" else 1)
+    if args.scaling == "strong" and world > 1:
+        # this rank's contiguous slice of the global batch: no data exchange
+        lo, hi = shard(wl.shape.N, rank, world)
+        inputs_cpu = {k: (v[lo:hi].contiguous() if v is not None and k in
+                          ("mixed_qkv", "conv_state", "a", "b", "S0") else v)
+                      for k, v in inputs_cpu.items()}
+        wl = dataclasses.replace(wl, shape=dataclasses.replace(wl.shape, N=hi - lo))
+    s = wl.shape
     inp = {k: (v.to(dev) if v is not None else None) for k, v in inputs_cpu.items()}
     shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
     ws = kda.alloc_workspace(shape, dev)
@@ -297,13 +316,9 @@ def run_ours(args, wl):
         barrier()
         kernel_ms = e0.elapsed_time(e1)
     clocks.mark_off()
-    t_max = torch.tensor([kernel_ms], device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    kernel_ms = float(t_max.item())
+    kernel_ms = max_over_ranks(kernel_ms, dev)
     ms_per_step = kernel_ms / K
-    value = world * s.head_steps * K / (kernel_ms / 1e3)
+    value = global_head_steps * K / (kernel_ms / 1e3)
 
     # end to end: pinned host inputs in, every output back, through the same call
     E = max(1, min(args.e2e_steps, K))
@@ -332,12 +347,8 @@ def run_ours(args, wl):
         e2e_step()
     f1.record(stream)
     barrier()
-    e2e_ms = f0.elapsed_time(f1)
-    t_e2e = torch.tensor([e2e_ms], device=dev)
-    if world > 1:
-        import torch.distributed as dist
-        dist.all_reduce(t_e2e, op=dist.ReduceOp.MAX)
-    e2e_value = world * s.head_steps * E / (float(t_e2e.item()) / 1e3)
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), dev)
+    e2e_value = global_head_steps * E / (e2e_ms / 1e3)
 
     if rank == 0:
         clocks.stop()
@@ -354,7 +365,7 @@ def run_ours(args, wl):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "scaling": args.scaling, "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "K": s.K,
                    "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
                    "variant": {1: "small_batch", 2: "large_batch"}[plan.variant],
@@ -380,9 +391,78 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Time each sweep point in both variants and the dispatcher's pick.
+    Inputs are drawn on the device (timing only); L2 is flushed before every
+    timed launch when a launch moves less than twice the L2 size."""
+    import torch
+    from linear_attention_speculative_gb300 import kda
+    from linear_attention_speculative_gb300 import workloads as wk
+
+    dev = torch.device("cuda", 0)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    K = max(3, args.steps)
+    rows = []
+    sink = open(args.sweep_out, "w") if args.sweep_out else None
+    for wl in wk.sweep():
+        s = wl.shape
+        inp = wk.make_inputs_on_device(wl, dev)
+        out = {k: v for k, v in wk.empty_outputs(wl, device=dev).items()}
+        shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
+        ws = kda.alloc_workspace(shape, dev)
+        row = {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "gate": wl.gate,
+               "alg_bytes": s.algorithmic_bytes(), "head_steps": s.head_steps}
+        for variant in ("small_batch", "large_batch"):
+            def step():
+                kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"],
+                                inp["A_log"], inp["dt_bias"], inp["a"], inp["b"], inp["S0"],
+                                wl.gate, out["o"], out["inter_ssm"], out["conv_snapshots"], ws,
+                                stream=stream, variant=variant, shape=shape)
+            for _ in range(3):
+                step()
+            times = []
+            for i in range(K):
+                flush.fill_(float(i))
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+                times.append((e0, e1))
+            torch.cuda.synchronize(dev)
+            ms = sorted(a.elapsed_time(b) for a, b in times)[len(times) // 2]
+            row[variant + "_us"] = 1e3 * ms
+            row[variant + "_gbs"] = s.algorithmic_bytes() / (ms / 1e3) / 1e9
+        plan = kda.make_plan(shape, sms, "auto")
+        row["auto"] = {1: "small_batch", 2: "large_batch"}[plan.variant]
+        row["best"] = min(("small_batch", "large_batch"), key=lambda v: row[v + "_us"])
+        row["auto_over_best"] = row[row["auto"] + "_us"] / row[row["best"] + "_us"]
+        rows.append(row)
+        if sink:
+            sink.write(json.dumps(row) + "\n")
+            sink.flush()
+        print(f"{wl.name:40s} small {row['small_batch_us']:9.1f} us  large "
+              f"{row['large_batch_us']:9.1f} us  auto={row['auto']:11s} "
+              f"x{row['auto_over_best']:.3f}  {row[row['best'] + '_gbs']:7.0f} GB/s", flush=True)
+        del inp, out, ws
+        torch.cuda.empty_cache()
+    worst = max(rows, key=lambda r: r["auto_over_best"])
+    print(json.dumps({"sweep_points": len(rows), "worst_auto_over_best": worst["auto_over_best"],
+                      "worst_point": worst["workload"]}))
+
+
 def main():
     args = parse()
+    if args.sweep:
+        run_sweep(args)
+        return
     wl = workload(args.workload)
+    if args.N:
+        import dataclasses
+        sh = dataclasses.replace(wl.shape, N=args.N)
+        wl = dataclasses.replace(wl, shape=sh, name=f"{wl.name}_as_N{args.N}")
     if args.impl == "reference":
         run_reference(args, wl)
     else:

@@ -197,6 +197,40 @@ def make_inputs(wl: Workload, device: str = "cpu") -> Dict[str, Optional[torch.T
     return out
 
 
+def make_inputs_on_device(wl: Workload, device) -> Dict[str, Optional[torch.Tensor]]:
+    """Inputs with the same shapes, dtypes and distributions drawn directly on
+    `device` by its own seeded generator: fast for large timing-only runs, but
+    the values differ from `make_inputs` (never use them for parity)."""
+    s = wl.shape
+    g = torch.Generator(device=device)
+    g.manual_seed(wl.seed)
+    act = s.torch_act
+    f32 = dict(generator=g, dtype=torch.float32, device=device)
+
+    def uni(shape, lo, hi):
+        return torch.rand(shape, **f32).mul_(hi - lo).add_(lo)
+
+    out: Dict[str, Optional[torch.Tensor]] = {
+        "mixed_qkv": torch.randn((s.N, s.T, s.dim), **f32).to(act),
+        "conv_state": torch.randn((s.N, s.dim, s.W - 1), **f32).to(act),
+        "conv_w": uni((s.dim, s.W), -0.5, 0.5).to(act),
+    }
+    shape = (s.N, s.T, s.HV, s.K)
+    a = (torch.randn(shape, **f32).mul_(wl.a_dist[1]) if wl.a_dist[0] == "normal"
+         else uni(shape, wl.a_dist[1], wl.a_dist[2]))
+    if wl.plant:
+        flat = a.view(-1)
+        for j, val in enumerate(wl.plant):
+            flat[j * (wl.plant_stride // max(1, len(wl.plant)))::wl.plant_stride] = val
+    out["a"] = a.to(act)
+    out["b"] = torch.randn((s.N, s.T, s.HV), **f32).to(act)
+    out["S0"] = torch.randn((s.N, s.HV, s.K, s.V), **f32).mul_(wl.s0_std)
+    sp = wl.gate == GATE_SOFTPLUS
+    out["A_log"] = uni((s.HV,), 0.0, math.log(16.0)) if sp else None
+    out["dt_bias"] = uni((s.HV, s.K), -1.0, 1.0) if sp else None
+    return out
+
+
 def empty_outputs(wl: Workload, device: str = "cpu") -> Dict[str, torch.Tensor]:
     """Uninitialised output buffers of the right shapes and dtypes."""
     s = wl.shape

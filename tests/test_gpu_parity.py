@@ -252,3 +252,19 @@ def test_rejects_bad_args_on_device():
                         inp["dt_bias"], inp["a"], inp["b"], inp["S0"].view(-1)[1:], "softplus",
                         o, st, sn, ws, shape=shape)
     assert e.value.code == -4
+
+
+def _sweep_sample():
+    pts = list(wk.sweep())
+    pick = pts[::13] + [pts[-1], pts[-2]]  # spread + the largest points (N=512, T=8, HV=64)
+    return pick
+
+
+@pytest.mark.parametrize("wl", _sweep_sample(), ids=lambda w: w.name)
+def test_parity_sweep_points(wl):
+    inp = wk.make_inputs(wl)
+    seqs = _sample(wl.shape.N, k=2, seed=wl.seed) if wl.shape.N > 8 else None
+    ref = oracle.verify(inp, wl.gate, seqs=seqs, threads=8)
+    out, cs = run_kernel(inp, wl.gate, "auto")
+    assert_parity(out, cs, ref, seqs=seqs)
+    conv_window_properties(inp, out, cs)
