@@ -79,6 +79,8 @@ typedef struct {
 #define KDA_ERR_GATE (-7)        /* unknown gate mode, or softplus without A_log/dt_bias */
 #define KDA_ERR_VARIANT (-8)     /* unknown variant */
 #define KDA_ERR_DEVICE (-9)      /* device query or driver entry point failed */
+#define KDA_ERR_SCRATCH_LIMIT (-10) /* kda_conv_verify_noalloc: the shape needs more
+                                       scratch than the built-in array holds */
 
 /* Device status bits, written into the workspace by a kernel that gave up a
  * bounded wait (the kernel then returns without hanging the GPU). */
@@ -122,6 +124,29 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
                             kda_gate_mode gate_mode, void* o, float* inter_ssm,
                             void* conv_snapshots, void* workspace, size_t workspace_bytes,
                             kda_variant variant, kda_stream_t stream);
+
+/* Allocation-free variant of kda_conv_verify.  The verify-decode page has no
+ * counterpart: this entry point exists for callers that cannot allocate
+ * device memory -- a plugin given only its input and output buffers, a
+ * serving loop whose memory pool is fixed after start-up, code that must not
+ * call cudaMalloc (it synchronises the device and can fail under a memory
+ * cap).  Arguments are those of kda_conv_verify without the workspace: the
+ * scratch (arrival counters) lives in a static device array of
+ * KDA_NOALLOC_MAX_SCRATCH_BYTES inside the library, held on every GPU that
+ * loads the library until the process exits.  A shape whose
+ * kda_workspace_bytes() exceeds that size is rejected with
+ * KDA_ERR_SCRATCH_LIMIT (N*H up to 65532 fits).  The first call on a device,
+ * with that device current, looks up the array's device address; make it
+ * before any stream capture.  Each call clears the counters it needs on
+ * `stream`, then launches the same kernel as kda_conv_verify; it never
+ * allocates or frees.  All calls share the one array: calls whose kernels
+ * overlap on the GPU race and must be serialised by the caller. */
+#define KDA_NOALLOC_MAX_SCRATCH_BYTES (256 * 1024)
+int kda_conv_verify_noalloc(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                            void* conv_state, const float* A_log, const float* dt_bias,
+                            const void* a, const void* b, const float* S0,
+                            kda_gate_mode gate_mode, void* o, float* inter_ssm,
+                            void* conv_snapshots, kda_stream_t stream);
 
 /* Bytes of workspace a call with shape `s` needs (arrival counters for the
  * shared q/k conv_state write-back, N*H int32, plus a status word), rounded

@@ -1,8 +1,9 @@
 """Build the CUDA library (sm_103a) in-tree with nvcc.
 
-Three translation units are compiled in parallel (the C ABI and one unit per
-activation type) and linked into ``_lib/libkda_gb300.so``.  The shared CUDA
-runtime is used so the library and PyTorch share one runtime instance.
+Four translation units are compiled in parallel (the C ABI, one unit per
+activation type, and the allocation-free entry point) and linked into
+``_lib/libkda_gb300.so``.  The shared CUDA runtime is used so the library and
+PyTorch share one runtime instance.
 """
 
 from __future__ import annotations
@@ -18,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(LIB_DIR, "obj")
 LIB_PATH = os.path.join(LIB_DIR, "libkda_gb300.so")
-SOURCES = ("kda_api.cu", "kda_inst_bf16.cu", "kda_inst_f32.cu")
+SOURCES = ("kda_api.cu", "kda_inst_bf16.cu", "kda_inst_f32.cu", "kda_noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -278,6 +278,8 @@ const char* kda_strerror(int code) {
     case KDA_ERR_GATE: return "unknown gate mode, or softplus gate without A_log/dt_bias";
     case KDA_ERR_VARIANT: return "unknown kernel variant";
     case KDA_ERR_DEVICE: return "device query or driver entry point failed";
+    case KDA_ERR_SCRATCH_LIMIT:
+      return "shape needs more scratch than the no-alloc entry point's built-in array holds";
     default: break;
   }
   if (code > 0) return cudaGetErrorString(static_cast<cudaError_t>(code));

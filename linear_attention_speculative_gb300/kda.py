@@ -28,8 +28,10 @@ BF16 = 1
 MAX_T = 16
 
 # The names declared in include/kda_verify.h.
-EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_workspace_bytes",
-            "kda_make_plan", "kda_read_status", "kda_strerror", "kda_version")
+EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_noalloc",
+            "kda_workspace_bytes", "kda_make_plan", "kda_read_status", "kda_strerror",
+            "kda_version")
+NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
 
 class KdaShape(ctypes.Structure):
@@ -69,6 +71,9 @@ def _load():
     L.kda_conv_verify.argtypes = args_common + [vp]
     L.kda_conv_verify_variant.restype = ctypes.c_int
     L.kda_conv_verify_variant.argtypes = args_common + [ctypes.c_int, vp]
+    L.kda_conv_verify_noalloc.restype = ctypes.c_int
+    L.kda_conv_verify_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
+                                          vp, vp, vp, vp]
     L.kda_workspace_bytes.restype = sz
     L.kda_workspace_bytes.argtypes = [sp]
     L.kda_make_plan.restype = ctypes.c_int
@@ -151,6 +156,22 @@ def conv_verify(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: s
         VARIANTS[variant], _stream_handle(stream))
     if rc != 0:
         raise KdaError(rc)
+
+
+def conv_verify_noalloc(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: str,
+                        o, inter_ssm, conv_snapshots, stream=None,
+                        shape: Optional[KdaShape] = None) -> None:
+    """The allocation-free entry point: no workspace argument, the scratch is
+    the library's built-in device array (calls must not overlap on the GPU)."""
+    if shape is None:
+        shape = shape_of(mixed_qkv, a, S0)
+    gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
+    rc = lib().kda_conv_verify_noalloc(
+        ctypes.byref(shape), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_state), _ptr(A_log),
+        _ptr(dt_bias), _ptr(a), _ptr(b), _ptr(S0), gm, _ptr(o), _ptr(inter_ssm),
+        _ptr(conv_snapshots), _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_conv_verify_noalloc")
 
 
 def read_status(shape: KdaShape, workspace: torch.Tensor, stream=None) -> int:
