@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="large_bf16_n256_t4_h32")
     ap.add_argument("--variant", default="auto")
+    ap.add_argument("--plan", default="",
+                    help="explicit launch plan, e.g. small:32 or large:64 (overrides --variant)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--scaling", default="weak", choices=["weak", "strong"],
@@ -58,6 +60,8 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the T x N x heads x gate sweep in both variants")
     ap.add_argument("--sweep-out", default="")
+    ap.add_argument("--sweep-plans", default="auto,small:16,small:32,small:64,small:128,large:64",
+                    help="plans timed at every sweep point")
     return ap.parse_args()
 
 
@@ -277,7 +281,7 @@ def run_ours(args, wl):
         kda.conv_verify(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"], x["dt_bias"],
                         x["a"], x["b"], x["S0"], wl.gate, out["o"], out["inter_ssm"],
                         out["conv_snapshots"], ws, stream=stream, variant=args.variant,
-                        shape=shape)
+                        shape=shape, plan=args.plan or None)
 
     def barrier():
         if world > 1:
@@ -362,6 +366,8 @@ def run_ours(args, wl):
     achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
     plan = kda.make_plan(shape, torch.cuda.get_device_properties(dev).multi_processor_count,
                          args.variant)
+    if args.plan:
+        plan = kda.parse_plan(args.plan)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -369,7 +375,7 @@ def run_ours(args, wl):
         "config": {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "K": s.K,
                    "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
                    "variant": {1: "small_batch", 2: "large_batch"}[plan.variant],
-                   "grid": plan.grid, "warps_per_cta": plan.warps,
+                   "v_tile": plan.bv, "plan": args.plan or "auto",
                    "l2": ("L2 flushed between steps (256 MB write)" if flush_l2 else
                           f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB moved per step"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
@@ -377,7 +383,7 @@ def run_ours(args, wl):
                      "frac": achieved / peak, "traffic": ncu_traffic(wl.name),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
-                     "kernel": "kda_verify_kernel"},
+                     "kernel": "kda_ws_kernel" if plan.variant == 2 else "kda_tile_kernel"},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": E},
         "gpu_launches": K,
@@ -391,10 +397,14 @@ def run_ours(args, wl):
         dist.destroy_process_group()
 
 
+def plan_label(plan) -> str:
+    return f"{'large' if plan.variant == 2 else 'small'}:{plan.bv}"
+
+
 def run_sweep(args):
-    """Time each sweep point in both variants and the dispatcher's pick.
-    Inputs are drawn on the device (timing only); L2 is flushed before every
-    timed launch when a launch moves less than twice the L2 size."""
+    """Time each sweep point with every plan of --sweep-plans ("auto" = the
+    dispatcher's pick).  Inputs are drawn on the device (timing only); L2 is
+    flushed before every timed launch.  Median of --steps launches."""
     import torch
     from linear_attention_speculative_gb300 import kda
     from linear_attention_speculative_gb300 import workloads as wk
@@ -404,6 +414,7 @@ def run_sweep(args):
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     K = max(3, args.steps)
+    plans = [p for p in args.sweep_plans.split(",") if p]
     rows = []
     sink = open(args.sweep_out, "w") if args.sweep_out else None
     for wl in wk.sweep():
@@ -412,14 +423,18 @@ def run_sweep(args):
         out = {k: v for k, v in wk.empty_outputs(wl, device=dev).items()}
         shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
         ws = kda.alloc_workspace(shape, dev)
+        auto = plan_label(kda.make_plan(shape, sms, "auto"))
         row = {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "gate": wl.gate,
-               "alg_bytes": s.algorithmic_bytes(), "head_steps": s.head_steps}
-        for variant in ("small_batch", "large_batch"):
+               "alg_bytes": s.algorithmic_bytes(), "head_steps": s.head_steps, "auto": auto,
+               "us": {}}
+        for spec in plans:
+            plan = None if spec == "auto" else spec
+
             def step():
                 kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"],
                                 inp["A_log"], inp["dt_bias"], inp["a"], inp["b"], inp["S0"],
                                 wl.gate, out["o"], out["inter_ssm"], out["conv_snapshots"], ws,
-                                stream=stream, variant=variant, shape=shape)
+                                stream=stream, shape=shape, plan=plan)
             for _ in range(3):
                 step()
             times = []
@@ -432,25 +447,27 @@ def run_sweep(args):
                 e1.record(stream)
                 times.append((e0, e1))
             torch.cuda.synchronize(dev)
-            ms = sorted(a.elapsed_time(b) for a, b in times)[len(times) // 2]
-            row[variant + "_us"] = 1e3 * ms
-            row[variant + "_gbs"] = s.algorithmic_bytes() / (ms / 1e3) / 1e9
-        plan = kda.make_plan(shape, sms, "auto")
-        row["auto"] = {1: "small_batch", 2: "large_batch"}[plan.variant]
-        row["best"] = min(("small_batch", "large_batch"), key=lambda v: row[v + "_us"])
-        row["auto_over_best"] = row[row["auto"] + "_us"] / row[row["best"] + "_us"]
+            row["us"][spec] = 1e3 * sorted(a.elapsed_time(b) for a, b in times)[len(times) // 2]
+        explicit = {k: v for k, v in row["us"].items() if k != "auto"}
+        best = min(explicit, key=explicit.get) if explicit else "auto"
+        row["best"] = best
+        row["best_gbs"] = s.algorithmic_bytes() / (row["us"][best] / 1e6) / 1e9
+        if "auto" in row["us"]:
+            row["auto_over_best"] = row["us"]["auto"] / row["us"][best]
         rows.append(row)
         if sink:
             sink.write(json.dumps(row) + "\n")
             sink.flush()
-        print(f"{wl.name:40s} small {row['small_batch_us']:9.1f} us  large "
-              f"{row['large_batch_us']:9.1f} us  auto={row['auto']:11s} "
-              f"x{row['auto_over_best']:.3f}  {row[row['best'] + '_gbs']:7.0f} GB/s", flush=True)
+        cols = "  ".join(f"{k} {v:8.1f}" for k, v in row["us"].items())
+        print(f"{wl.name:38s} {cols}  auto={auto} best={best} "
+              f"x{row.get('auto_over_best', 1.0):.3f} {row['best_gbs']:6.0f} GB/s", flush=True)
         del inp, out, ws
         torch.cuda.empty_cache()
-    worst = max(rows, key=lambda r: r["auto_over_best"])
-    print(json.dumps({"sweep_points": len(rows), "worst_auto_over_best": worst["auto_over_best"],
-                      "worst_point": worst["workload"]}))
+    if rows and "auto_over_best" in rows[0]:
+        worst = max(rows, key=lambda r: r["auto_over_best"])
+        print(json.dumps({"sweep_points": len(rows),
+                          "worst_auto_over_best": worst["auto_over_best"],
+                          "worst_point": worst["workload"]}))
 
 
 def main():

@@ -168,6 +168,19 @@ typedef struct {
 } kda_plan;
 int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
 
+/* Same as kda_conv_verify with an explicit launch plan, e.g. one returned by
+ * kda_make_plan and then edited.  Read from `plan`: variant (SMALL_BATCH or
+ * LARGE_BATCH), bv (v-tile width: 16, 32, 64 or 128 for SMALL_BATCH; 32, 64
+ * or 128 for LARGE_BATCH; at most V and dividing V) and, for LARGE_BATCH,
+ * grid (persistent CTAs; <= 0 picks the default).  The other fields are
+ * recomputed.  An invalid plan returns KDA_ERR_VARIANT.  Every plan produces
+ * bit-identical outputs. */
+int kda_conv_verify_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                         void* conv_state, const float* A_log, const float* dt_bias,
+                         const void* a, const void* b, const float* S0, kda_gate_mode gate_mode,
+                         void* o, float* inter_ssm, void* conv_snapshots, void* workspace,
+                         size_t workspace_bytes, const kda_plan* plan, kda_stream_t stream);
+
 /* Synchronously read (and clear) the device status word of `workspace` on
  * `stream`.  *status receives KDA_STATUS_* bits.  Returns 0 or an error. */
 int kda_read_status(const kda_shape* s, void* workspace, int* status, kda_stream_t stream);

@@ -1,7 +1,7 @@
 """Build the CUDA library (sm_103a) in-tree with nvcc.
 
-Four translation units are compiled in parallel (the C ABI, one unit per
-activation type, and the allocation-free entry point) and linked into
+Six translation units are compiled in parallel (the C ABI, one unit per
+kernel and activation type, and the allocation-free entry point) and linked into
 ``_lib/libkda_gb300.so``.  The shared CUDA runtime is used so the library and
 PyTorch share one runtime instance.
 """
@@ -19,7 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(LIB_DIR, "obj")
 LIB_PATH = os.path.join(LIB_DIR, "libkda_gb300.so")
-SOURCES = ("kda_api.cu", "kda_inst_bf16.cu", "kda_inst_f32.cu", "kda_noalloc.cu")
+SOURCES = ("kda_api.cu", "kda_inst_tile_bf16.cu", "kda_inst_tile_f32.cu", "kda_inst_ws_bf16.cu",
+           "kda_inst_ws_f32.cu", "kda_noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

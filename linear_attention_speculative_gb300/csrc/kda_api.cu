@@ -37,10 +37,33 @@ int check_shape(const kda_shape* s) {
 
 size_t act_bytes(const kda_shape* s) { return s->act == KDA_F32 ? 4 : 2; }
 
-int ctas_per_sm_for(int warps, size_t smem) {
-  const int by_regs = 16 / warps;  // launch bounds cap registers at 128/thread
+int ctas_per_sm_for(int regs_limit, size_t smem) {
   const int by_smem = (int)(kSmemPerSm / (smem + kSmemReservedPerCta));
-  return std::max(1, std::min(by_regs, by_smem));
+  return std::max(1, std::min(regs_limit, by_smem));
+}
+
+bool valid_tile_bv(int bv, int V) { return (bv == 16 || bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
+bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
+
+// Fill the derived fields of a plan whose variant and bv are set.
+void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_grid) {
+  const long long units = (long long)s->N * s->HV;
+  const int ab = s->act == KDA_F32 ? 4 : 2;
+  out->items = units * (s->V / out->bv);
+  if (out->variant == KDA_VARIANT_LARGE_BATCH) {
+    out->warps = out->bv / 16;
+    const size_t smem = kda::ws_smem_bytes(s->T, s->K, out->bv, ab);
+    out->ctas_per_sm = ctas_per_sm_for(kda::ws_min_blocks(out->warps), smem);
+    const long long cap = (long long)num_sms * out->ctas_per_sm;
+    long long grid = requested_grid > 0 ? requested_grid : cap;
+    out->grid = (int)std::max(1LL, std::min(out->items, grid));
+  } else {
+    out->warps = out->bv / 16;
+    const size_t smem = kda::tile_smem_bytes(s->T, s->K, out->bv);
+    out->ctas_per_sm = ctas_per_sm_for(16 / out->warps, smem);
+    out->grid = (int)std::max(1LL, out->items);
+  }
+  if (units == 0) out->grid = 0;
 }
 
 struct Span {
@@ -104,49 +127,38 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
       variant != KDA_VARIANT_LARGE_BATCH)
     return KDA_ERR_VARIANT;
   const long long units = (long long)s->N * s->HV;
-  kda_variant v = variant;
-  if (v == KDA_VARIANT_AUTO) {
-    // Large batch once every SM gets at least two whole (n, hv) units; below
-    // that, split V across CTAs to put more SMs to work.
-    v = units >= 2LL * num_sms ? KDA_VARIANT_LARGE_BATCH : KDA_VARIANT_SMALL_BATCH;
-  }
   std::memset(out, 0, sizeof(*out));
-  out->variant = v;
-  if (v == KDA_VARIANT_LARGE_BATCH) {
-    out->bv = s->V;
-    out->warps = s->V / 16;
-    const size_t smem = kda::smem_bytes(s->T, s->K, out->bv, 2);
-    out->ctas_per_sm = ctas_per_sm_for(out->warps, smem);
-    out->items = units;
-    const long long cap = (long long)num_sms * out->ctas_per_sm;
-    out->grid = (int)std::max(1LL, std::min(units, cap));
+  if (variant == KDA_VARIANT_LARGE_BATCH) {
+    out->variant = KDA_VARIANT_LARGE_BATCH;
+    out->bv = s->V >= 64 ? 64 : s->V;
   } else {
-    int bv = 32;
-    if (units * (s->V / 32) < 4LL * num_sms) bv = 16;
-    out->bv = bv;
-    out->warps = bv / 16;
-    const size_t smem = kda::smem_bytes(s->T, s->K, bv, 1);
-    out->ctas_per_sm = ctas_per_sm_for(out->warps, smem);
-    out->items = units * (s->V / bv);
-    out->grid = (int)std::max(1LL, out->items);
+    // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
+    // many threads for its producer tasks and the q/k conv is not repeated per
+    // v-tile.  Measured on GB300 over the 150-point sweep, half states
+    // (BV = 64) are a few per cent faster only for T <= 3 once every SM has
+    // several units.
+    out->variant = KDA_VARIANT_SMALL_BATCH;
+    out->bv = std::min(s->V, 128);
+    if (s->T <= 3 && units >= 4LL * num_sms && s->V >= 64) out->bv = 64;
   }
-  if (units == 0) out->grid = 0;
+  finish_plan(s, num_sms, out, 0);
   return KDA_OK;
 }
 
-int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
-                            void* conv_state, const float* A_log, const float* dt_bias,
-                            const void* a, const void* b, const float* S0,
-                            kda_gate_mode gate_mode, void* o, float* inter_ssm,
-                            void* conv_snapshots, void* workspace, size_t workspace_bytes,
-                            kda_variant variant, kda_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Every host-side check of one call (nothing touches the GPU).
+int validate_call(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                  void* conv_state, const float* A_log, const float* dt_bias, const void* a,
+                  const void* b, const float* S0, kda_gate_mode gate_mode, void* o,
+                  float* inter_ssm, void* conv_snapshots, void* workspace,
+                  size_t workspace_bytes) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (gate_mode != KDA_GATE_SOFTPLUS && gate_mode != KDA_GATE_SAFE) return KDA_ERR_GATE;
-  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
-      variant != KDA_VARIANT_LARGE_BATCH)
-    return KDA_ERR_VARIANT;
-  if (s->N == 0) return KDA_OK;  // nothing to do
+  if (s->N == 0) return KDA_OK;
   if (!mixed_qkv || !conv_w || !conv_state || !a || !b || !S0 || !o || !inter_ssm ||
       !conv_snapshots)
     return KDA_ERR_NULL;
@@ -185,14 +197,17 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
     for (size_t j = 0; j < sizeof(wr) / sizeof(wr[0]); ++j)
       if (j != i && overlap(wr[i], wr[j])) return KDA_ERR_ALIAS;
   }
+  return KDA_OK;
+}
 
-  int num_sms = 0;
-  rc = num_sms_of_current_device(&num_sms);
-  if (rc) return rc;
-  kda_plan plan;
-  rc = kda_make_plan(s, num_sms, variant, &plan);
-  if (rc) return rc;
-
+// Encode the state tensor map and launch the kernel of `plan`.
+int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, void* conv_state,
+                const float* A_log, const float* dt_bias, const void* a, const void* b,
+                const float* S0, kda_gate_mode gate_mode, void* o, float* inter_ssm,
+                void* conv_snapshots, void* workspace, const kda_plan& plan,
+                kda_stream_t stream) {
+  const size_t N = s->N, H = s->H, HV = s->HV, K = s->K, V = s->V;
+  const size_t dim = 2 * H * K + HV * V;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return KDA_ERR_DEVICE;
   CUtensorMap tmap;
@@ -234,13 +249,70 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
   LaunchCfg cfg;
   cfg.K = s->K;
   cfg.warps = plan.warps;
-  cfg.persist = plan.variant == KDA_VARIANT_LARGE_BATCH;
+  cfg.ws = plan.variant == KDA_VARIANT_LARGE_BATCH;
   cfg.grid = plan.grid;
-  cfg.smem = kda::smem_bytes(s->T, s->K, plan.bv, cfg.persist ? 2 : 1);
+  const int ab = s->act == KDA_F32 ? 4 : 2;
+  cfg.smem = cfg.ws ? kda::ws_smem_bytes(s->T, s->K, plan.bv, ab)
+                    : kda::tile_smem_bytes(s->T, s->K, plan.bv);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  rc = s->act == KDA_BF16 ? kda::launch_bf16(tmap, p, cfg, st) : kda::launch_f32(tmap, p, cfg, st);
+  int rc;
+  if (s->act == KDA_BF16)
+    rc = cfg.ws ? kda::launch_ws_bf16(tmap, p, cfg, st) : kda::launch_tile_bf16(tmap, p, cfg, st);
+  else
+    rc = cfg.ws ? kda::launch_ws_f32(tmap, p, cfg, st) : kda::launch_tile_f32(tmap, p, cfg, st);
   if (rc < 0) return KDA_ERR_SHAPE;
   return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                            void* conv_state, const float* A_log, const float* dt_bias,
+                            const void* a, const void* b, const float* S0,
+                            kda_gate_mode gate_mode, void* o, float* inter_ssm,
+                            void* conv_snapshots, void* workspace, size_t workspace_bytes,
+                            kda_variant variant, kda_stream_t stream) {
+  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
+      variant != KDA_VARIANT_LARGE_BATCH)
+    return KDA_ERR_VARIANT;
+  int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
+                         o, inter_ssm, conv_snapshots, workspace, workspace_bytes);
+  if (rc || s->N == 0) return rc;
+  int num_sms = 0;
+  rc = num_sms_of_current_device(&num_sms);
+  if (rc) return rc;
+  kda_plan plan;
+  rc = kda_make_plan(s, num_sms, variant, &plan);
+  if (rc) return rc;
+  return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
+                     inter_ssm, conv_snapshots, workspace, plan, stream);
+}
+
+int kda_conv_verify_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
+                         void* conv_state, const float* A_log, const float* dt_bias,
+                         const void* a, const void* b, const float* S0, kda_gate_mode gate_mode,
+                         void* o, float* inter_ssm, void* conv_snapshots, void* workspace,
+                         size_t workspace_bytes, const kda_plan* plan, kda_stream_t stream) {
+  if (!plan) return KDA_ERR_NULL;
+  int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
+                         o, inter_ssm, conv_snapshots, workspace, workspace_bytes);
+  if (rc || s->N == 0) return rc;
+  if (plan->variant == KDA_VARIANT_SMALL_BATCH) {
+    if (!valid_tile_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
+  } else if (plan->variant == KDA_VARIANT_LARGE_BATCH) {
+    if (!valid_ws_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
+  } else {
+    return KDA_ERR_VARIANT;
+  }
+  int num_sms = 0;
+  rc = num_sms_of_current_device(&num_sms);
+  if (rc) return rc;
+  kda_plan p = *plan;
+  finish_plan(s, num_sms, &p, plan->grid);
+  return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
+                     inter_ssm, conv_snapshots, workspace, p, stream);
 }
 
 int kda_conv_verify(const kda_shape* s, const void* mixed_qkv, const void* conv_w,

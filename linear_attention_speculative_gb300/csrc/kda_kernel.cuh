@@ -1,19 +1,17 @@
-// kda_kernel.cuh -- the fused causal-conv1d + KDA verify-decode kernel for
+// kda_kernel.cuh -- the fused causal-conv1d + KDA verify-decode kernels for
 // sm_103a ("[KDA] Fuse causal conv1d into MTP verify decode", cuLA pull
 // request 107).
 //
 // Work item: (sequence n, value head hv, v-tile vt) = a K x BV slice of one
-// recurrent state.  A CTA of WARPS warps owns BV = 16 * WARPS columns.
+// recurrent state, BV = 16 * (consumer warps).
 //
 //   producer  conv1d(W=4) + SiLU of the q/k channels of head h = hv / G and of
-//             the tile's v channels for all T tokens, q/k L2 norm (q scaled by
-//             K^-1/2), alpha = exp(g) and beta, staged in shared memory; the
-//             raw conv windows are streamed out as snapshots.  All global
-//             loads are 16-byte vectors.
+//             the tile's v channels, one task per (8-channel vector, token);
+//             q/k L2 norm (q scaled by K^-1/2), alpha = exp(g) and beta,
+//             staged in shared memory; the raw conv windows are streamed out
+//             as snapshots and the conv_state is rolled.
 //   state     the item's S0 slice arrives in shared memory by one 2-D TMA
-//             tile load (mbarrier completion); in the persistent variant the
-//             next item's tile is requested as soon as the current one has
-//             moved to registers, so the load overlaps the recurrence.
+//             tile load (mbarrier completion), then moves to registers.
 //   consumer  every warp owns 16 columns; lane = (row group rg in 0..7,
 //             column quad cg in 0..3) keeps rows [rg*K/8, (rg+1)*K/8) x 4
 //             columns of S in registers.  Per token: decay + S^T k partial
@@ -21,15 +19,24 @@
 //             update fused with the S^T q partial sums and the 16-byte
 //             streaming store of the snapshot, a second butterfly, o.
 //
-// Both variants (one item per CTA, or persistent CTAs) run the same
-// producer/consumer code with the same per-warp layout, hence the same
-// floating-point operation order: their outputs are bit-identical.
+// Two kernels run that same producer arithmetic and consumer code:
+//   kda_tile_kernel  one item per CTA; every warp produces, then consumes.
+//                    The hardware block scheduler keeps several CTAs in
+//                    different phases on every SM.
+//   kda_ws_kernel    persistent and warp-specialised: one producer warp
+//                    stages the NEXT item -- its raw inputs arrive by 1-D
+//                    bulk TMA copies, its state tile by a 2-D TMA load as soon
+//                    as the consumers have moved the current tile to
+//                    registers -- while the consumer warps stream the
+//                    recurrence of the current item.  Full/empty mbarriers
+//                    hand stages and tiles over; every wait is bounded.
+// Same floating-point operations in the same order => bit-identical outputs.
 //
 // Shared q/k conv_state write-back: the q/k channels of group (n, h) are read
 // by G * (V / BV) items.  Each item arrives on a per-group counter after its
 // reads; the last arrival rolls the group's q/k conv_state and resets the
 // counter to zero.  Nothing ever waits on another CTA.  v channels belong to
-// exactly one item, which rolls them right after reading them.
+// exactly one item, which rolls them itself.
 #pragma once
 
 #include "kda_device.cuh"
@@ -57,16 +64,31 @@ struct Params {
 constexpr int kConvW = 4;
 constexpr float kL2Eps = 1e-6f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kStatusTmaTimeout = 1;              // KDA_STATUS_TMA_TIMEOUT
 
 __host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
+__host__ __device__ constexpr size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
 
 // floats of one stage: q[T][K], k[T][K], alpha[T][K], v[T][BV], beta[round4(T)]
 __host__ __device__ constexpr int stage_floats(int T, int K, int BV) {
   return 3 * T * K + T * BV + round4(T);
 }
 
-__host__ __device__ constexpr size_t smem_bytes(int T, int K, int BV, int nstage) {
-  return 128 + sizeof(float) * (size_t)K * BV + sizeof(float) * (size_t)nstage * stage_floats(T, K, BV);
+// raw-input bytes of one item (warp-specialised kernel): x_q, x_k [T][K],
+// x_v [T][BV], conv_state blocks [C][3], conv_w blocks [C][4] (C = 2K + BV
+// channels), a [T][K], dt_bias [K] fp32.
+__host__ __device__ constexpr size_t raw_bytes(int T, int K, int BV, int ab) {
+  return (size_t)ab * ((size_t)T * (2 * K + BV) + (size_t)(2 * K + BV) * 7 + (size_t)T * K) +
+         4 * (size_t)K;
+}
+
+// dynamic shared memory of the two kernels
+__host__ __device__ constexpr size_t tile_smem_bytes(int T, int K, int BV) {
+  return 128 + sizeof(float) * ((size_t)K * BV + stage_floats(T, K, BV));
+}
+__host__ __device__ constexpr size_t ws_smem_bytes(int T, int K, int BV, int ab) {
+  return 128 + sizeof(float) * ((size_t)K * BV + 2 * (size_t)stage_floats(T, K, BV)) +
+         round16(raw_bytes(T, K, BV, ab));
 }
 
 struct Item {
@@ -84,234 +106,260 @@ __device__ __forceinline__ Item decode_item(const Params& p, long long item) {
   return it;
 }
 
+// First channel (within dim) of a block: kind 0 = q of head h, 1 = k of head
+// h, 2 = the item's v tile.
+template <int K, int BV>
+__device__ __forceinline__ int block_channel(const Params& p, const Item& it, int kind) {
+  return kind == 0 ? it.h * K
+                   : (kind == 1 ? p.H * K + it.h * K : 2 * p.H * K + it.hv * p.V + it.vt * BV);
+}
+
 // ---------------------------------------------------------------------------
-// producer phase 1: conv + SiLU (q, k, v), gate, beta
+// where a producer task reads its raw inputs from; e0 = first channel of an
+// 8-(bf16) / 4-(fp32) channel vector within the block
 // ---------------------------------------------------------------------------
-template <typename Act, int K, int BV, int NT>
-__device__ __forceinline__ void produce_phase1(const Params& p, const Item& it, float* sQ,
-                                               float* sK, float* sA, float* sV, float* sB,
-                                               int tid) {
+
+// Straight from global memory (one-item-per-CTA kernel).
+template <typename Act, int K, int BV>
+struct GlobalSrc {
+  const Params& p;
+  const Item& it;
+  __device__ __forceinline__ uint4 x(int kind, int t, int e0) const {
+    const Act* b = static_cast<const Act*>(p.mixed_qkv) + ((size_t)it.n * p.T + t) * p.dim;
+    return ld_ro_16(b + block_channel<K, BV>(p, it, kind) + e0);
+  }
+  __device__ __forceinline__ uint4 cs(int kind, int e0, int m) const {
+    const Act* b = static_cast<const Act*>(p.conv_state) +
+                   ((size_t)it.n * p.dim + block_channel<K, BV>(p, it, kind) + e0) * (kConvW - 1);
+    return ld_rw_16(reinterpret_cast<const char*>(b) + 16 * m);
+  }
+  __device__ __forceinline__ uint4 w(int kind, int e0, int m) const {
+    const Act* b = static_cast<const Act*>(p.conv_w) +
+                   (size_t)(block_channel<K, BV>(p, it, kind) + e0) * kConvW;
+    return ld_ro_16(reinterpret_cast<const char*>(b) + 16 * m);
+  }
+  __device__ __forceinline__ uint4 a(int t, int e0) const {
+    return ld_ro_16(static_cast<const Act*>(p.a) + (((size_t)it.n * p.T + t) * p.HV + it.hv) * K + e0);
+  }
+  __device__ __forceinline__ float4 dt(int e0) const {
+    return __ldg(reinterpret_cast<const float4*>(p.dt_bias + (size_t)it.hv * K + e0));
+  }
+};
+
+// From the item's raw-input buffer in shared memory (warp-specialised kernel).
+template <typename Act, int K, int BV>
+struct SmemSrc {
+  const unsigned char* raw;
+  int T;
+  static constexpr int AB = sizeof(Act);
+  // x_q [T][K] | x_k [T][K] | x_v [T][BV] | cs [2K+BV][3] | w [2K+BV][4] | a [T][K] | dt [K]
+  __device__ __forceinline__ size_t off_x(int kind, int t) const {
+    return kind == 0 ? (size_t)t * K * AB
+                     : (kind == 1 ? (size_t)(T + t) * K * AB
+                                  : (size_t)2 * T * K * AB + (size_t)t * BV * AB);
+  }
+  __device__ __forceinline__ size_t base_cs() const { return (size_t)T * (2 * K + BV) * AB; }
+  __device__ __forceinline__ size_t base_w() const { return base_cs() + (size_t)(2 * K + BV) * 3 * AB; }
+  __device__ __forceinline__ size_t base_a() const { return base_w() + (size_t)(2 * K + BV) * 4 * AB; }
+  __device__ __forceinline__ size_t base_dt() const { return base_a() + (size_t)T * K * AB; }
+  __device__ __forceinline__ static int blk(int kind) { return kind == 0 ? 0 : (kind == 1 ? K : 2 * K); }
+  __device__ __forceinline__ uint4 x(int kind, int t, int e0) const {
+    return *reinterpret_cast<const uint4*>(raw + off_x(kind, t) + (size_t)e0 * AB);
+  }
+  __device__ __forceinline__ uint4 cs(int kind, int e0, int m) const {
+    return *reinterpret_cast<const uint4*>(raw + base_cs() + (size_t)(blk(kind) + e0) * 3 * AB + 16 * m);
+  }
+  __device__ __forceinline__ uint4 w(int kind, int e0, int m) const {
+    return *reinterpret_cast<const uint4*>(raw + base_w() + (size_t)(blk(kind) + e0) * 4 * AB + 16 * m);
+  }
+  __device__ __forceinline__ uint4 a(int t, int e0) const {
+    return *reinterpret_cast<const uint4*>(raw + base_a() + ((size_t)t * K + e0) * AB);
+  }
+  __device__ __forceinline__ float4 dt(int e0) const {
+    return *reinterpret_cast<const float4*>(raw + base_dt() + (size_t)e0 * 4);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// producer arithmetic (shared by both kernels)
+// ---------------------------------------------------------------------------
+
+// Select x_ext[idx] (idx < 3: the old state) with compile-time register
+// indices only.
+template <typename Raw, int VEC>
+__device__ __forceinline__ void select_state(const Raw (&cs)[3 * VEC], int idx, Raw (&out)[VEC]) {
+#pragma unroll
+  for (int jj = 0; jj < kConvW - 1; ++jj)
+    if (jj == idx) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) out[e] = cs[e * (kConvW - 1) + jj];
+    }
+}
+
+// One conv task: VEC channels of block `kind` at token t.  Writes SiLU(conv)
+// to dst[e], the snapshot of token t when `snap`, and at t = T-1 the rolled
+// state of these channels when `roll`.
+template <typename Act, typename Src>
+__device__ __forceinline__ void conv_task(const Src& src, const Params& p, const Item& it,
+                                          int kind, int e0, int c, int t, float* dst, bool snap,
+                                          bool roll) {
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
-  constexpr int NQ = K / VEC;   // channel vectors per q (or k) head
-  constexpr int NVV = BV / VEC; // channel vectors of the v tile
-  constexpr int NCONV = 2 * NQ + NVV;
   const int T = p.T;
-  const int dim = p.dim;
-  const int ntask_gate = T * NQ;
-  const int ntask = NCONV + ntask_gate + T;
-  // q/k snapshots are written once per group: by its first v-head, first tile
-  const bool qk_snap_owner = (it.hv % p.G == 0) && (it.vt == 0);
-
-  const Act* xq = static_cast<const Act*>(p.mixed_qkv) + (size_t)it.n * T * dim;
-  Act* cs_base = static_cast<Act*>(p.conv_state) + (size_t)it.n * dim * (kConvW - 1);
-  Act* snap_base = static_cast<Act*>(p.conv_snapshots) + (size_t)it.n * T * dim * (kConvW - 1);
-
-  for (int task = tid; task < ntask; task += NT) {
-    if (task < NCONV) {
-      int c, kind, e0;
-      if (task < NQ) {
-        kind = 0; e0 = task * VEC; c = it.h * K + e0;
-      } else if (task < 2 * NQ) {
-        kind = 1; e0 = (task - NQ) * VEC; c = p.H * K + it.h * K + e0;
-      } else {
-        kind = 2; e0 = (task - 2 * NQ) * VEC; c = 2 * p.H * K + it.hv * p.V + it.vt * BV + e0;
-      }
-      // weights: VEC channels x 4 taps = 4 x 16 bytes
-      float wf[VEC][kConvW];
-      {
-        const char* wp = reinterpret_cast<const char*>(static_cast<const Act*>(p.conv_w) +
-                                                       (size_t)c * kConvW);
-        Raw r[4 * VEC];
+  Raw cs[3 * VEC] = {};
+  if (t < kConvW - 1) {
 #pragma unroll
-        for (int m = 0; m < 4; ++m) AT::unpack(ld_ro_16(wp + 16 * m), r + m * VEC);
+    for (int m = 0; m < 3; ++m) AT::unpack(src.cs(kind, e0, m), cs + m * VEC);
+  }
+  // window x_ext[t .. t+3]: x_ext[i] = state[i] for i < 3, else token i-3
+  Raw win[kConvW][VEC];
 #pragma unroll
-        for (int e = 0; e < VEC; ++e)
-#pragma unroll
-          for (int j = 0; j < kConvW; ++j) wf[e][j] = AT::to_f(r[e * kConvW + j]);
-      }
-      // conv window: 3 state values (oldest first) + the current token
-      Raw win[VEC][kConvW];
-      Act* csp = cs_base + (size_t)c * (kConvW - 1);
-      {
-        Raw r[3 * VEC];
-#pragma unroll
-        for (int m = 0; m < 3; ++m)
-          AT::unpack(ld_rw_16(reinterpret_cast<const char*>(csp) + 16 * m), r + m * VEC);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-#pragma unroll
-          for (int j = 0; j < kConvW - 1; ++j) win[e][j] = r[e * (kConvW - 1) + j];
-      }
-      const bool snap = (kind == 2) || qk_snap_owner;
-      float* dst = kind == 0 ? sQ + e0 : (kind == 1 ? sK + e0 : sV + e0);
-      const int dstride = kind == 2 ? BV : K;
-      uint4 xnext = ld_ro_16(xq + c);
-      for (int t = 0; t < T; ++t) {
-        const uint4 xv = xnext;
-        if (t + 1 < T) xnext = ld_ro_16(xq + (size_t)(t + 1) * dim + c);
-        {
-          Raw r[VEC];
-          AT::unpack(xv, r);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) win[e][kConvW - 1] = r[e];
-        }
-        float y[VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          float acc = __fmul_rn(wf[e][0], AT::to_f(win[e][0]));
-#pragma unroll
-          for (int j = 1; j < kConvW; ++j) acc = __fmaf_rn(wf[e][j], AT::to_f(win[e][j]), acc);
-          y[e] = silu_f(acc);
-        }
-#pragma unroll
-        for (int e = 0; e < VEC; e += 4)
-          *reinterpret_cast<float4*>(dst + t * dstride + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
-        if (snap) {
-          Raw r[3 * VEC];
-#pragma unroll
-          for (int e = 0; e < VEC; ++e)
-#pragma unroll
-            for (int j = 0; j < kConvW - 1; ++j) r[e * (kConvW - 1) + j] = win[e][j + 1];
-          char* sp = reinterpret_cast<char*>(snap_base + ((size_t)t * dim + c) * (kConvW - 1));
-#pragma unroll
-          for (int m = 0; m < 3; ++m) st_16(sp + 16 * m, AT::pack(r + m * VEC));
-        }
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-#pragma unroll
-          for (int j = 0; j < kConvW - 1; ++j) win[e][j] = win[e][j + 1];
-      }
-      if (kind == 2) {
-        // v channels are read by this item only: roll them in place now
-        Raw r[3 * VEC];
-#pragma unroll
-        for (int e = 0; e < VEC; ++e)
-#pragma unroll
-          for (int j = 0; j < kConvW - 1; ++j) r[e * (kConvW - 1) + j] = win[e][j];
-#pragma unroll
-        for (int m = 0; m < 3; ++m) st_16(reinterpret_cast<char*>(csp) + 16 * m, AT::pack(r + m * VEC));
-      }
-    } else if (task < NCONV + ntask_gate) {
-      const int g = task - NCONV;
-      const int t = g / NQ;
-      const int e0 = (g - t * NQ) * VEC;
-      const Act* ap = static_cast<const Act*>(p.a) + (((size_t)it.n * T + t) * p.HV + it.hv) * K + e0;
-      Raw r[VEC];
-      AT::unpack(ld_ro_16(ap), r);
-      float al[VEC];
-      if (p.gate_mode == 0) {
-        const float negA = -expf(__ldg(p.A_log + it.hv));
-        const float* dtp = p.dt_bias + (size_t)it.hv * K + e0;
-#pragma unroll
-        for (int e = 0; e < VEC; e += 4) {
-          const float4 d = __ldg(reinterpret_cast<const float4*>(dtp + e));
-          const float dd[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float x = __fadd_rn(AT::to_f(r[e + j]), dd[j]);
-            al[e + j] = expf(__fmul_rn(negA, softplus_f(x)));
-          }
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) al[e] = expf(fminf(AT::to_f(r[e]), 0.0f));
-      }
-#pragma unroll
-      for (int e = 0; e < VEC; e += 4)
-        *reinterpret_cast<float4*>(sA + t * K + e0 + e) = make_float4(al[e], al[e + 1], al[e + 2], al[e + 3]);
+  for (int j = 0; j < kConvW; ++j) {
+    const int idx = t + j;
+    if (idx >= kConvW - 1) {
+      AT::unpack(src.x(kind, idx - (kConvW - 1), e0), win[j]);
     } else {
-      const int t = task - NCONV - ntask_gate;
-      const Act* bp = static_cast<const Act*>(p.b) + ((size_t)it.n * T + t) * p.HV + it.hv;
-      float bv;
-      if constexpr (sizeof(Act) == 4) {
-        bv = __ldg(reinterpret_cast<const float*>(bp));
-      } else {
-        bv = AT::to_f(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(bp))));
-      }
-      sB[t] = sigmoid_f(bv);
+      select_state<Raw, VEC>(cs, idx, win[j]);
     }
   }
-}
-
-// ---------------------------------------------------------------------------
-// producer phase 2: L2 norm of q and k per token (one warp per vector)
-// ---------------------------------------------------------------------------
-template <int K, int WARPS>
-__device__ __forceinline__ void produce_phase2(int T, float* sQ, float* sK, int warp, int lane) {
-  const float scale = rsqrtf(static_cast<float>(K));
-  for (int r = warp; r < 2 * T; r += WARPS) {
-    float* x = r < T ? sQ + r * K : sK + (r - T) * K;
-    float xs[K / 32];
-    float ss = 0.0f;
+  Raw wr[4 * VEC];
 #pragma unroll
-    for (int m = 0; m < K / 32; ++m) {
-      xs[m] = x[lane + 32 * m];
-      ss = __fmaf_rn(xs[m], xs[m], ss);
-    }
+  for (int m = 0; m < 4; ++m) AT::unpack(src.w(kind, e0, m), wr + m * VEC);
+  float y[VEC];
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
-    float inv = rsqrtf(__fadd_rn(ss, kL2Eps));
-    if (r < T) inv = __fmul_rn(inv, scale);
+  for (int e = 0; e < VEC; ++e) {
+    float acc = __fmul_rn(AT::to_f(wr[e * kConvW]), AT::to_f(win[0][e]));
 #pragma unroll
-    for (int m = 0; m < K / 32; ++m) x[lane + 32 * m] = __fmul_rn(xs[m], inv);
+    for (int j = 1; j < kConvW; ++j) acc = __fmaf_rn(AT::to_f(wr[e * kConvW + j]), AT::to_f(win[j][e]), acc);
+    y[e] = silu_f(acc);
   }
-}
-
-// ---------------------------------------------------------------------------
-// last arrival of a q/k group rolls the group's q/k conv_state
-// ---------------------------------------------------------------------------
-template <typename Act, int K, int NT>
-__device__ __forceinline__ void roll_qk(const Params& p, const Item& it, int tid) {
-  using AT = ActT<Act>;
-  using Raw = typename AT::Raw;
-  constexpr int VEC = AT::VEC;
-  constexpr int NQ = K / VEC;
-  const int T = p.T;
-  const int dim = p.dim;
-  const Act* xq = static_cast<const Act*>(p.mixed_qkv) + (size_t)it.n * T * dim;
-  Act* cs_base = static_cast<Act*>(p.conv_state) + (size_t)it.n * dim * (kConvW - 1);
-  for (int task = tid; task < 2 * NQ; task += NT) {
-    const int c = task < NQ ? it.h * K + task * VEC : p.H * K + it.h * K + (task - NQ) * VEC;
-    Act* csp = cs_base + (size_t)c * (kConvW - 1);
-    Raw old[3 * VEC] = {};
-    if (T < kConvW - 1) {
 #pragma unroll
-      for (int m = 0; m < 3; ++m)
-        AT::unpack(ld_rw_16(reinterpret_cast<const char*>(csp) + 16 * m), old + m * VEC);
-    }
+  for (int e = 0; e < VEC; e += 4)
+    *reinterpret_cast<float4*>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+  const bool do_roll = roll && t == T - 1;
+  if (snap || do_roll) {
+    // the raw window after token t: x_ext[t+1 .. t+3], channel-major [e][j]
     Raw r[3 * VEC];
 #pragma unroll
-    for (int j = 0; j < kConvW - 1; ++j) {
-      const int idx = T + j;  // position in [state || tokens]
-      Raw xv[VEC];
-      if (idx >= kConvW - 1) {
-        AT::unpack(ld_ro_16(xq + (size_t)(idx - (kConvW - 1)) * dim + c), xv);
+    for (int e = 0; e < VEC; ++e)
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) r[e * (kConvW - 1) + j] = xv[e];
-      } else {
-        // select old[.., idx] with compile-time indices only (no local memory)
+      for (int j = 0; j < kConvW - 1; ++j) r[e * (kConvW - 1) + j] = win[j + 1][e];
+    if (snap) {
+      char* sp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_snapshots) +
+                                         (((size_t)it.n * T + t) * p.dim + c) * (kConvW - 1));
 #pragma unroll
-        for (int jj = 0; jj < kConvW - 1; ++jj)
-          if (jj == idx) {
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) r[e * (kConvW - 1) + j] = old[e * (kConvW - 1) + jj];
-          }
-      }
+      for (int m = 0; m < 3; ++m) st_16(sp + 16 * m, AT::pack(r + m * VEC));
     }
+    if (do_roll) {
+      char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
+                                         ((size_t)it.n * p.dim + c) * (kConvW - 1));
 #pragma unroll
-    for (int m = 0; m < 3; ++m) st_16(reinterpret_cast<char*>(csp) + 16 * m, AT::pack(r + m * VEC));
+      for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
+    }
   }
 }
 
-// Arrival of one item on its q/k group counter (thread 0 only).  Returns true
+// One gate task: alpha = exp(g) of VEC channels at token t.
+template <typename Act, typename Src>
+__device__ __forceinline__ void gate_task(const Src& src, int gate_mode, float negA, int t,
+                                          int e0, float* dst) {
+  using AT = ActT<Act>;
+  using Raw = typename AT::Raw;
+  constexpr int VEC = AT::VEC;
+  Raw r[VEC];
+  AT::unpack(src.a(t, e0), r);
+  float al[VEC];
+  if (gate_mode == 0) {
+#pragma unroll
+    for (int e = 0; e < VEC; e += 4) {
+      const float4 d = src.dt(e0 + e);
+      const float dd[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x = __fadd_rn(AT::to_f(r[e + j]), dd[j]);
+        al[e + j] = expf(__fmul_rn(negA, softplus_f(x)));
+      }
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) al[e] = expf(fminf(AT::to_f(r[e]), 0.0f));
+  }
+#pragma unroll
+  for (int e = 0; e < VEC; e += 4)
+    *reinterpret_cast<float4*>(dst + e) = make_float4(al[e], al[e + 1], al[e + 2], al[e + 3]);
+}
+
+template <typename Act>
+__device__ __forceinline__ float load_b(const Params& p, const Item& it, int t) {
+  const Act* bp = static_cast<const Act*>(p.b) + ((size_t)it.n * p.T + t) * p.HV + it.hv;
+  if constexpr (sizeof(Act) == 4) {
+    return __ldg(reinterpret_cast<const float*>(bp));
+  } else {
+    return ActT<Act>::to_f(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(bp))));
+  }
+}
+
+// All conv / gate / beta tasks of one item, spread over `nthr` threads.
+template <typename Act, int K, int BV, typename Src>
+__device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, const Item& it,
+                                              float* sQ, float* sK, float* sA, float* sV,
+                                              float* sB, int tid, int nthr) {
+  constexpr int VEC = ActT<Act>::VEC;
+  constexpr int NQ = K / VEC;
+  constexpr int NCV = 2 * NQ + BV / VEC;  // channel vectors of the item
+  const int T = p.T;
+  const int n_conv = NCV * T;
+  const int n_gate = NQ * T;
+  // q/k snapshots are written once per group: by its first v-head, first tile
+  const bool qk_snap_owner = (it.hv % p.G == 0) && (it.vt == 0);
+  const float negA = p.gate_mode == 0 ? -expf(__ldg(p.A_log + it.hv)) : 0.0f;
+  for (int task = tid; task < n_conv + n_gate + T; task += nthr) {
+    if (task < n_conv) {
+      const int cv = task / T;
+      const int t = task - cv * T;
+      const int kind = cv < NQ ? 0 : (cv < 2 * NQ ? 1 : 2);
+      const int e0 = (cv - kind * NQ) * VEC;
+      float* dst = kind == 0 ? sQ + t * K + e0 : (kind == 1 ? sK + t * K + e0 : sV + t * BV + e0);
+      const int c = block_channel<K, BV>(p, it, kind) + e0;
+      conv_task<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 || qk_snap_owner, kind == 2);
+    } else if (task < n_conv + n_gate) {
+      const int g = task - n_conv;
+      const int t = g / NQ;
+      const int e0 = (g - t * NQ) * VEC;
+      gate_task<Act>(src, p.gate_mode, negA, t, e0, sA + t * K + e0);
+    } else {
+      const int t = task - n_conv - n_gate;
+      sB[t] = sigmoid_f(load_b<Act>(p, it, t));
+    }
+  }
+}
+
+// L2 norm of one K-vector by one warp (q additionally scaled by K^-1/2).
+template <int K>
+__device__ __forceinline__ void l2norm_warp(float* x, bool is_q, int lane) {
+  float xs[K / 32];
+  float ss = 0.0f;
+#pragma unroll
+  for (int m = 0; m < K / 32; ++m) {
+    xs[m] = x[lane + 32 * m];
+    ss = __fmaf_rn(xs[m], xs[m], ss);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+  float inv = rsqrtf(__fadd_rn(ss, kL2Eps));
+  if (is_q) inv = __fmul_rn(inv, rsqrtf(static_cast<float>(K)));
+#pragma unroll
+  for (int m = 0; m < K / 32; ++m) x[lane + 32 * m] = __fmul_rn(xs[m], inv);
+}
+
+// Arrival of one item on its q/k group counter (one thread).  Returns true
 // for the last arrival, which also resets the counter.
 __device__ __forceinline__ bool arrive_qk_group(const Params& p, const Item& it) {
   const int expected = p.G * p.nvt;
   if (expected == 1) return true;
   int* cnt = p.counters + (size_t)it.n * p.H + it.h;
-  __threadfence();  // this CTA's conv_state reads are done (a barrier precedes)
+  __threadfence();  // this item's conv_state reads are complete (ordered before)
   const int old = atomicAdd(cnt, 1);
   if (old != expected - 1) return false;
   atomicExch(cnt, 0);
@@ -319,9 +367,56 @@ __device__ __forceinline__ bool arrive_qk_group(const Params& p, const Item& it)
   return true;
 }
 
+// Roll the q/k conv_state of group (n, h) to x_ext[T .. T+2].
+template <typename Act, int K, int BV, typename Src>
+__device__ __forceinline__ void roll_qk(const Src& src, const Params& p, const Item& it, int tid,
+                                        int nthr) {
+  using AT = ActT<Act>;
+  using Raw = typename AT::Raw;
+  constexpr int VEC = AT::VEC;
+  constexpr int NQ = K / VEC;
+  const int T = p.T;
+  for (int task = tid; task < 2 * NQ; task += nthr) {
+    const int kind = task < NQ ? 0 : 1;
+    const int e0 = (task - kind * NQ) * VEC;
+    const int c = block_channel<K, BV>(p, it, kind) + e0;
+    Raw old[3 * VEC] = {};
+    if (T < kConvW - 1) {
+#pragma unroll
+      for (int m = 0; m < 3; ++m) AT::unpack(src.cs(kind, e0, m), old + m * VEC);
+    }
+    Raw r[3 * VEC];
+#pragma unroll
+    for (int j = 0; j < kConvW - 1; ++j) {
+      const int idx = T + j;
+      Raw xv[VEC];
+      if (idx >= kConvW - 1) {
+        AT::unpack(src.x(kind, idx - (kConvW - 1), e0), xv);
+      } else {
+        select_state<Raw, VEC>(old, idx, xv);
+      }
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) r[e * (kConvW - 1) + j] = xv[e];
+    }
+    char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
+                                       ((size_t)it.n * p.dim + c) * (kConvW - 1));
+#pragma unroll
+    for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
+  }
+}
+
 // ---------------------------------------------------------------------------
 // consumer: the recurrence on register-resident S
 // ---------------------------------------------------------------------------
+template <int K, int BV>
+__device__ __forceinline__ void load_tile(const float* sbuf, float4 (&s)[K / 8], int warp, int lane) {
+  constexpr int R = K / 8;
+  const int rg = lane >> 2, cg = lane & 3;
+  const float* src = sbuf + (rg * R) * BV + warp * 16 + cg * 4;
+#pragma unroll
+  for (int i = 0; i < R; ++i) s[i] = *reinterpret_cast<const float4*>(src + i * BV);
+}
+
 template <typename Act, int K, int BV>
 __device__ __forceinline__ void consume(const Params& p, const Item& it, const float* sQ,
                                        const float* sK, const float* sA, const float* sV,
@@ -401,11 +496,11 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
 }
 
 // ---------------------------------------------------------------------------
-// the kernel
+// one item per CTA: every warp produces, then consumes
 // ---------------------------------------------------------------------------
-template <typename Act, int K, int WARPS, bool PERSIST>
+template <typename Act, int K, int WARPS>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
-    kda_verify_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
+    kda_tile_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
   constexpr int BV = WARPS * 16;
   constexpr int NT = WARPS * 32;
   constexpr int R = K / 8;
@@ -413,86 +508,248 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);
-  int* sflag = reinterpret_cast<int*>(smem + 8);  // [NSTAGE] last-arrival flags
+  int* sflag = reinterpret_cast<int*>(smem + 8);
   float* sbuf = reinterpret_cast<float*>(smem + 128);
-  float* stage0 = sbuf + K * BV;
   const int T = p.T;
-  const int sf = stage_floats(T, K, BV);
+  float* sQ = sbuf + K * BV;
+  float* sK = sQ + T * K;
+  float* sA = sK + T * K;
+  float* sV = sA + T * K;
+  float* sB = sV + T * BV;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-
-  long long item = blockIdx.x;
+  const long long item = blockIdx.x;
   if (item >= p.num_items) return;
-  const long long stride = PERSIST ? (long long)gridDim.x : p.num_items;
+  const Item it = decode_item(p, item);
 
   if (tid == 0) {
     mbar_init(mbar, 1);
     fence_mbar_init();
+    prefetch_tensormap(&tmap_s0);
+    mbar_arrive_expect_tx(mbar, K * BV * sizeof(float));
+    tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.unit * K), mbar,
+                l2_policy_evict_first());
+  }
+  const GlobalSrc<Act, K, BV> src{p, it};
+  produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, tid, NT);
+  __syncthreads();  // every conv_state read of this CTA is done, stage written
+  if (tid == 0) sflag[0] = arrive_qk_group(p, it) ? 1 : 0;
+  for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * K : sK + (r - T) * K, r < T, lane);
+  const bool ok = mbar_wait_bounded(mbar, 0, kWaitLimitNs);
+  if (__syncthreads_or(!ok)) {
+    // give up without hanging: report, let the copy in flight land, leave
+    if (tid == 0) atomicOr(p.status, kStatusTmaTimeout);
+    mbar_wait_bounded(mbar, 0, kWaitLimitNs);
+    return;
+  }
+  float4 s[R];
+  load_tile<K, BV>(sbuf, s, warp, lane);
+  consume<Act, K, BV>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
+  if (sflag[0]) roll_qk<Act, K, BV>(src, p, it, tid, NT);
+}
+
+// ---------------------------------------------------------------------------
+// persistent, warp-specialised: warp CW produces, warps 0..CW-1 consume
+// ---------------------------------------------------------------------------
+struct WsBars {
+  uint64_t tile_full;       // TMA state tile landed (1 arrival + tx)
+  uint64_t tile_empty;      // consumers moved the tile to registers (CW*32)
+  uint64_t raw_full;        // raw inputs landed (1 arrival + tx)
+  uint64_t stage_full[2];   // producer staged q/k/alpha/v/beta (32)
+  uint64_t stage_empty[2];  // consumers done with the stage (CW*32)
+  int abort_flag;
+};
+
+// Bounded wait that also gives up when another warp of the CTA gave up.
+__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void ws_fail(const Params& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicOr(p.status, kStatusTmaTimeout);
+}
+
+template <typename Act, int K, int BV>
+__device__ __forceinline__ uint32_t raw_tx_bytes(const Params& p) {
+  constexpr int AB = sizeof(Act);
+  return static_cast<uint32_t>(AB * (p.T * (2 * K + BV) + (2 * K + BV) * 7 + p.T * K) +
+                               (p.gate_mode == 0 ? 4 * K : 0));
+}
+
+// 1-D bulk copies of one item's raw inputs into `raw`, spread over the lanes
+// of one warp (lane 0 has already posted raw_tx_bytes on `bar`).
+template <typename Act, int K, int BV>
+__device__ __forceinline__ void issue_raw(const Params& p, const Item& it, unsigned char* raw,
+                                          uint64_t* bar, int lane) {
+  constexpr int AB = sizeof(Act);
+  const int T = p.T;
+  const SmemSrc<Act, K, BV> L{raw, T};
+  const int ncopy = 4 * T + 6 + (p.gate_mode == 0 ? 1 : 0);
+  const char* xq = static_cast<const char*>(p.mixed_qkv);
+  for (int c = lane; c < ncopy; c += 32) {
+    const char* src;
+    unsigned char* dst;
+    uint32_t bytes;
+    if (c < 3 * T) {
+      const int t = c / 3, kind = c - 3 * t;
+      src = xq + (((size_t)it.n * T + t) * p.dim + block_channel<K, BV>(p, it, kind)) * AB;
+      dst = raw + L.off_x(kind, t);
+      bytes = (kind == 2 ? BV : K) * AB;
+    } else if (c < 3 * T + 6) {
+      const int q = c - 3 * T;  // 0..2 conv_state blocks, 3..5 conv_w blocks
+      const int kind = q % 3;
+      const int ch = block_channel<K, BV>(p, it, kind);
+      const int nch = kind == 2 ? BV : K;
+      if (q < 3) {
+        src = static_cast<const char*>(p.conv_state) + ((size_t)it.n * p.dim + ch) * 3 * AB;
+        dst = raw + L.base_cs() + (size_t)L.blk(kind) * 3 * AB;
+        bytes = nch * 3 * AB;
+      } else {
+        src = static_cast<const char*>(p.conv_w) + (size_t)ch * 4 * AB;
+        dst = raw + L.base_w() + (size_t)L.blk(kind) * 4 * AB;
+        bytes = nch * 4 * AB;
+      }
+    } else if (c < 4 * T + 6) {
+      const int t = c - 3 * T - 6;
+      src = static_cast<const char*>(p.a) + ((((size_t)it.n * T + t) * p.HV + it.hv) * K) * AB;
+      dst = raw + L.base_a() + (size_t)t * K * AB;
+      bytes = K * AB;
+    } else {
+      src = reinterpret_cast<const char*>(p.dt_bias + (size_t)it.hv * K);
+      dst = raw + L.base_dt();
+      bytes = K * 4;
+    }
+    bulk_load(dst, src, bytes, bar);
+  }
+}
+
+__host__ __device__ constexpr int ws_min_blocks(int cw) { return cw >= 8 ? 1 : (cw >= 4 ? 3 : 5); }
+
+template <typename Act, int K, int CW>
+__global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
+    kda_ws_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
+  constexpr int BV = CW * 16;
+  constexpr int R = K / 8;
+  static_assert(K % 32 == 0 && K <= 128, "K must be 32, 64 or 128");
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  WsBars* bars = reinterpret_cast<WsBars*>(smem);
+  volatile int* abort_flag = &bars->abort_flag;
+  float* sbuf = reinterpret_cast<float*>(smem + 128);
+  const int T = p.T;
+  const int sf = stage_floats(T, K, BV);
+  float* stage0 = sbuf + K * BV;
+  unsigned char* raw = reinterpret_cast<unsigned char*>(stage0 + 2 * sf);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long stride = gridDim.x;
+  if ((long long)blockIdx.x >= p.num_items) return;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars->tile_full, 1);
+    mbar_init(&bars->tile_empty, CW * 32);
+    mbar_init(&bars->raw_full, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->stage_full[s], 32);
+      mbar_init(&bars->stage_empty[s], CW * 32);
+    }
+    bars->abort_flag = 0;
+    fence_mbar_init();
   }
   __syncthreads();
-  const uint64_t pol = l2_policy_evict_first();
-  if (tid == 0) {
-    prefetch_tensormap(&tmap_s0);
-    const Item it = decode_item(p, item);
-    mbar_arrive_expect_tx(mbar, K * BV * sizeof(float));
-    tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.unit * K), mbar, pol);
-  }
 
-  auto produce = [&](long long itm, int buf) {
-    const Item it = decode_item(p, itm);
-    float* st = stage0 + buf * sf;
-    float* sQ = st;
-    float* sK = sQ + T * K;
-    float* sA = sK + T * K;
-    float* sV = sA + T * K;
-    float* sB = sV + T * BV;
-    produce_phase1<Act, K, BV, NT>(p, it, sQ, sK, sA, sV, sB, tid);
-    __syncthreads();
-    if (tid == 0) sflag[buf] = arrive_qk_group(p, it) ? 1 : 0;
-    produce_phase2<K, WARPS>(T, sQ, sK, warp, lane);
-    __syncthreads();
-  };
-
-  produce(item, 0);
-  for (int iter = 0;; ++iter) {
-    const int buf = PERSIST ? (iter & 1) : 0;
-    const Item it = decode_item(p, item);
-    const bool ok = mbar_wait_bounded(mbar, static_cast<uint32_t>(iter & 1), kWaitLimitNs);
-    if (__syncthreads_or(!ok)) {
-      // give up without hanging: report, let the copy in flight land, leave
-      if (tid == 0) atomicOr(p.status, 1);
-      mbar_wait_bounded(mbar, static_cast<uint32_t>(iter & 1), kWaitLimitNs);
-      __syncthreads();
-      return;
+  if (warp == CW) {
+    // ------------------------------ producer ------------------------------
+    const uint64_t pol = l2_policy_evict_first();
+    long long item = blockIdx.x;
+    Item it = decode_item(p, item);
+    if (lane == 0) {
+      prefetch_tensormap(&tmap_s0);
+      mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
+      tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.unit * K), &bars->tile_full, pol);
+      mbar_arrive_expect_tx(&bars->raw_full, raw_tx_bytes<Act, K, BV>(p));
     }
-    float4 s[R];
-    {
-      const int rg = lane >> 2, cg = lane & 3;
-      const float* src = sbuf + (rg * R) * BV + warp * 16 + cg * 4;
-#pragma unroll
-      for (int i = 0; i < R; ++i) s[i] = *reinterpret_cast<const float4*>(src + i * BV);
-    }
-    const long long next = item + stride;
-    const bool has_next = PERSIST && next < p.num_items;
-    if (PERSIST) {
-      __syncthreads();  // every thread has copied the tile out of sbuf
-      if (has_next && tid == 0) {
-        fence_proxy_async_smem();
-        const Item nx = decode_item(p, next);
-        mbar_arrive_expect_tx(mbar, K * BV * sizeof(float));
-        tma_load_2d(sbuf, &tmap_s0, nx.vt * BV, static_cast<int>(nx.unit * K), mbar, pol);
+    __syncwarp();
+    issue_raw<Act, K, BV>(p, it, raw, &bars->raw_full, lane);
+    int raw_phase = 0;   // phase of raw_full that the newest raw copy completes
+    int tile_phase = 0;  // phase of tile_full that the newest tile load completes
+    bool failed = false;
+    for (int j = 0;; ++j) {
+      const int s = j & 1;
+      float* sQ = stage0 + s * sf;
+      float* sK = sQ + T * K;
+      float* sA = sK + T * K;
+      float* sV = sA + T * K;
+      float* sB = sV + T * BV;
+      if (!ws_wait(&bars->raw_full, j & 1, abort_flag)) { failed = true; break; }
+      if (j >= 2 && !ws_wait(&bars->stage_empty[s], ((j >> 1) + 1) & 1, abort_flag)) {
+        failed = true;
+        break;
       }
+      const SmemSrc<Act, K, BV> src{raw, T};
+      produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, lane, 32);
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = arrive_qk_group(p, it) ? 1 : 0;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) roll_qk<Act, K, BV>(src, p, it, lane, 32);
+      __syncwarp();  // every lane is done with the raw buffer
+      const long long next = item + stride;
+      const bool has_next = next < p.num_items;
+      const Item nx = has_next ? decode_item(p, next) : it;
+      if (has_next) {
+        fence_proxy_async_smem();
+        if (lane == 0) mbar_arrive_expect_tx(&bars->raw_full, raw_tx_bytes<Act, K, BV>(p));
+        __syncwarp();
+        issue_raw<Act, K, BV>(p, nx, raw, &bars->raw_full, lane);
+        raw_phase = j + 1;
+      }
+      for (int r = 0; r < 2 * T; ++r) l2norm_warp<K>(r < T ? sQ + r * K : sK + (r - T) * K, r < T, lane);
+      mbar_arrive(&bars->stage_full[s]);
+      if (!has_next) break;
+      // hand the next state tile over as soon as the consumers hold this one
+      if (!ws_wait(&bars->tile_empty, j & 1, abort_flag)) { failed = true; break; }
+      if (lane == 0) {
+        fence_proxy_async_smem();
+        mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
+        tma_load_2d(sbuf, &tmap_s0, nx.vt * BV, static_cast<int>(nx.unit * K), &bars->tile_full, pol);
+      }
+      tile_phase = j + 1;
+      item = next;
+      it = nx;
     }
-    {
-      const float* st = stage0 + buf * sf;
+    if (failed) {
+      // report, then let the newest copies in flight land before leaving
+      ws_fail(p, abort_flag);
+      mbar_wait_bounded(&bars->raw_full, raw_phase & 1, kWaitLimitNs);
+      mbar_wait_bounded(&bars->tile_full, tile_phase & 1, kWaitLimitNs);
+    }
+  } else {
+    // ------------------------------ consumers -----------------------------
+    long long item = blockIdx.x;
+    for (int j = 0; item < p.num_items; ++j, item += stride) {
+      const int s = j & 1;
+      const Item it = decode_item(p, item);
+      if (!ws_wait(&bars->tile_full, j & 1, abort_flag)) { ws_fail(p, abort_flag); return; }
+      float4 sreg[R];
+      load_tile<K, BV>(sbuf, sreg, warp, lane);
+      mbar_arrive(&bars->tile_empty);
+      if (!ws_wait(&bars->stage_full[s], (j >> 1) & 1, abort_flag)) { ws_fail(p, abort_flag); return; }
+      const float* st = stage0 + s * sf;
       consume<Act, K, BV>(p, it, st, st + T * K, st + 2 * T * K, st + 3 * T * K,
-                          st + 3 * T * K + T * BV, s, warp, lane);
+                          st + 3 * T * K + T * BV, sreg, warp, lane);
+      mbar_arrive(&bars->stage_empty[s]);
     }
-    if (sflag[buf]) roll_qk<Act, K, NT>(p, it, tid);
-    if (!has_next) break;
-    item = next;
-    produce(item, buf ^ 1);
   }
 }
 

@@ -1,6 +1,6 @@
 // kda_launch.cuh -- host-side launch of one kernel instantiation.  Each
-// activation type is instantiated in its own translation unit
-// (kda_inst_bf16.cu, kda_inst_f32.cu) so the two compile in parallel.
+// (activation type, kernel) pair is instantiated in its own translation unit
+// (kda_inst_*.cu) so that they compile in parallel.
 #pragma once
 
 #include <cuda.h>
@@ -12,47 +12,75 @@ namespace kda {
 
 struct LaunchCfg {
   int K;        // 32, 64 or 128
-  int warps;    // warps per CTA; the v-tile is 16 * warps columns
-  bool persist; // persistent CTAs with next-tile prefetch
+  int warps;    // tile kernel: warps per CTA; ws kernel: consumer warps
+  bool ws;      // warp-specialised persistent kernel
   int grid;     // CTAs
   size_t smem;  // dynamic shared memory bytes
 };
 
 // Launch the instantiation that matches `cfg`; returns a cudaError_t value,
 // or -1 when no instantiation matches.
-int launch_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
-int launch_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+int launch_tile_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+int launch_tile_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+int launch_ws_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+int launch_ws_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
 
-template <typename Act, int K, int WARPS, bool PERSIST>
-int launch_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
-  auto fn = kda_verify_kernel<Act, K, WARPS, PERSIST>;
-  // Opt in to large dynamic shared memory once per device.
-  static unsigned long long configured = 0;  // bit per device ordinal (< 64)
+// Opt a kernel in to large dynamic shared memory once per device.
+template <typename Fn>
+int configure_once(Fn fn, unsigned long long* configured) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return static_cast<int>(e);
   const unsigned long long bit = 1ull << (dev & 63);
-  if (!(__atomic_load_n(&configured, __ATOMIC_ACQUIRE) & bit)) {
+  if (!(__atomic_load_n(configured, __ATOMIC_ACQUIRE) & bit)) {
     int max_optin = 0;
     e = cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return static_cast<int>(e);
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, max_optin);
     if (e != cudaSuccess) return static_cast<int>(e);
-    __atomic_fetch_or(&configured, bit, __ATOMIC_RELEASE);
+    __atomic_fetch_or(configured, bit, __ATOMIC_RELEASE);
   }
+  return 0;
+}
+
+template <typename Act, int K, int WARPS>
+int launch_tile_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
+  auto fn = kda_tile_kernel<Act, K, WARPS>;
+  static unsigned long long configured = 0;  // bit per device ordinal (< 64)
+  int rc = configure_once(fn, &configured);
+  if (rc) return rc;
   fn<<<cfg.grid, WARPS * 32, cfg.smem, st>>>(tmap, p);
   return static_cast<int>(cudaGetLastError());
 }
 
+template <typename Act, int K, int CW>
+int launch_ws_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
+  auto fn = kda_ws_kernel<Act, K, CW>;
+  static unsigned long long configured = 0;
+  int rc = configure_once(fn, &configured);
+  if (rc) return rc;
+  fn<<<cfg.grid, (CW + 1) * 32, cfg.smem, st>>>(tmap, p);
+  return static_cast<int>(cudaGetLastError());
+}
+
 template <typename Act>
-int launch_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c, cudaStream_t st) {
-#define KDA_CASE(KK, WW, PP)                                      \
-  if (c.K == KK && c.warps == WW && c.persist == PP)              \
-    return launch_one<Act, KK, WW, PP>(tmap, p, c, st);
-#define KDA_CASES_K(KK)                                           \
-  KDA_CASE(KK, 1, false) KDA_CASE(KK, 2, false) KDA_CASE(KK, 4, false) \
-  KDA_CASE(KK, 8, false) KDA_CASE(KK, 2, true) KDA_CASE(KK, 4, true)   \
-  KDA_CASE(KK, 8, true)
+int launch_tile_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c, cudaStream_t st) {
+#define KDA_CASE(KK, WW) \
+  if (c.K == KK && c.warps == WW) return launch_tile_one<Act, KK, WW>(tmap, p, c, st);
+#define KDA_CASES_K(KK) KDA_CASE(KK, 1) KDA_CASE(KK, 2) KDA_CASE(KK, 4) KDA_CASE(KK, 8)
+  KDA_CASES_K(32)
+  KDA_CASES_K(64)
+  KDA_CASES_K(128)
+#undef KDA_CASES_K
+#undef KDA_CASE
+  return -1;
+}
+
+template <typename Act>
+int launch_ws_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c, cudaStream_t st) {
+#define KDA_CASE(KK, WW) \
+  if (c.K == KK && c.warps == WW) return launch_ws_one<Act, KK, WW>(tmap, p, c, st);
+#define KDA_CASES_K(KK) KDA_CASE(KK, 2) KDA_CASE(KK, 4) KDA_CASE(KK, 8)
   KDA_CASES_K(32)
   KDA_CASES_K(64)
   KDA_CASES_K(128)

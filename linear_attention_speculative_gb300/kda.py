@@ -28,9 +28,9 @@ BF16 = 1
 MAX_T = 16
 
 # The names declared in include/kda_verify.h.
-EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_noalloc",
-            "kda_workspace_bytes", "kda_make_plan", "kda_read_status", "kda_strerror",
-            "kda_version")
+EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan",
+            "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan",
+            "kda_read_status", "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
 
@@ -71,6 +71,8 @@ def _load():
     L.kda_conv_verify.argtypes = args_common + [vp]
     L.kda_conv_verify_variant.restype = ctypes.c_int
     L.kda_conv_verify_variant.argtypes = args_common + [ctypes.c_int, vp]
+    L.kda_conv_verify_plan.restype = ctypes.c_int
+    L.kda_conv_verify_plan.argtypes = args_common + [ctypes.POINTER(KdaPlan), vp]
     L.kda_conv_verify_noalloc.restype = ctypes.c_int
     L.kda_conv_verify_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                           vp, vp, vp, vp]
@@ -138,22 +140,38 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def parse_plan(spec: str) -> KdaPlan:
+    """'small:32' / 'large:64' / 'large:64:300' (variant, v-tile width, grid)."""
+    parts = spec.split(":")
+    plan = KdaPlan()
+    plan.variant = {"small": VARIANT_SMALL_BATCH, "small_batch": VARIANT_SMALL_BATCH,
+                    "large": VARIANT_LARGE_BATCH, "large_batch": VARIANT_LARGE_BATCH}[parts[0]]
+    plan.bv = int(parts[1])
+    plan.grid = int(parts[2]) if len(parts) > 2 else 0
+    return plan
+
+
 def conv_verify(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: str,
                 o, inter_ssm, conv_snapshots, workspace, stream=None, variant: str = "auto",
-                shape: Optional[KdaShape] = None) -> None:
+                shape: Optional[KdaShape] = None, plan=None) -> None:
     """Launch the fused verify decode on `stream` (default: current stream).
 
     Tensors must be contiguous CUDA tensors in the layouts of the header;
     conv_state is updated in place; o / inter_ssm / conv_snapshots are
-    written.  Raises KdaError on any non-zero return code."""
+    written.  `plan` (a KdaPlan or a 'small:32'-style string) overrides the
+    dispatcher.  Raises KdaError on any non-zero return code."""
     if shape is None:
         shape = shape_of(mixed_qkv, a, S0)
     gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
-    rc = lib().kda_conv_verify_variant(
-        ctypes.byref(shape), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_state), _ptr(A_log),
-        _ptr(dt_bias), _ptr(a), _ptr(b), _ptr(S0), gm, _ptr(o), _ptr(inter_ssm),
-        _ptr(conv_snapshots), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        VARIANTS[variant], _stream_handle(stream))
+    args = (ctypes.byref(shape), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_state), _ptr(A_log),
+            _ptr(dt_bias), _ptr(a), _ptr(b), _ptr(S0), gm, _ptr(o), _ptr(inter_ssm),
+            _ptr(conv_snapshots), _ptr(workspace), workspace.numel() * workspace.element_size())
+    if plan is not None:
+        if isinstance(plan, str):
+            plan = parse_plan(plan)
+        rc = lib().kda_conv_verify_plan(*args, ctypes.byref(plan), _stream_handle(stream))
+    else:
+        rc = lib().kda_conv_verify_variant(*args, VARIANTS[variant], _stream_handle(stream))
     if rc != 0:
         raise KdaError(rc)
 
@@ -184,7 +202,7 @@ def read_status(shape: KdaShape, workspace: torch.Tensor, stream=None) -> int:
 
 
 def run(inputs: Dict[str, torch.Tensor], gate: str, variant: str = "auto",
-        workspace: Optional[torch.Tensor] = None, stream=None) -> Dict[str, torch.Tensor]:
+        workspace: Optional[torch.Tensor] = None, stream=None, plan=None) -> Dict[str, torch.Tensor]:
     """Convenience: allocate outputs on the inputs' device and launch.
     `inputs["conv_state"]` is rolled in place."""
     x = inputs["mixed_qkv"]
@@ -201,5 +219,5 @@ def run(inputs: Dict[str, torch.Tensor], gate: str, variant: str = "auto",
     conv_verify(x, inputs["conv_w"], inputs["conv_state"], inputs.get("A_log"),
                 inputs.get("dt_bias"), inputs["a"], inputs["b"], inputs["S0"], gate,
                 out["o"], out["inter_ssm"], out["conv_snapshots"], ws, stream=stream,
-                variant=variant, shape=shape)
+                variant=variant, shape=shape, plan=plan)
     return out

@@ -74,10 +74,14 @@ def to_device(inputs, device="cuda"):
 
 def run_kernel(inputs_cpu, gate, variant="auto"):
     """Copy inputs to the GPU, run one call, return (device outputs, rolled
-    conv_state on the device)."""
+    conv_state on the device).  `variant` is auto / small_batch / large_batch
+    or an explicit plan such as 'small:64' or 'large:32'."""
     from linear_attention_speculative_gb300 import kda
     dev = to_device(inputs_cpu)
-    out = kda.run(dev, gate, variant=variant)
+    if ":" in variant:
+        out = kda.run(dev, gate, plan=variant)
+    else:
+        out = kda.run(dev, gate, variant=variant)
     torch.cuda.synchronize()
     return out, dev["conv_state"]
 

@@ -59,23 +59,31 @@ def test_workspace_bytes(kda):
 
 # ---- the dispatcher (host logic only) --------------------------------------
 
-def test_plan_large_batch_for_many_units(kda):
+def test_plan_auto_uses_one_item_per_cta(kda):
+    # whole states per 8-warp CTA, one item per CTA
     p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
-    assert p.variant == kda.VARIANT_LARGE_BATCH
-    assert p.bv == 128 and p.warps == 8 and p.items == 256 * 32
-    assert 1 <= p.grid <= 152 * p.ctas_per_sm
-
-
-def test_plan_small_batch_for_few_units(kda):
-    p = kda.make_plan(kda.make_shape(16, 4, 16, 16), 152)
     assert p.variant == kda.VARIANT_SMALL_BATCH
-    assert p.items == 16 * 16 * (128 // p.bv)
-    assert p.grid == p.items
-    p1 = kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)
-    assert p1.bv == 16 and p1.warps == 1  # narrowest tiles for the tiniest batch
+    assert p.bv == 128 and p.warps == 8 and p.items == 256 * 32 and p.grid == p.items
+    # short verifies over many units: half states
+    p2 = kda.make_plan(kda.make_shape(512, 2, 32, 64), 152)
+    assert p2.bv == 64 and p2.items == 512 * 64 * 2
+    assert kda.make_plan(kda.make_shape(8, 2, 16, 16), 152).bv == 128
+    # fewer units than SMs: whole states per CTA
+    p1 = kda.make_plan(kda.make_shape(1, 4, 16, 16), 152)
+    assert p1.variant == kda.VARIANT_SMALL_BATCH and p1.bv == 128 and p1.warps == 8
+    assert p1.items == 16 and p1.grid == 16
 
 
-def test_plan_forced_variants_and_small_heads(kda):
+def test_plan_large_batch_is_persistent(kda):
+    p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152, "large_batch")
+    assert p.variant == kda.VARIANT_LARGE_BATCH
+    assert p.bv == 64 and p.warps == 4 and p.items == 256 * 32 * 2
+    assert 152 <= p.grid <= 152 * p.ctas_per_sm
+    tiny = kda.make_plan(kda.make_shape(1, 2, 1, 1), 152, "large_batch")
+    assert tiny.grid == tiny.items == 2  # never more CTAs than items
+
+
+def test_plan_small_heads(kda):
     s = kda.make_shape(8, 2, 2, 4, K=64, V=32)
     big = kda.make_plan(s, 152, "large_batch")
     assert big.variant == kda.VARIANT_LARGE_BATCH and big.bv == 32 and big.warps == 2
@@ -104,6 +112,27 @@ def _fake_args(kda, **over):
     ptrs = {n: base + i * (1 << 24) for i, n in enumerate(names)}
     ptrs.update(over)
     return ptrs
+
+
+def _call_plan(kda, shape, ptrs, plan, gate=0, ws_bytes=1 << 20):
+    L = kda.lib()
+    v = lambda n: ctypes.c_void_p(ptrs[n]) if ptrs[n] is not None else None
+    return L.kda_conv_verify_plan(
+        ctypes.byref(shape), v("mixed_qkv"), v("conv_w"), v("conv_state"), v("A_log"),
+        v("dt_bias"), v("a"), v("b"), v("S0"), gate, v("o"), v("inter_ssm"),
+        v("conv_snapshots"), v("workspace"), ws_bytes, ctypes.byref(plan), None)
+
+
+def test_rejects_invalid_plans(kda):
+    s = kda.make_shape(2, 2, 2, 2, 32, 64)
+    for spec in ("small:8", "small:128", "small:48", "large:16", "large:128"):
+        assert _call_plan(kda, s, _fake_args(kda), kda.parse_plan(spec)) == -8, spec
+    bad = kda.KdaPlan()
+    bad.variant, bad.bv = 0, 32  # AUTO is not a concrete plan
+    assert _call_plan(kda, s, _fake_args(kda), bad) == -8
+    # a NULL plan is rejected before anything else is looked at
+    args = [ctypes.byref(s)] + [None] * 8 + [0] + [None] * 4 + [0]
+    assert kda.lib().kda_conv_verify_plan(*args, None, None) == -1
 
 
 def _call(kda, shape, ptrs, gate=0, ws_bytes=1 << 20, variant=0):

@@ -22,6 +22,8 @@ from parity_util import (TOL, assert_parity, conv_window_properties, max_rel_err
 pytestmark = pytest.mark.gpu
 
 VARIANTS = ("auto", "small_batch", "large_batch")
+# every explicit plan of a V = 128 problem
+ALL_PLANS = ("small:16", "small:32", "small:64", "small:128", "large:32", "large:64", "large:128")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -79,17 +81,45 @@ def test_large_workload_takes_the_softplus_overflow_branch():
     assert torch.isfinite(out["inter_ssm"][seqs]).all()
 
 
+def _valid_plans(V):
+    return [p for p in ALL_PLANS if int(p.split(":")[1]) <= V]
+
+
 @pytest.mark.parametrize("wl", [wk.DECODE, wk.GVA,
                                 wk.custom(5, 3, 2, 8, 64, 128, gate="safe", seed=3),
-                                wk.custom(7, 2, 4, 4, 128, 64, seed=4)],
+                                wk.custom(7, 2, 4, 4, 128, 64, seed=4),
+                                wk.custom(3, 16, 2, 4, 32, 32, act="f32", seed=5)],
                          ids=lambda w: w.name)
-def test_variants_bit_identical(wl):
+def test_all_plans_bit_identical(wl):
     inp = wk.make_inputs(wl)
-    outs = {v: run_kernel(inp, wl.gate, v) for v in ("small_batch", "large_batch")}
-    a, b = outs["small_batch"], outs["large_batch"]
-    for key in ("o", "inter_ssm", "conv_snapshots"):
-        assert torch.equal(a[0][key], b[0][key]), key
-    assert torch.equal(a[1], b[1])
+    plans = _valid_plans(wl.shape.V)
+    ref = run_kernel(inp, wl.gate, plans[0])
+    for plan in plans[1:]:
+        out = run_kernel(inp, wl.gate, plan)
+        for key in ("o", "inter_ssm", "conv_snapshots"):
+            assert torch.equal(ref[0][key], out[0][key]), (plan, key)
+        assert torch.equal(ref[1], out[1]), plan
+
+
+@pytest.mark.parametrize("plan", ALL_PLANS)
+def test_parity_every_plan_decode(plan):
+    wl = wk.DECODE
+    inp = wk.make_inputs(wl)
+    ref = oracle.verify(inp, wl.gate, threads=8)
+    out, cs = run_kernel(inp, wl.gate, plan)
+    assert_parity(out, cs, ref)
+
+
+def test_persistent_grid_smaller_than_items():
+    # a handful of persistent CTAs walk many items each (stage/tile hand-over)
+    wl = wk.GVA
+    inp = wk.make_inputs(wl)
+    seqs = [0, 17, 63]
+    ref = oracle.verify(inp, wl.gate, seqs=seqs, threads=4)
+    for plan in ("large:64:3", "large:32:7", "large:128:1"):
+        out, cs = run_kernel(inp, wl.gate, plan)
+        assert_parity(out, cs, ref, seqs=seqs)
+        conv_window_properties(inp, out, cs)
 
 
 def test_deterministic_across_repeats():
@@ -97,7 +127,7 @@ def test_deterministic_across_repeats():
     wl = wk.GVA
     inp = wk.make_inputs(wl)
     first = None
-    for v in ("small_batch", "large_batch"):
+    for v in ("small:32", "small:128", "large:64"):
         for _ in range(iters):
             out, cs = run_kernel(inp, wl.gate, v)
             cur = (out["o"], out["inter_ssm"], out["conv_snapshots"], cs)
@@ -176,8 +206,8 @@ def test_workspace_is_left_zeroed():
     inp = to_device(wk.make_inputs(wl))
     shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
     ws = kda.alloc_workspace(shape, "cuda")
-    for v in ("small_batch", "large_batch"):
-        kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate, variant=v, workspace=ws)
+    for v in ("small:16", "small:128", "large:32", "large:128"):
+        kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate, plan=v, workspace=ws)
         torch.cuda.synchronize()
         assert int(ws.count_nonzero()) == 0
     assert kda.read_status(shape, ws) == 0
