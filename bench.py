@@ -60,6 +60,8 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the T x N x heads x gate sweep in both variants")
     ap.add_argument("--sweep-out", default="")
+    ap.add_argument("--sweep-filter", default="",
+                    help="regular expression: only sweep points whose name matches")
     ap.add_argument("--sweep-plans", default="auto,small:16,small:32,small:64,small:128,large:64",
                     help="plans timed at every sweep point")
     return ap.parse_args()
@@ -183,28 +185,25 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def cpu_baseline(wl, inputs_cpu, max_seconds=30.0):
-    """Time the CPU oracle as it stands on a bounded sample of the workload,
-    one sequence per thread at a time, on all host cores."""
+def cpu_baseline(wl, inputs_cpu, cpu_seconds=12.0):
+    """Time the CPU oracle as it stands on a bounded sample of the workload:
+    whole passes over its sequences (one sequence per thread at a time, all
+    host cores), repeated until about `cpu_seconds` of CPU time were spent."""
     import oracle
     cores = os.cpu_count() or 1
     s = wl.shape
-    per_seq = s.T * s.HV
-    # one sequence costs ~1e-3 s per head-step on one core; aim at ~20 s of CPU work
-    n_seq = max(cores, min(s.N, int(20.0 / (per_seq * 1.0e-3))))
-    n_seq = min(s.N, (n_seq + cores - 1) // cores * cores)
-    seqs = list(range(n_seq))
-    sub = {k: (v[seqs] if v is not None and k in ("mixed_qkv", "conv_state", "a", "b", "S0") else v)
-           for k, v in inputs_cpu.items()}
     # bf16/fp32 -> fp64 conversion of the inputs happens outside the timed region
-    sub = {k: (oracle._f64(v) if v is not None else None) for k, v in sub.items()}
-    t0 = time.perf_counter()
-    oracle.verify(sub, wl.gate, threads=cores)
-    dt = time.perf_counter() - t0
-    hs = n_seq * per_seq
+    sub = {k: (oracle._f64(v) if v is not None else None) for k, v in inputs_cpu.items()}
+    passes, dt = 0, 0.0
+    while passes == 0 or (dt * cores < cpu_seconds and passes < 64):
+        t0 = time.perf_counter()
+        oracle.verify(sub, wl.gate, threads=cores)
+        dt += time.perf_counter() - t0
+        passes += 1
+    hs = passes * s.head_steps
     return {"value": hs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n_seq} of {s.N} sequences of {wl.name} ({hs} head-steps), fp64 C oracle, "
-                      f"{cores} threads, {dt:.2f} s wall"}
+            "sample": f"{passes} full pass(es) over the {s.N} sequences of {wl.name} ({hs} head-steps), "
+                      f"fp64 C oracle, {cores} threads, {dt:.2f} s wall (~{dt * cores:.0f} s CPU)"}
 
 
 def run_reference(args, wl):
@@ -418,6 +417,8 @@ def run_sweep(args):
     rows = []
     sink = open(args.sweep_out, "w") if args.sweep_out else None
     for wl in wk.sweep():
+        if args.sweep_filter and not re.search(args.sweep_filter, wl.name):
+            continue
         s = wl.shape
         inp = wk.make_inputs_on_device(wl, dev)
         out = {k: v for k, v in wk.empty_outputs(wl, device=dev).items()}

@@ -165,6 +165,10 @@ typedef struct {
   int grid;
   int ctas_per_sm;
   long long items;
+  /* SMALL_BATCH: each CTA prefetches into L2 the inputs and state tile of the
+   * item this many items ahead (about one wave of resident CTAs).  In a plan
+   * given to kda_conv_verify_plan: < 0 off, 0 the default, > 0 explicit. */
+  int prefetch;
 } kda_plan;
 int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
 
@@ -172,8 +176,8 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
  * kda_make_plan and then edited.  Read from `plan`: variant (SMALL_BATCH or
  * LARGE_BATCH), bv (v-tile width: 16, 32, 64 or 128 for SMALL_BATCH; 32, 64
  * or 128 for LARGE_BATCH; at most V and dividing V) and, for LARGE_BATCH,
- * grid (persistent CTAs; <= 0 picks the default).  The other fields are
- * recomputed.  An invalid plan returns KDA_ERR_VARIANT.  Every plan produces
+ * grid (persistent CTAs; <= 0 picks the default), for SMALL_BATCH prefetch
+ * (see kda_plan).  The other fields are recomputed.  An invalid plan returns KDA_ERR_VARIANT.  Every plan produces
  * bit-identical outputs. */
 int kda_conv_verify_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
                          void* conv_state, const float* A_log, const float* dt_bias,

@@ -46,7 +46,8 @@ bool valid_tile_bv(int bv, int V) { return (bv == 16 || bv == 32 || bv == 64 || 
 bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
 
 // Fill the derived fields of a plan whose variant and bv are set.
-void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_grid) {
+void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_grid,
+                 int requested_prefetch) {
   const long long units = (long long)s->N * s->HV;
   const int ab = s->act == KDA_F32 ? 4 : 2;
   out->items = units * (s->V / out->bv);
@@ -62,6 +63,11 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
     const size_t smem = kda::tile_smem_bytes(s->T, s->K, out->bv);
     out->ctas_per_sm = ctas_per_sm_for(16 / out->warps, smem);
     out->grid = (int)std::max(1LL, out->items);
+    // 3/8 of a wave of resident CTAs ahead: measured on GB300, any distance
+    // between ~1/4 and ~5/8 of a wave is within 2 %; a full wave or more lets
+    // the streaming snapshot writes evict the prefetched lines before use
+    const int dist = std::max(1, num_sms * out->ctas_per_sm * 3 / 8);
+    out->prefetch = requested_prefetch < 0 ? 0 : (requested_prefetch > 0 ? requested_prefetch : dist);
   }
   if (units == 0) out->grid = 0;
 }
@@ -134,14 +140,13 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
   } else {
     // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
     // many threads for its producer tasks and the q/k conv is not repeated per
-    // v-tile.  Measured on GB300 over the 150-point sweep, half states
-    // (BV = 64) are a few per cent faster only for T <= 3 once every SM has
-    // several units.
+    // v-tile.  Measured on GB300 (with the L2 prefetch), half states (BV = 64)
+    // win only single-token verifies of grouped heads, by a few per cent.
     out->variant = KDA_VARIANT_SMALL_BATCH;
     out->bv = std::min(s->V, 128);
-    if (s->T <= 3 && units >= 4LL * num_sms && s->V >= 64) out->bv = 64;
+    if (s->T == 1 && s->HV > s->H && units >= 4LL * num_sms && s->V >= 64) out->bv = 64;
   }
-  finish_plan(s, num_sms, out, 0);
+  finish_plan(s, num_sms, out, 0, 0);
   return KDA_OK;
 }
 
@@ -236,6 +241,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.counters = static_cast<int*>(workspace);
   p.status = static_cast<int*>(workspace) + N * H;
   p.num_items = plan.items;
+  p.prefetch = plan.variant == KDA_VARIANT_SMALL_BATCH ? plan.prefetch : 0;
   p.N = s->N;
   p.T = s->T;
   p.H = s->H;
@@ -310,7 +316,7 @@ int kda_conv_verify_plan(const kda_shape* s, const void* mixed_qkv, const void* 
   rc = num_sms_of_current_device(&num_sms);
   if (rc) return rc;
   kda_plan p = *plan;
-  finish_plan(s, num_sms, &p, plan->grid);
+  finish_plan(s, num_sms, &p, plan->grid, plan->prefetch);
   return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
                      inter_ssm, conv_snapshots, workspace, p, stream);
 }

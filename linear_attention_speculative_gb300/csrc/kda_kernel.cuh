@@ -57,6 +57,7 @@ struct Params {
   int* counters;          // [N * H]
   int* status;            // device status word
   long long num_items;    // N * HV * nvt
+  long long prefetch;     // one-item-per-CTA kernel: L2-prefetch item + prefetch (0: off)
   int N, T, H, HV, V, dim, G, nvt;
   int gate_mode;          // 0 softplus, 1 safe
 };
@@ -495,6 +496,39 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
   }
 }
 
+// L2 prefetch of everything item `itm` reads from HBM: its state tile and its
+// raw input rows (q/k/v token rows, conv_state blocks, gate rows), spread over
+// the lanes of one warp.  Issued about one residency wave ahead, so the CTA
+// that later takes the item finds its inputs in L2.
+template <typename Act, int K, int BV>
+__device__ __forceinline__ void prefetch_item_l2(const Params& p, const CUtensorMap* tmap,
+                                                 long long itm, int lane) {
+  constexpr int AB = sizeof(Act);
+  const Item it = decode_item(p, itm);
+  const int T = p.T;
+  const int n_pf = 3 * T + 3 + T + 1;
+  for (int c = lane; c < n_pf; c += 32) {
+    if (c < 3 * T) {
+      const int t = c / 3, kind = c - 3 * t;
+      const char* src = static_cast<const char*>(p.mixed_qkv) +
+                        (((size_t)it.n * T + t) * p.dim + block_channel<K, BV>(p, it, kind)) * AB;
+      bulk_prefetch_l2(src, (kind == 2 ? BV : K) * AB);
+    } else if (c < 3 * T + 3) {
+      const int kind = c - 3 * T;
+      const char* src = static_cast<const char*>(p.conv_state) +
+                        ((size_t)it.n * p.dim + block_channel<K, BV>(p, it, kind)) * 3 * AB;
+      bulk_prefetch_l2(src, (kind == 2 ? BV : K) * 3 * AB);
+    } else if (c < 4 * T + 3) {
+      const int t = c - 3 * T - 3;
+      bulk_prefetch_l2(static_cast<const char*>(p.a) +
+                           ((((size_t)it.n * T + t) * p.HV + it.hv) * K) * AB,
+                       K * AB);
+    } else {
+      tma_prefetch_2d(tmap, it.vt * BV, static_cast<int>(it.unit * K));
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // one item per CTA: every warp produces, then consumes
 // ---------------------------------------------------------------------------
@@ -531,6 +565,8 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.unit * K), mbar,
                 l2_policy_evict_first());
   }
+  if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items)
+    prefetch_item_l2<Act, K, BV>(p, &tmap_s0, item + p.prefetch, lane);
   const GlobalSrc<Act, K, BV> src{p, it};
   produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, tid, NT);
   __syncthreads();  // every conv_state read of this CTA is done, stage written

@@ -43,7 +43,7 @@ class KdaShape(ctypes.Structure):
 class KdaPlan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bv", ctypes.c_int), ("warps", ctypes.c_int),
                 ("grid", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("items", ctypes.c_longlong)]
+                ("items", ctypes.c_longlong), ("prefetch", ctypes.c_int)]
 
 
 class KdaError(RuntimeError):
@@ -141,13 +141,15 @@ def _stream_handle(stream) -> ctypes.c_void_p:
 
 
 def parse_plan(spec: str) -> KdaPlan:
-    """'small:32' / 'large:64' / 'large:64:300' (variant, v-tile width, grid)."""
+    """'small:32' / 'large:64' / 'large:64:300' / 'small:128:0:-1' (variant,
+    v-tile width, grid, L2 prefetch distance: -1 off, 0 default)."""
     parts = spec.split(":")
     plan = KdaPlan()
     plan.variant = {"small": VARIANT_SMALL_BATCH, "small_batch": VARIANT_SMALL_BATCH,
                     "large": VARIANT_LARGE_BATCH, "large_batch": VARIANT_LARGE_BATCH}[parts[0]]
     plan.bv = int(parts[1])
     plan.grid = int(parts[2]) if len(parts) > 2 else 0
+    plan.prefetch = int(parts[3]) if len(parts) > 3 else 0
     return plan
 
 
