@@ -57,6 +57,8 @@ def parse():
                          "its sequences")
     ap.add_argument("--N", type=int, default=0,
                     help="override the number of sequences (small profiling cases)")
+    ap.add_argument("--op", default="verify", choices=["verify", "commit"],
+                    help="commit: time kda_commit (accept a random count per sequence) instead")
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the T x N x heads x gate sweep in both variants")
     ap.add_argument("--sweep-out", default="")
@@ -471,10 +473,52 @@ def run_sweep(args):
                           "worst_point": worst["workload"]}))
 
 
+def run_commit(args, wl):
+    """HBM bandwidth of kda_commit after one verify of the workload."""
+    import torch
+    from linear_attention_speculative_gb300 import kda
+    from linear_attention_speculative_gb300 import workloads as wk
+    dev = torch.device("cuda", 0)
+    s = wl.shape
+    inp = wk.make_inputs_on_device(wl, dev)
+    out = kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate)
+    g = torch.Generator(device=dev)
+    g.manual_seed(wl.seed)
+    acc = torch.randint(1, s.T + 1, (s.N,), generator=g, device=dev, dtype=torch.int32)
+    S = torch.empty_like(inp["S0"])
+    cs = torch.empty_like(inp["conv_state"])
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.commit(acc, out["inter_ssm"], out["conv_snapshots"], S, cs, stream=stream)
+    for _ in range(max(3, args.warmup)):
+        step()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    ev = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    us = 1e3 * sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
+    nbytes = 2 * s.N * (4 * s.HV * s.K * s.V + 3 * s.dim * s.act_bytes) + 4 * s.N
+    peak, src = measured_hbm_peak()
+    print(json.dumps({"op": "commit", "workload": wl.name, "us": us, "bytes": nbytes,
+                      "GB/s": nbytes / (us / 1e6) / 1e9, "frac": nbytes / (us / 1e6) / 1e9 / peak,
+                      "peak_source": src, "timing": "median of per-launch CUDA events, L2 flushed"}))
+
+
 def main():
     args = parse()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.op == "commit":
+        run_commit(args, workload(args.workload))
         return
     wl = workload(args.workload)
     if args.N:

@@ -86,6 +86,7 @@ typedef struct {
  * bounded wait (the kernel then returns without hanging the GPU). */
 #define KDA_STATUS_OK 0
 #define KDA_STATUS_TMA_TIMEOUT 1
+#define KDA_STATUS_BAD_ACCEPT 2  /* kda_commit: an accepted count outside [1, T] */
 
 /* The fused verify decode.
  *   s              problem shape (host pointer, read during the call only)
@@ -124,6 +125,28 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
                             kda_gate_mode gate_mode, void* o, float* inter_ssm,
                             void* conv_snapshots, void* workspace, size_t workspace_bytes,
                             kda_variant variant, kda_stream_t stream);
+
+/* Commit / rollback after a verify: accept the first accepted[n] tokens of
+ * every sequence ("[KDA] Fuse causal conv1d into MTP verify decode": the
+ * verify writes per-token state and conv-window snapshots for rollback).
+ * For each n with 1 <= accepted[n] <= T:
+ *   S[n]          <- inter_ssm[n, accepted[n]-1]        f32 [HV, K, V]
+ *   conv_state[n] <- conv_snapshots[n, accepted[n]-1]   act [dim, W-1]
+ *   s               the shape of the verify call (T = tokens verified)
+ *   accepted        int32 [N], device
+ *   inter_ssm       f32 [N, T, HV, K, V], conv_snapshots act [N, T, dim, W-1]:
+ *                   the verify's outputs (read)
+ *   S               f32 [N, HV, K, V] OUT (e.g. the persistent state the
+ *                   verify read as S0)
+ *   conv_state      act [N, dim, W-1] OUT
+ *   status          optional device int: KDA_STATUS_BAD_ACCEPT is OR-ed in
+ *                   when a count is out of range; that sequence is left
+ *                   untouched.  May be NULL.
+ * A pure HBM copy, asynchronous on `stream`.  Outputs must not overlap the
+ * inputs.  Returns 0, a negative KDA_ERR_* code, or a cudaError_t. */
+int kda_commit(const kda_shape* s, const int32_t* accepted, const float* inter_ssm,
+               const void* conv_snapshots, float* S, void* conv_state, int* status,
+               kda_stream_t stream);
 
 /* Allocation-free variant of kda_conv_verify.  The verify-decode page has no
  * counterpart: this entry point exists for callers that cannot allocate

@@ -1,0 +1,118 @@
+// kda_commit.cu -- kda_commit: accept the first acc[n] verified tokens of
+// every sequence ("[KDA] Fuse causal conv1d into MTP verify decode", cuLA pull
+// request 107: the verify writes per-token state and conv-window snapshots
+// "for rollback"; this is that rollback / commit step).
+//
+// For each sequence n with 1 <= acc[n] <= T:
+//     S[n]          <- inter_ssm[n, acc[n]-1]        (fp32, HV x K x V)
+//     conv_state[n] <- conv_snapshots[n, acc[n]-1]   (act, dim x 3)
+// A pure HBM copy: one 16-byte streaming load and store per vector over a
+// flat, non-persistent grid.  Sequences whose count is out of range are left
+// untouched and reported in the status word.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+
+#include "kda_device.cuh"
+#include "../../include/kda_verify.h"
+
+namespace {
+
+constexpr int kCommitThreads = 256;
+constexpr int kCommitUnroll = 4;
+
+struct CommitParams {
+  const int32_t* acc;
+  const float* inter_ssm;
+  const unsigned char* snaps;
+  float* S;
+  unsigned char* conv_state;
+  int* status;
+  long long state_vecs;  // 16-byte vectors of one sequence's state (HV*K*V/4)
+  long long conv_vecs;   // 16-byte vectors of one sequence's conv window
+  long long total;       // N * (state_vecs + conv_vecs)
+  int T;
+};
+
+__global__ void __launch_bounds__(kCommitThreads) kda_commit_kernel(const CommitParams p) {
+  const long long per_seq = p.state_vecs + p.conv_vecs;
+  const long long base = (long long)blockIdx.x * kCommitThreads * kCommitUnroll + threadIdx.x;
+#pragma unroll
+  for (int u = 0; u < kCommitUnroll; ++u) {
+    const long long v = base + (long long)u * kCommitThreads;
+    if (v >= p.total) return;
+    const long long n = v / per_seq;
+    const long long r = v - n * per_seq;
+    const int a = __ldg(p.acc + n);
+    if (a < 1 || a > p.T) {
+      if (r == 0 && p.status) atomicOr(p.status, KDA_STATUS_BAD_ACCEPT);
+      continue;
+    }
+    if (r < p.state_vecs) {
+      const float4* src = reinterpret_cast<const float4*>(p.inter_ssm) +
+                          ((n * p.T + (a - 1)) * p.state_vecs + r);
+      float4* dst = reinterpret_cast<float4*>(p.S) + (n * p.state_vecs + r);
+      __stcs(dst, __ldcs(src));
+    } else {
+      const long long c = r - p.state_vecs;
+      const uint4* src = reinterpret_cast<const uint4*>(p.snaps) + ((n * p.T + (a - 1)) * p.conv_vecs + c);
+      uint4* dst = reinterpret_cast<uint4*>(p.conv_state) + (n * p.conv_vecs + c);
+      __stcs(dst, __ldcs(src));
+    }
+  }
+}
+
+bool overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
+  return na && nb && a < b + nb && b < a + na;
+}
+
+}  // namespace
+
+extern "C" int kda_commit(const kda_shape* s, const int32_t* accepted, const float* inter_ssm,
+                          const void* conv_snapshots, float* S, void* conv_state, int* status,
+                          kda_stream_t stream) {
+  if (!s) return KDA_ERR_NULL;
+  if (s->act != KDA_F32 && s->act != KDA_BF16) return KDA_ERR_DTYPE;
+  if (s->N < 0 || s->T < 1 || s->T > KDA_MAX_T || s->H < 1 || s->HV < s->H ||
+      s->HV % s->H != 0 || s->W != 4 || (s->K != 32 && s->K != 64 && s->K != 128) ||
+      (s->V != 32 && s->V != 64 && s->V != 128))
+    return KDA_ERR_SHAPE;
+  if (s->N == 0) return KDA_OK;
+  if (!accepted || !inter_ssm || !conv_snapshots || !S || !conv_state) return KDA_ERR_NULL;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al16(inter_ssm) || !al16(conv_snapshots) || !al16(S) || !al16(conv_state) ||
+      (reinterpret_cast<uintptr_t>(accepted) & 3u) || (reinterpret_cast<uintptr_t>(status) & 3u))
+    return KDA_ERR_MISALIGNED;
+  const size_t ab = s->act == KDA_F32 ? 4 : 2;
+  const size_t N = s->N, T = s->T, HV = s->HV, K = s->K, V = s->V;
+  const size_t dim = 2 * (size_t)s->H * K + HV * V;
+  const uintptr_t in[3][2] = {{reinterpret_cast<uintptr_t>(accepted), N * 4},
+                              {reinterpret_cast<uintptr_t>(inter_ssm), N * T * HV * K * V * 4},
+                              {reinterpret_cast<uintptr_t>(conv_snapshots), N * T * dim * 3 * ab}};
+  const uintptr_t out[3][2] = {{reinterpret_cast<uintptr_t>(S), N * HV * K * V * 4},
+                               {reinterpret_cast<uintptr_t>(conv_state), N * dim * 3 * ab},
+                               {reinterpret_cast<uintptr_t>(status), status ? 4u : 0u}};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 3; ++j)
+      if (overlap(out[i][0], out[i][1], in[j][0], in[j][1])) return KDA_ERR_ALIAS;
+    for (int j = 0; j < 3; ++j)
+      if (j != i && overlap(out[i][0], out[i][1], out[j][0], out[j][1])) return KDA_ERR_ALIAS;
+  }
+  CommitParams p;
+  p.acc = accepted;
+  p.inter_ssm = inter_ssm;
+  p.snaps = static_cast<const unsigned char*>(conv_snapshots);
+  p.S = S;
+  p.conv_state = static_cast<unsigned char*>(conv_state);
+  p.status = status;
+  p.state_vecs = (long long)(HV * K * V / 4);
+  p.conv_vecs = (long long)(dim * 3 * ab / 16);
+  p.total = (long long)N * (p.state_vecs + p.conv_vecs);
+  p.T = s->T;
+  const long long per_block = (long long)kCommitThreads * kCommitUnroll;
+  const long long blocks = (p.total + per_block - 1) / per_block;
+  if (blocks > 0x7fffffffLL) return KDA_ERR_SHAPE;
+  kda_commit_kernel<<<(unsigned)blocks, kCommitThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  return static_cast<int>(cudaGetLastError());
+}

@@ -29,7 +29,7 @@ MAX_T = 16
 
 # The names declared in include/kda_verify.h.
 EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan",
-            "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan",
+            "kda_commit", "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan",
             "kda_read_status", "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
@@ -73,6 +73,8 @@ def _load():
     L.kda_conv_verify_variant.argtypes = args_common + [ctypes.c_int, vp]
     L.kda_conv_verify_plan.restype = ctypes.c_int
     L.kda_conv_verify_plan.argtypes = args_common + [ctypes.POINTER(KdaPlan), vp]
+    L.kda_commit.restype = ctypes.c_int
+    L.kda_commit.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
     L.kda_conv_verify_noalloc.restype = ctypes.c_int
     L.kda_conv_verify_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                           vp, vp, vp, vp]
@@ -192,6 +194,26 @@ def conv_verify_noalloc(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0,
         _ptr(conv_snapshots), _stream_handle(stream))
     if rc != 0:
         raise KdaError(rc, "kda_conv_verify_noalloc")
+
+
+STATUS_TMA_TIMEOUT = 1
+STATUS_BAD_ACCEPT = 2
+
+
+def commit(accepted, inter_ssm, conv_snapshots, S, conv_state, status=None, stream=None,
+           shape: Optional[KdaShape] = None) -> None:
+    """Accept accepted[n] (int32, device) verified tokens of every sequence:
+    S[n] <- inter_ssm[n, acc-1], conv_state[n] <- conv_snapshots[n, acc-1]."""
+    if shape is None:
+        N, T, HV, K, V = inter_ssm.shape
+        dim = conv_snapshots.shape[2]
+        H = (dim - HV * V) // (2 * K)
+        shape = make_shape(N, T, H, HV, K, V, conv_snapshots.dtype)
+    rc = lib().kda_commit(ctypes.byref(shape), _ptr(accepted), _ptr(inter_ssm),
+                          _ptr(conv_snapshots), _ptr(S), _ptr(conv_state), _ptr(status),
+                          _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_commit")
 
 
 def read_status(shape: KdaShape, workspace: torch.Tensor, stream=None) -> int:

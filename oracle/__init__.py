@@ -66,6 +66,8 @@ def lib():
             L.orc_delta_rule_step.restype = None
             L.orc_delta_rule_step.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp,
                                               ctypes.c_double, _dp, ctypes.c_double, _dp]
+            L.orc_commit_seq.restype = ctypes.c_int
+            L.orc_commit_seq.argtypes = [ctypes.c_int] * 7 + [_dp] * 4
             L.orc_kda_conv_verify_seq.restype = ctypes.c_int
             L.orc_kda_conv_verify_seq.argtypes = ([ctypes.c_int] * 7 + [ctypes.c_double]
                                                   + [_dp] * 12)
@@ -197,3 +199,22 @@ def verify(inputs: Dict, gate: str, seqs: Optional[Iterable[int]] = None,
     if bad:
         raise ValueError(f"oracle rejected the call (code {bad[0]})")
     return out
+
+
+def commit(acc, inter_ssm, conv_snapshots) -> Dict[str, np.ndarray]:
+    """Accept acc[n] tokens of every sequence: returns the committed state
+    S [N,HV,K,V] and conv_state [N,dim,W-1] (float64)."""
+    L = lib()
+    inter = _f64(inter_ssm)
+    snap = _f64(conv_snapshots)
+    N, T, HV, K, V = inter.shape
+    dim, W1 = snap.shape[2], snap.shape[3]
+    acc = [int(a) for a in (acc.tolist() if hasattr(acc, "tolist") else acc)]
+    S = np.empty((N, HV, K, V))
+    cs = np.empty((N, dim, W1))
+    for n in range(N):
+        rc = L.orc_commit_seq(T, HV, K, V, dim, W1 + 1, acc[n], _ptr(inter[n]), _ptr(snap[n]),
+                              _ptr(S[n]), _ptr(cs[n]))
+        if rc != 0:
+            raise ValueError(f"oracle commit rejected acc[{n}] = {acc[n]}")
+    return {"S": S, "conv_state": cs}

@@ -209,3 +209,21 @@ int orc_kda_conv_verify_seq(int T, int H, int HV, int K, int V, int W,
   free(y); free(xext); free(yc); free(S); free(qn); free(kn); free(g);
   return ORC_OK;
 }
+
+/* ---- commit after verify ------------------------------------------------- */
+
+/* Accept the first `acc` (1 <= acc <= T) verified tokens of ONE sequence:
+ * the persistent state becomes the state snapshot after token acc-1 and the
+ * conv_state becomes the conv-window snapshot after token acc-1 (the rollback
+ * the per-token snapshots exist for, per the verify-decode page).
+ *   inter   [T][HV][K][V],  snap [T][dim][W-1]  (this sequence's snapshots)
+ *   S_out   [HV][K][V],     cs_out [dim][W-1]
+ * Returns ORC_EBADARG (and writes nothing) when acc is out of range. */
+int orc_commit_seq(int T, int HV, int K, int V, int dim, int W, int acc, const double* inter,
+                   const double* snap, double* S_out, double* cs_out) {
+  if (acc < 1 || acc > T) return ORC_EBADARG;
+  const size_t ns = (size_t)HV * K * V, nc = (size_t)dim * (W - 1);
+  memcpy(S_out, inter + (size_t)(acc - 1) * ns, sizeof(double) * ns);
+  memcpy(cs_out, snap + (size_t)(acc - 1) * nc, sizeof(double) * nc);
+  return ORC_OK;
+}

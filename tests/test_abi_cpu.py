@@ -200,3 +200,24 @@ def test_valid_arguments_reach_the_device_query(kda):
     import torch
     if not torch.cuda.is_available():
         assert rc > 0
+
+
+# ---- kda_commit argument checks (fake pointers, nothing launched) -----------
+
+def _commit(kda, shape, acc=0x7f0000000000, inter=0x7f0100000000, snaps=0x7f0200000000,
+            S=0x7f0300000000, cs=0x7f0400000000, status=None):
+    L = kda.lib()
+    v = lambda x: ctypes.c_void_p(x) if x is not None else None
+    return L.kda_commit(ctypes.byref(shape), v(acc), v(inter), v(snaps), v(S), v(cs), v(status), None)
+
+
+def test_commit_rejects_bad_arguments(kda):
+    s = kda.make_shape(4, 3, 2, 2, 32, 32)
+    assert _commit(kda, s, acc=None) == -1
+    assert _commit(kda, s, S=None) == -1
+    assert _commit(kda, s, inter=0x7f0100000008) == -4
+    assert _commit(kda, s, acc=0x7f0000000002) == -4
+    assert _commit(kda, s, S=0x7f0100000000 + 4096) == -5   # state out inside inter_ssm
+    assert _commit(kda, s, cs=0x7f0300000000 + 16) == -5     # two outputs overlap
+    assert _commit(kda, kda.make_shape(4, 0, 2, 2, 32, 32)) == -2
+    assert _commit(kda, kda.make_shape(0, 3, 2, 2, 32, 32), acc=None, S=None) == 0

@@ -1,0 +1,82 @@
+"""GPU parity of kda_commit (accept the first acc[n] verified tokens).
+
+Pure copies, so the check is bit-exact: against the CPU oracle's commit, and
+against the identity that a T-token verify followed by commit(a) equals a
+verify of the first a tokens alone."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_speculative_gb300 import workloads as wk
+from parity_util import to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from linear_attention_speculative_gb300 import kda
+    kda.lib()
+
+
+@pytest.mark.parametrize("act", ["bf16", "f32"])
+def test_commit_matches_oracle_and_reports_bad_counts(act):
+    from linear_attention_speculative_gb300 import kda
+    T = 4
+    wl = wk.custom(9, T, 2, 4, 128, 64, act=act, seed=71)
+    inp = to_device(wk.make_inputs(wl))
+    out = kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate)
+    acc = torch.tensor([1, 2, 3, 4, 4, 0, 5, -1, 2], dtype=torch.int32, device="cuda")
+    S = torch.full_like(inp["S0"], 7.0)
+    cs = torch.full_like(inp["conv_state"], 3.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.commit(acc, out["inter_ssm"], out["conv_snapshots"], S, cs, status=status)
+    torch.cuda.synchronize()
+    good = [i for i, a in enumerate(acc.tolist()) if 1 <= a <= T]
+    bad = [i for i in range(9) if i not in good]
+    ref = oracle.commit([acc.tolist()[i] for i in good], out["inter_ssm"][good].cpu(),
+                        out["conv_snapshots"][good].cpu())
+    np.testing.assert_array_equal(S[good].double().cpu().numpy(), ref["S"])
+    np.testing.assert_array_equal(cs[good].double().cpu().numpy(), ref["conv_state"])
+    assert bool((S[bad] == 7.0).all()) and bool((cs[bad] == 3.0).all())  # untouched
+    assert int(status.item()) == kda.STATUS_BAD_ACCEPT
+
+
+@pytest.mark.parametrize("gate", ["softplus", "safe"])
+def test_verify_then_commit_equals_verify_of_the_prefix(gate):
+    from linear_attention_speculative_gb300 import kda
+    T = 5
+    wl = wk.custom(5, T, 2, 4, 128, 128, gate=gate, seed=72)
+    inp = to_device(wk.make_inputs(wl))
+    full = kda.run(dict(inp, conv_state=inp["conv_state"].clone()), gate)
+    acc = torch.tensor([1, 2, 3, 4, 5], dtype=torch.int32, device="cuda")
+    S = torch.empty_like(inp["S0"])
+    cs = torch.empty_like(inp["conv_state"])
+    kda.commit(acc, full["inter_ssm"], full["conv_snapshots"], S, cs)
+    for n, a in enumerate(acc.tolist()):
+        pre = dict(inp)
+        for key in ("mixed_qkv", "a", "b"):
+            pre[key] = inp[key][n:n + 1, :a].contiguous()
+        pre["S0"] = inp["S0"][n:n + 1].contiguous()
+        pre["conv_state"] = inp["conv_state"][n:n + 1].clone()
+        ref = kda.run(pre, gate)
+        torch.cuda.synchronize()
+        assert torch.equal(S[n], ref["inter_ssm"][0, a - 1])
+        assert torch.equal(cs[n], pre["conv_state"][0])
+
+
+def test_commit_in_place_into_the_verified_state():
+    # the usual chain: verify reads S0, commit writes the accepted state back into S0
+    from linear_attention_speculative_gb300 import kda
+    wl = wk.custom(4, 3, 2, 2, 128, 128, seed=73)
+    inp = to_device(wk.make_inputs(wl))
+    out = kda.run(inp, wl.gate)
+    acc = torch.tensor([3, 1, 2, 3], dtype=torch.int32, device="cuda")
+    kda.commit(acc, out["inter_ssm"], out["conv_snapshots"], inp["S0"], inp["conv_state"])
+    torch.cuda.synchronize()
+    for n, a in enumerate(acc.tolist()):
+        assert torch.equal(inp["S0"][n], out["inter_ssm"][n, a - 1])
+        assert torch.equal(inp["conv_state"][n], out["conv_snapshots"][n, a - 1])

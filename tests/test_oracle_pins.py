@@ -346,3 +346,40 @@ def test_frozen_tiny_fp32_values():
     out = oracle.verify(wk.make_inputs(wk.TINY), wk.TINY.gate)
     for (key, idx), val in stored.items():
         assert out[key][idx] == pytest.approx(val, rel=1e-12, abs=1e-15), (key, idx)
+
+
+# ---- commit after verify ----------------------------------------------------
+
+@pytest.mark.parametrize("gate", ["softplus", "safe"])
+def test_commit_equals_verify_of_the_accepted_prefix(gate):
+    # verify T tokens, then accept a of them == verify only the first a tokens
+    T = 4
+    wl, inp = _tiny(N=4, T=T, H=1, HV=2, K=8, V=4, gate=gate, seed=61)
+    full = oracle.verify(inp, gate)
+    acc = [1, 2, 3, 4]
+    com = oracle.commit(acc, full["inter_ssm"], full["conv_snapshots"])
+    for n, a in enumerate(acc):
+        pre = dict(inp)
+        for key in ("mixed_qkv", "a", "b"):
+            pre[key] = inp[key][n:n + 1, :a]
+        for key in ("conv_state", "S0"):
+            pre[key] = inp[key][n:n + 1]
+        ref = oracle.verify(pre, gate)
+        np.testing.assert_array_equal(com["S"][n], ref["inter_ssm"][0, a - 1])
+        np.testing.assert_array_equal(com["conv_state"][n], ref["conv_state"][0])
+
+
+def test_commit_of_every_token_is_the_rolled_state():
+    wl, inp = _tiny(N=2, T=3, H=1, HV=1, K=4, V=4, seed=62)
+    full = oracle.verify(inp, "softplus")
+    com = oracle.commit([3, 3], full["inter_ssm"], full["conv_snapshots"])
+    np.testing.assert_array_equal(com["conv_state"], full["conv_state"])
+    np.testing.assert_array_equal(com["S"], full["inter_ssm"][:, -1])
+
+
+def test_commit_rejects_out_of_range_counts():
+    wl, inp = _tiny(N=2, T=3, H=1, HV=1, K=4, V=4, seed=63)
+    full = oracle.verify(inp, "softplus")
+    for bad in ([0, 1], [1, 4], [-1, 2]):
+        with pytest.raises(ValueError):
+            oracle.commit(bad, full["inter_ssm"], full["conv_snapshots"])
