@@ -68,6 +68,20 @@ typedef struct {
 
 #define KDA_MAX_T 16
 
+/* A launch plan (see kda_make_plan and kda_conv_verify_plan). */
+typedef struct {
+  int variant;
+  int bv;
+  int warps;
+  int grid;
+  int ctas_per_sm;
+  long long items;
+  /* SMALL_BATCH: each CTA prefetches into L2 the inputs and state tile of the
+   * item this many items ahead (about one wave of resident CTAs).  In a plan
+   * given to kda_conv_verify_plan: < 0 off, 0 the default, > 0 explicit. */
+  int prefetch;
+} kda_plan;
+
 /* Error codes (negative: rejected on the host, nothing launched). */
 #define KDA_OK 0
 #define KDA_ERR_NULL (-1)        /* a required pointer is NULL */
@@ -87,6 +101,7 @@ typedef struct {
 #define KDA_STATUS_OK 0
 #define KDA_STATUS_TMA_TIMEOUT 1
 #define KDA_STATUS_BAD_ACCEPT 2  /* kda_commit: an accepted count outside [1, T] */
+#define KDA_STATUS_BAD_INDEX 4   /* a state-pool slot >= its pool size (sequence skipped) */
 
 /* The fused verify decode.
  *   s              problem shape (host pointer, read during the call only)
@@ -126,6 +141,43 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
                             void* conv_snapshots, void* workspace, size_t workspace_bytes,
                             kda_variant variant, kda_stream_t stream);
 
+/* State-pool indirection ("[KDA] Fuse causal conv1d into MTP verify decode":
+ * conv_state_indices, cache_indices and intermediate_state_indices are
+ * normalised independently).  Each array is int32 [N] on the device, or NULL
+ * for the identity (slot = n, pool of N slots):
+ *   cache_indices               slot of sequence n's persistent state in the
+ *                               S0 pool  f32 [state_pool, HV, K, V]
+ *   conv_state_indices          slot of its conv window in the conv_state pool
+ *                               act [conv_pool, dim, W-1]
+ *   intermediate_state_indices  slot of its snapshots in the inter_ssm pool
+ *                               f32 [inter_pool, T, HV, K, V] and the
+ *                               conv_snapshots pool act [inter_pool, T, dim, W-1]
+ * A negative slot in any array marks a padding sequence: nothing of it is read
+ * or written (its o rows are left untouched).  A slot >= its pool size skips
+ * the sequence the same way and sets KDA_STATUS_BAD_INDEX in the workspace
+ * status word.  Two live sequences must not share a slot. */
+typedef struct {
+  const int32_t* cache_indices;
+  const int32_t* conv_state_indices;
+  const int32_t* intermediate_state_indices;
+  int state_pool;  /* slots in the S0 pool (used when cache_indices != NULL) */
+  int conv_pool;   /* slots in the conv_state pool */
+  int inter_pool;  /* slots in the inter_ssm / conv_snapshots pools */
+} kda_state_indices;
+
+/* kda_conv_verify over state pools: conv_state, S0, inter_ssm and
+ * conv_snapshots are the pools described by `idx` (NULL = dense, as
+ * kda_conv_verify); mixed_qkv, a, b and o stay dense [N, ...].  `plan` may be
+ * NULL (the dispatcher's choice) or an explicit plan as for
+ * kda_conv_verify_plan.  Outputs of every plan are bit-identical to the dense
+ * call on the gathered inputs. */
+int kda_conv_verify_indexed(const kda_shape* s, const kda_state_indices* idx,
+                            const void* mixed_qkv, const void* conv_w, void* conv_state,
+                            const float* A_log, const float* dt_bias, const void* a,
+                            const void* b, const float* S0, kda_gate_mode gate_mode, void* o,
+                            float* inter_ssm, void* conv_snapshots, void* workspace,
+                            size_t workspace_bytes, const kda_plan* plan, kda_stream_t stream);
+
 /* Commit / rollback after a verify: accept the first accepted[n] tokens of
  * every sequence ("[KDA] Fuse causal conv1d into MTP verify decode": the
  * verify writes per-token state and conv-window snapshots for rollback).
@@ -147,6 +199,16 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
 int kda_commit(const kda_shape* s, const int32_t* accepted, const float* inter_ssm,
                const void* conv_snapshots, float* S, void* conv_state, int* status,
                kda_stream_t stream);
+
+/* kda_commit over state pools: reads the snapshots of sequence n from slot
+ * intermediate_state_indices[n] of the inter_ssm / conv_snapshots pools and
+ * writes S slot cache_indices[n] and conv_state slot conv_state_indices[n]
+ * (NULL arrays: identity).  Padding (negative) slots are skipped; slots beyond
+ * a pool skip the sequence and set KDA_STATUS_BAD_INDEX in *status. */
+int kda_commit_indexed(const kda_shape* s, const kda_state_indices* idx,
+                       const int32_t* accepted, const float* inter_ssm,
+                       const void* conv_snapshots, float* S, void* conv_state, int* status,
+                       kda_stream_t stream);
 
 /* Allocation-free variant of kda_conv_verify.  The verify-decode page has no
  * counterpart: this entry point exists for callers that cannot allocate
@@ -181,18 +243,6 @@ size_t kda_workspace_bytes(const kda_shape* s);
  *   variant   requested variant (AUTO lets the dispatcher decide)
  * Out: chosen variant, v-tile width bv (columns of V per CTA), warps per
  * CTA, grid size.  Returns 0 or a negative KDA_ERR_* code. */
-typedef struct {
-  int variant;
-  int bv;
-  int warps;
-  int grid;
-  int ctas_per_sm;
-  long long items;
-  /* SMALL_BATCH: each CTA prefetches into L2 the inputs and state tile of the
-   * item this many items ahead (about one wave of resident CTAs).  In a plan
-   * given to kda_conv_verify_plan: < 0 off, 0 the default, > 0 explicit. */
-  int prefetch;
-} kda_plan;
 int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
 
 /* Same as kda_conv_verify with an explicit launch plan, e.g. one returned by

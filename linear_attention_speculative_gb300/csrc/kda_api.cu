@@ -155,11 +155,43 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
 namespace {
 
 // Every host-side check of one call (nothing touches the GPU).
+// Slots of the three state pools (identity and N slots for the dense calls).
+struct Pools {
+  const int32_t* idx_state = nullptr;
+  const int32_t* idx_conv = nullptr;
+  const int32_t* idx_inter = nullptr;
+  size_t n_state = 0, n_conv = 0, n_inter = 0;
+};
+
+Pools dense_pools(const kda_shape* s) {
+  Pools pl;
+  pl.n_state = pl.n_conv = pl.n_inter = (size_t)std::max(0, s->N);
+  return pl;
+}
+
+int pools_from(const kda_shape* s, const kda_state_indices* idx, Pools* out) {
+  *out = dense_pools(s);
+  if (!idx) return KDA_OK;
+  auto one = [&](const int32_t* ix, int pool, const int32_t** dst, size_t* n) {
+    if (!ix) return KDA_OK;
+    if (pool < 1) return KDA_ERR_SHAPE;
+    if (reinterpret_cast<uintptr_t>(ix) & 3u) return KDA_ERR_MISALIGNED;
+    *dst = ix;
+    *n = (size_t)pool;
+    return KDA_OK;
+  };
+  int rc = one(idx->cache_indices, idx->state_pool, &out->idx_state, &out->n_state);
+  if (!rc) rc = one(idx->conv_state_indices, idx->conv_pool, &out->idx_conv, &out->n_conv);
+  if (!rc) rc = one(idx->intermediate_state_indices, idx->inter_pool, &out->idx_inter, &out->n_inter);
+  if (!rc && (long long)out->n_state * s->HV * s->K >= (1ll << 31)) rc = KDA_ERR_SHAPE;
+  return rc;
+}
+
 int validate_call(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
                   void* conv_state, const float* A_log, const float* dt_bias, const void* a,
                   const void* b, const float* S0, kda_gate_mode gate_mode, void* o,
                   float* inter_ssm, void* conv_snapshots, void* workspace,
-                  size_t workspace_bytes) {
+                  size_t workspace_bytes, const Pools& pl) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (gate_mode != KDA_GATE_SOFTPLUS && gate_mode != KDA_GATE_SAFE) return KDA_ERR_GATE;
@@ -191,10 +223,12 @@ int validate_call(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
       span(mixed_qkv, N * T * dim * ab), span(conv_w, dim * 4 * ab),
       span(gate_mode == KDA_GATE_SOFTPLUS ? A_log : nullptr, HV * 4),
       span(gate_mode == KDA_GATE_SOFTPLUS ? dt_bias : nullptr, HV * K * 4),
-      span(a, N * T * HV * K * ab), span(b, N * T * HV * ab), span(S0, N * HV * K * V * 4)};
-  const Span wr[] = {span(conv_state, N * dim * 3 * ab), span(o, N * T * HV * V * ab),
-                     span(inter_ssm, N * T * HV * K * V * 4),
-                     span(conv_snapshots, N * T * dim * 3 * ab),
+      span(a, N * T * HV * K * ab), span(b, N * T * HV * ab),
+      span(S0, pl.n_state * HV * K * V * 4), span(pl.idx_state, N * 4), span(pl.idx_conv, N * 4),
+      span(pl.idx_inter, N * 4)};
+  const Span wr[] = {span(conv_state, pl.n_conv * dim * 3 * ab), span(o, N * T * HV * V * ab),
+                     span(inter_ssm, pl.n_inter * T * HV * K * V * 4),
+                     span(conv_snapshots, pl.n_inter * T * dim * 3 * ab),
                      span(workspace, kda_workspace_bytes(s))};
   for (size_t i = 0; i < sizeof(wr) / sizeof(wr[0]); ++i) {
     for (const Span& x : in)
@@ -209,7 +243,7 @@ int validate_call(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
 int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, void* conv_state,
                 const float* A_log, const float* dt_bias, const void* a, const void* b,
                 const float* S0, kda_gate_mode gate_mode, void* o, float* inter_ssm,
-                void* conv_snapshots, void* workspace, const kda_plan& plan,
+                void* conv_snapshots, void* workspace, const kda_plan& plan, const Pools& pl,
                 kda_stream_t stream) {
   const size_t N = s->N, H = s->H, HV = s->HV, K = s->K, V = s->V;
   const size_t dim = 2 * H * K + HV * V;
@@ -217,7 +251,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   if (!encode) return KDA_ERR_DEVICE;
   CUtensorMap tmap;
   std::memset(&tmap, 0, sizeof(tmap));
-  cuuint64_t gdim[2] = {(cuuint64_t)V, (cuuint64_t)(N * HV * K)};
+  cuuint64_t gdim[2] = {(cuuint64_t)V, (cuuint64_t)(pl.n_state * HV * K)};
   cuuint64_t gstride[1] = {(cuuint64_t)(V * sizeof(float))};
   cuuint32_t box[2] = {(cuuint32_t)plan.bv, (cuuint32_t)K};
   cuuint32_t estride[2] = {1, 1};
@@ -242,6 +276,12 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.status = static_cast<int*>(workspace) + N * H;
   p.num_items = plan.items;
   p.prefetch = plan.variant == KDA_VARIANT_SMALL_BATCH ? plan.prefetch : 0;
+  p.idx_state = pl.idx_state;
+  p.idx_conv = pl.idx_conv;
+  p.idx_inter = pl.idx_inter;
+  p.pool_state = (int)pl.n_state;
+  p.pool_conv = (int)pl.n_conv;
+  p.pool_inter = (int)pl.n_inter;
   p.N = s->N;
   p.T = s->T;
   p.H = s->H;
@@ -283,8 +323,10 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
   if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
       variant != KDA_VARIANT_LARGE_BATCH)
     return KDA_ERR_VARIANT;
+  if (!s) return KDA_ERR_NULL;
+  const Pools pl = dense_pools(s);
   int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
-                         o, inter_ssm, conv_snapshots, workspace, workspace_bytes);
+                         o, inter_ssm, conv_snapshots, workspace, workspace_bytes, pl);
   if (rc || s->N == 0) return rc;
   int num_sms = 0;
   rc = num_sms_of_current_device(&num_sms);
@@ -293,32 +335,75 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
   rc = kda_make_plan(s, num_sms, variant, &plan);
   if (rc) return rc;
   return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
-                     inter_ssm, conv_snapshots, workspace, plan, stream);
+                     inter_ssm, conv_snapshots, workspace, plan, pl, stream);
 }
+
+}  // extern "C"
+
+namespace {
+
+// Shared tail of the explicit-plan and indexed entry points.
+int verify_with(const kda_shape* s, const Pools& pl, const void* mixed_qkv, const void* conv_w,
+                void* conv_state, const float* A_log, const float* dt_bias, const void* a,
+                const void* b, const float* S0, kda_gate_mode gate_mode, void* o, float* inter_ssm,
+                void* conv_snapshots, void* workspace, size_t workspace_bytes, const kda_plan* plan,
+                kda_stream_t stream) {
+  int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
+                         o, inter_ssm, conv_snapshots, workspace, workspace_bytes, pl);
+  if (rc || s->N == 0) return rc;
+  if (plan) {
+    if (plan->variant == KDA_VARIANT_SMALL_BATCH) {
+      if (!valid_tile_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
+    } else if (plan->variant == KDA_VARIANT_LARGE_BATCH) {
+      if (!valid_ws_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
+    } else {
+      return KDA_ERR_VARIANT;
+    }
+  }
+  int num_sms = 0;
+  rc = num_sms_of_current_device(&num_sms);
+  if (rc) return rc;
+  kda_plan p;
+  if (!plan) {
+    rc = kda_make_plan(s, num_sms, KDA_VARIANT_AUTO, &p);
+    if (rc) return rc;
+  } else {
+    p = *plan;
+    finish_plan(s, num_sms, &p, plan->grid, plan->prefetch);
+  }
+  return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
+                     inter_ssm, conv_snapshots, workspace, p, pl, stream);
+}
+
+}  // namespace
+
+extern "C" {
 
 int kda_conv_verify_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
                          void* conv_state, const float* A_log, const float* dt_bias,
                          const void* a, const void* b, const float* S0, kda_gate_mode gate_mode,
                          void* o, float* inter_ssm, void* conv_snapshots, void* workspace,
                          size_t workspace_bytes, const kda_plan* plan, kda_stream_t stream) {
-  if (!plan) return KDA_ERR_NULL;
-  int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
-                         o, inter_ssm, conv_snapshots, workspace, workspace_bytes);
-  if (rc || s->N == 0) return rc;
-  if (plan->variant == KDA_VARIANT_SMALL_BATCH) {
-    if (!valid_tile_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
-  } else if (plan->variant == KDA_VARIANT_LARGE_BATCH) {
-    if (!valid_ws_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
-  } else {
-    return KDA_ERR_VARIANT;
-  }
-  int num_sms = 0;
-  rc = num_sms_of_current_device(&num_sms);
+  if (!plan || !s) return KDA_ERR_NULL;
+  return verify_with(s, dense_pools(s), mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0,
+                     gate_mode, o, inter_ssm, conv_snapshots, workspace, workspace_bytes, plan,
+                     stream);
+}
+
+int kda_conv_verify_indexed(const kda_shape* s, const kda_state_indices* idx,
+                            const void* mixed_qkv, const void* conv_w, void* conv_state,
+                            const float* A_log, const float* dt_bias, const void* a,
+                            const void* b, const float* S0, kda_gate_mode gate_mode, void* o,
+                            float* inter_ssm, void* conv_snapshots, void* workspace,
+                            size_t workspace_bytes, const kda_plan* plan, kda_stream_t stream) {
+  if (!s) return KDA_ERR_NULL;
+  int rc = check_shape(s);
   if (rc) return rc;
-  kda_plan p = *plan;
-  finish_plan(s, num_sms, &p, plan->grid, plan->prefetch);
-  return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
-                     inter_ssm, conv_snapshots, workspace, p, stream);
+  Pools pl;
+  rc = pools_from(s, idx, &pl);
+  if (rc) return rc;
+  return verify_with(s, pl, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
+                     inter_ssm, conv_snapshots, workspace, workspace_bytes, plan, stream);
 }
 
 int kda_conv_verify(const kda_shape* s, const void* mixed_qkv, const void* conv_w,

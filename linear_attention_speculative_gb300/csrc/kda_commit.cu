@@ -24,6 +24,10 @@ constexpr int kCommitUnroll = 4;
 
 struct CommitParams {
   const int32_t* acc;
+  const int32_t* idx_state;  // optional pool slots (NULL: slot = n)
+  const int32_t* idx_conv;
+  const int32_t* idx_inter;
+  long long pool_state, pool_conv, pool_inter;
   const float* inter_ssm;
   const unsigned char* snaps;
   float* S;
@@ -44,6 +48,14 @@ __global__ void __launch_bounds__(kCommitThreads) kda_commit_kernel(const Commit
     if (v >= p.total) return;
     const long long n = v / per_seq;
     const long long r = v - n * per_seq;
+    const long long ss = p.idx_state ? __ldg(p.idx_state + n) : n;
+    const long long sc = p.idx_conv ? __ldg(p.idx_conv + n) : n;
+    const long long si = p.idx_inter ? __ldg(p.idx_inter + n) : n;
+    if (ss < 0 || sc < 0 || si < 0) continue;  // padding sequence
+    if (ss >= p.pool_state || sc >= p.pool_conv || si >= p.pool_inter) {
+      if (r == 0 && p.status) atomicOr(p.status, KDA_STATUS_BAD_INDEX);
+      continue;
+    }
     const int a = __ldg(p.acc + n);
     if (a < 1 || a > p.T) {
       if (r == 0 && p.status) atomicOr(p.status, KDA_STATUS_BAD_ACCEPT);
@@ -51,13 +63,13 @@ __global__ void __launch_bounds__(kCommitThreads) kda_commit_kernel(const Commit
     }
     if (r < p.state_vecs) {
       const float4* src = reinterpret_cast<const float4*>(p.inter_ssm) +
-                          ((n * p.T + (a - 1)) * p.state_vecs + r);
-      float4* dst = reinterpret_cast<float4*>(p.S) + (n * p.state_vecs + r);
+                          ((si * p.T + (a - 1)) * p.state_vecs + r);
+      float4* dst = reinterpret_cast<float4*>(p.S) + (ss * p.state_vecs + r);
       __stcs(dst, __ldcs(src));
     } else {
       const long long c = r - p.state_vecs;
-      const uint4* src = reinterpret_cast<const uint4*>(p.snaps) + ((n * p.T + (a - 1)) * p.conv_vecs + c);
-      uint4* dst = reinterpret_cast<uint4*>(p.conv_state) + (n * p.conv_vecs + c);
+      const uint4* src = reinterpret_cast<const uint4*>(p.snaps) + ((si * p.T + (a - 1)) * p.conv_vecs + c);
+      uint4* dst = reinterpret_cast<uint4*>(p.conv_state) + (sc * p.conv_vecs + c);
       __stcs(dst, __ldcs(src));
     }
   }
@@ -69,9 +81,10 @@ bool overlap(uintptr_t a, size_t na, uintptr_t b, size_t nb) {
 
 }  // namespace
 
-extern "C" int kda_commit(const kda_shape* s, const int32_t* accepted, const float* inter_ssm,
-                          const void* conv_snapshots, float* S, void* conv_state, int* status,
-                          kda_stream_t stream) {
+extern "C" int kda_commit_indexed(const kda_shape* s, const kda_state_indices* idx,
+                                  const int32_t* accepted, const float* inter_ssm,
+                                  const void* conv_snapshots, float* S, void* conv_state,
+                                  int* status, kda_stream_t stream) {
   if (!s) return KDA_ERR_NULL;
   if (s->act != KDA_F32 && s->act != KDA_BF16) return KDA_ERR_DTYPE;
   if (s->N < 0 || s->T < 1 || s->T > KDA_MAX_T || s->H < 1 || s->HV < s->H ||
@@ -87,20 +100,38 @@ extern "C" int kda_commit(const kda_shape* s, const int32_t* accepted, const flo
   const size_t ab = s->act == KDA_F32 ? 4 : 2;
   const size_t N = s->N, T = s->T, HV = s->HV, K = s->K, V = s->V;
   const size_t dim = 2 * (size_t)s->H * K + HV * V;
-  const uintptr_t in[3][2] = {{reinterpret_cast<uintptr_t>(accepted), N * 4},
-                              {reinterpret_cast<uintptr_t>(inter_ssm), N * T * HV * K * V * 4},
-                              {reinterpret_cast<uintptr_t>(conv_snapshots), N * T * dim * 3 * ab}};
-  const uintptr_t out[3][2] = {{reinterpret_cast<uintptr_t>(S), N * HV * K * V * 4},
-                               {reinterpret_cast<uintptr_t>(conv_state), N * dim * 3 * ab},
+  size_t ps = N, pc = N, pi = N;
+  const int32_t *is = nullptr, *ic = nullptr, *ii = nullptr;
+  if (idx) {
+    if (idx->cache_indices) { if (idx->state_pool < 1) return KDA_ERR_SHAPE; is = idx->cache_indices; ps = idx->state_pool; }
+    if (idx->conv_state_indices) { if (idx->conv_pool < 1) return KDA_ERR_SHAPE; ic = idx->conv_state_indices; pc = idx->conv_pool; }
+    if (idx->intermediate_state_indices) { if (idx->inter_pool < 1) return KDA_ERR_SHAPE; ii = idx->intermediate_state_indices; pi = idx->inter_pool; }
+    if ((reinterpret_cast<uintptr_t>(is) | reinterpret_cast<uintptr_t>(ic) | reinterpret_cast<uintptr_t>(ii)) & 3u)
+      return KDA_ERR_MISALIGNED;
+  }
+  const uintptr_t in[6][2] = {{reinterpret_cast<uintptr_t>(accepted), N * 4},
+                              {reinterpret_cast<uintptr_t>(inter_ssm), pi * T * HV * K * V * 4},
+                              {reinterpret_cast<uintptr_t>(conv_snapshots), pi * T * dim * 3 * ab},
+                              {reinterpret_cast<uintptr_t>(is), is ? N * 4 : 0},
+                              {reinterpret_cast<uintptr_t>(ic), ic ? N * 4 : 0},
+                              {reinterpret_cast<uintptr_t>(ii), ii ? N * 4 : 0}};
+  const uintptr_t out[3][2] = {{reinterpret_cast<uintptr_t>(S), ps * HV * K * V * 4},
+                               {reinterpret_cast<uintptr_t>(conv_state), pc * dim * 3 * ab},
                                {reinterpret_cast<uintptr_t>(status), status ? 4u : 0u}};
   for (int i = 0; i < 3; ++i) {
-    for (int j = 0; j < 3; ++j)
+    for (int j = 0; j < 6; ++j)
       if (overlap(out[i][0], out[i][1], in[j][0], in[j][1])) return KDA_ERR_ALIAS;
     for (int j = 0; j < 3; ++j)
       if (j != i && overlap(out[i][0], out[i][1], out[j][0], out[j][1])) return KDA_ERR_ALIAS;
   }
   CommitParams p;
   p.acc = accepted;
+  p.idx_state = is;
+  p.idx_conv = ic;
+  p.idx_inter = ii;
+  p.pool_state = (long long)ps;
+  p.pool_conv = (long long)pc;
+  p.pool_inter = (long long)pi;
   p.inter_ssm = inter_ssm;
   p.snaps = static_cast<const unsigned char*>(conv_snapshots);
   p.S = S;
@@ -115,4 +146,11 @@ extern "C" int kda_commit(const kda_shape* s, const int32_t* accepted, const flo
   if (blocks > 0x7fffffffLL) return KDA_ERR_SHAPE;
   kda_commit_kernel<<<(unsigned)blocks, kCommitThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return static_cast<int>(cudaGetLastError());
+}
+
+extern "C" int kda_commit(const kda_shape* s, const int32_t* accepted, const float* inter_ssm,
+                          const void* conv_snapshots, float* S, void* conv_state, int* status,
+                          kda_stream_t stream) {
+  return kda_commit_indexed(s, nullptr, accepted, inter_ssm, conv_snapshots, S, conv_state, status,
+                            stream);
 }

@@ -58,6 +58,12 @@ struct Params {
   int* status;            // device status word
   long long num_items;    // N * HV * nvt
   long long prefetch;     // one-item-per-CTA kernel: L2-prefetch item + prefetch (0: off)
+  // optional state-pool slots per sequence (NULL: slot = n); a negative slot
+  // marks a padding sequence, which is skipped entirely
+  const int* idx_state;   // S0 slot        (pool of pool_state states)
+  const int* idx_conv;    // conv_state slot (pool of pool_conv windows)
+  const int* idx_inter;   // inter_ssm / conv_snapshots slot (pool of pool_inter)
+  int pool_state, pool_conv, pool_inter;
   int N, T, H, HV, V, dim, G, nvt;
   int gate_mode;          // 0 softplus, 1 safe
 };
@@ -66,6 +72,7 @@ constexpr int kConvW = 4;
 constexpr float kL2Eps = 1e-6f;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kStatusTmaTimeout = 1;              // KDA_STATUS_TMA_TIMEOUT
+constexpr int kStatusBadIndex = 4;                // KDA_STATUS_BAD_INDEX
 
 __host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
 __host__ __device__ constexpr size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -94,8 +101,21 @@ __host__ __device__ constexpr size_t ws_smem_bytes(int T, int K, int BV, int ab)
 
 struct Item {
   int n, hv, h, vt;
-  long long unit;  // n * HV + hv
+  long long unit;    // n * HV + hv
+  long long s_unit;  // state-pool slot * HV + hv: the item's S0 tile row / K
+  long long cs_row;  // conv_state-pool slot
+  long long im_row;  // inter_ssm / conv_snapshots-pool slot
+  bool skip;         // padding sequence or out-of-range slot: touch nothing
+  bool bad;          // out-of-range slot (reported in the status word)
 };
+
+__device__ __forceinline__ int resolve_slot(const int* idx, int n, int pool, bool& skip, bool& bad) {
+  if (!idx) return n;
+  const int sl = __ldg(idx + n);
+  if (sl < 0) skip = true;
+  if (sl >= pool) skip = bad = true;
+  return sl;
+}
 
 __device__ __forceinline__ Item decode_item(const Params& p, long long item) {
   Item it;
@@ -104,6 +124,13 @@ __device__ __forceinline__ Item decode_item(const Params& p, long long item) {
   it.n = static_cast<int>(it.unit / p.HV);
   it.hv = static_cast<int>(it.unit - (long long)it.n * p.HV);
   it.h = it.hv / p.G;
+  it.skip = it.bad = false;
+  const int ss = resolve_slot(p.idx_state, it.n, p.pool_state, it.skip, it.bad);
+  const int cs = resolve_slot(p.idx_conv, it.n, p.pool_conv, it.skip, it.bad);
+  const int im = resolve_slot(p.idx_inter, it.n, p.pool_inter, it.skip, it.bad);
+  it.s_unit = (long long)ss * p.HV + it.hv;
+  it.cs_row = cs;
+  it.im_row = im;
   return it;
 }
 
@@ -131,7 +158,7 @@ struct GlobalSrc {
   }
   __device__ __forceinline__ uint4 cs(int kind, int e0, int m) const {
     const Act* b = static_cast<const Act*>(p.conv_state) +
-                   ((size_t)it.n * p.dim + block_channel<K, BV>(p, it, kind) + e0) * (kConvW - 1);
+                   ((size_t)it.cs_row * p.dim + block_channel<K, BV>(p, it, kind) + e0) * (kConvW - 1);
     return ld_rw_16(reinterpret_cast<const char*>(b) + 16 * m);
   }
   __device__ __forceinline__ uint4 w(int kind, int e0, int m) const {
@@ -248,13 +275,13 @@ __device__ __forceinline__ void conv_task(const Src& src, const Params& p, const
       for (int j = 0; j < kConvW - 1; ++j) r[e * (kConvW - 1) + j] = win[j + 1][e];
     if (snap) {
       char* sp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_snapshots) +
-                                         (((size_t)it.n * T + t) * p.dim + c) * (kConvW - 1));
+                                         (((size_t)it.im_row * T + t) * p.dim + c) * (kConvW - 1));
 #pragma unroll
       for (int m = 0; m < 3; ++m) st_16(sp + 16 * m, AT::pack(r + m * VEC));
     }
     if (do_roll) {
       char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
-                                         ((size_t)it.n * p.dim + c) * (kConvW - 1));
+                                         ((size_t)it.cs_row * p.dim + c) * (kConvW - 1));
 #pragma unroll
       for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
     }
@@ -400,7 +427,7 @@ __device__ __forceinline__ void roll_qk(const Src& src, const Params& p, const I
       for (int e = 0; e < VEC; ++e) r[e * (kConvW - 1) + j] = xv[e];
     }
     char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
-                                       ((size_t)it.n * p.dim + c) * (kConvW - 1));
+                                       ((size_t)it.cs_row * p.dim + c) * (kConvW - 1));
 #pragma unroll
     for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
   }
@@ -464,7 +491,7 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
     u.x = __fmul_rn(be, __fsub_rn(v4.x, acc.x)); u.y = __fmul_rn(be, __fsub_rn(v4.y, acc.y));
     u.z = __fmul_rn(be, __fsub_rn(v4.z, acc.z)); u.w = __fmul_rn(be, __fsub_rn(v4.w, acc.w));
     // rank-1 update, partial S^T q, streaming snapshot store
-    float* dst = p.inter_ssm + ((((size_t)it.n * T + t) * p.HV + it.hv) * K + rg * R) * V + colg;
+    float* dst = p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + rg * R) * V + colg;
     float4 oa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < R; i += 4) {
@@ -505,6 +532,7 @@ __device__ __forceinline__ void prefetch_item_l2(const Params& p, const CUtensor
                                                  long long itm, int lane) {
   constexpr int AB = sizeof(Act);
   const Item it = decode_item(p, itm);
+  if (it.skip) return;
   const int T = p.T;
   const int n_pf = 3 * T + 3 + T + 1;
   for (int c = lane; c < n_pf; c += 32) {
@@ -516,7 +544,7 @@ __device__ __forceinline__ void prefetch_item_l2(const Params& p, const CUtensor
     } else if (c < 3 * T + 3) {
       const int kind = c - 3 * T;
       const char* src = static_cast<const char*>(p.conv_state) +
-                        ((size_t)it.n * p.dim + block_channel<K, BV>(p, it, kind)) * 3 * AB;
+                        ((size_t)it.cs_row * p.dim + block_channel<K, BV>(p, it, kind)) * 3 * AB;
       bulk_prefetch_l2(src, (kind == 2 ? BV : K) * 3 * AB);
     } else if (c < 4 * T + 3) {
       const int t = c - 3 * T - 3;
@@ -524,7 +552,7 @@ __device__ __forceinline__ void prefetch_item_l2(const Params& p, const CUtensor
                            ((((size_t)it.n * T + t) * p.HV + it.hv) * K) * AB,
                        K * AB);
     } else {
-      tma_prefetch_2d(tmap, it.vt * BV, static_cast<int>(it.unit * K));
+      tma_prefetch_2d(tmap, it.vt * BV, static_cast<int>(it.s_unit * K));
     }
   }
 }
@@ -556,13 +584,17 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   const long long item = blockIdx.x;
   if (item >= p.num_items) return;
   const Item it = decode_item(p, item);
+  if (it.skip) {  // padding sequence: nothing to read or write
+    if (it.bad && tid == 0 && it.hv == 0 && it.vt == 0) atomicOr(p.status, kStatusBadIndex);
+    return;
+  }
 
   if (tid == 0) {
     mbar_init(mbar, 1);
     fence_mbar_init();
     prefetch_tensormap(&tmap_s0);
     mbar_arrive_expect_tx(mbar, K * BV * sizeof(float));
-    tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.unit * K), mbar,
+    tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.s_unit * K), mbar,
                 l2_policy_evict_first());
   }
   if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items)
@@ -647,7 +679,7 @@ __device__ __forceinline__ void issue_raw(const Params& p, const Item& it, unsig
       const int ch = block_channel<K, BV>(p, it, kind);
       const int nch = kind == 2 ? BV : K;
       if (q < 3) {
-        src = static_cast<const char*>(p.conv_state) + ((size_t)it.n * p.dim + ch) * 3 * AB;
+        src = static_cast<const char*>(p.conv_state) + ((size_t)it.cs_row * p.dim + ch) * 3 * AB;
         dst = raw + L.base_cs() + (size_t)L.blk(kind) * 3 * AB;
         bytes = nch * 3 * AB;
       } else {
@@ -671,6 +703,14 @@ __device__ __forceinline__ void issue_raw(const Params& p, const Item& it, unsig
 
 __host__ __device__ constexpr int ws_min_blocks(int cw) { return cw >= 8 ? 1 : (cw >= 4 ? 3 : 5); }
 
+// First item at or after `item`, stepping by `stride`, that is not a padding
+// sequence (num_items when none is left).  Producer and consumers walk the
+// same sequence of items, so their mbarrier phases stay in step.
+__device__ __forceinline__ long long next_live_item(const Params& p, long long item, long long stride) {
+  while (item < p.num_items && decode_item(p, item).skip) item += stride;
+  return item;
+}
+
 template <typename Act, int K, int CW>
 __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
     kda_ws_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
@@ -689,7 +729,14 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long stride = gridDim.x;
-  if ((long long)blockIdx.x >= p.num_items) return;
+  const long long first = next_live_item(p, blockIdx.x, stride);
+  if (threadIdx.x == 0) {  // report out-of-range slots of this CTA's items
+    for (long long i = blockIdx.x; i < p.num_items; i += stride) {
+      const Item q = decode_item(p, i);
+      if (q.bad && q.hv == 0 && q.vt == 0) atomicOr(p.status, kStatusBadIndex);
+    }
+  }
+  if (first >= p.num_items) return;
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->tile_full, 1);
@@ -707,12 +754,12 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
   if (warp == CW) {
     // ------------------------------ producer ------------------------------
     const uint64_t pol = l2_policy_evict_first();
-    long long item = blockIdx.x;
+    long long item = first;
     Item it = decode_item(p, item);
     if (lane == 0) {
       prefetch_tensormap(&tmap_s0);
       mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
-      tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.unit * K), &bars->tile_full, pol);
+      tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.s_unit * K), &bars->tile_full, pol);
       mbar_arrive_expect_tx(&bars->raw_full, raw_tx_bytes<Act, K, BV>(p));
     }
     __syncwarp();
@@ -740,7 +787,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) roll_qk<Act, K, BV>(src, p, it, lane, 32);
       __syncwarp();  // every lane is done with the raw buffer
-      const long long next = item + stride;
+      const long long next = next_live_item(p, item + stride, stride);
       const bool has_next = next < p.num_items;
       const Item nx = has_next ? decode_item(p, next) : it;
       if (has_next) {
@@ -758,7 +805,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
       if (lane == 0) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
-        tma_load_2d(sbuf, &tmap_s0, nx.vt * BV, static_cast<int>(nx.unit * K), &bars->tile_full, pol);
+        tma_load_2d(sbuf, &tmap_s0, nx.vt * BV, static_cast<int>(nx.s_unit * K), &bars->tile_full, pol);
       }
       tile_phase = j + 1;
       item = next;
@@ -772,8 +819,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
     }
   } else {
     // ------------------------------ consumers -----------------------------
-    long long item = blockIdx.x;
-    for (int j = 0; item < p.num_items; ++j, item += stride) {
+    long long item = first;
+    for (int j = 0; item < p.num_items; ++j, item = next_live_item(p, item + stride, stride)) {
       const int s = j & 1;
       const Item it = decode_item(p, item);
       if (!ws_wait(&bars->tile_full, j & 1, abort_flag)) { ws_fail(p, abort_flag); return; }

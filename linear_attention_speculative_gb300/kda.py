@@ -29,7 +29,8 @@ MAX_T = 16
 
 # The names declared in include/kda_verify.h.
 EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan",
-            "kda_commit", "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan",
+            "kda_conv_verify_indexed", "kda_commit", "kda_commit_indexed",
+            "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan",
             "kda_read_status", "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
@@ -44,6 +45,19 @@ class KdaPlan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bv", ctypes.c_int), ("warps", ctypes.c_int),
                 ("grid", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
                 ("items", ctypes.c_longlong), ("prefetch", ctypes.c_int)]
+
+
+class KdaStateIndices(ctypes.Structure):
+    _fields_ = [("cache_indices", ctypes.c_void_p), ("conv_state_indices", ctypes.c_void_p),
+                ("intermediate_state_indices", ctypes.c_void_p), ("state_pool", ctypes.c_int),
+                ("conv_pool", ctypes.c_int), ("inter_pool", ctypes.c_int)]
+
+
+def state_indices(cache=None, conv=None, inter=None, state_pool=0, conv_pool=0,
+                  inter_pool=0) -> KdaStateIndices:
+    """Pool slots (int32 device tensors [N] or None for the identity)."""
+    ptr = lambda t: None if t is None else t.data_ptr()
+    return KdaStateIndices(ptr(cache), ptr(conv), ptr(inter), state_pool, conv_pool, inter_pool)
 
 
 class KdaError(RuntimeError):
@@ -75,6 +89,12 @@ def _load():
     L.kda_conv_verify_plan.argtypes = args_common + [ctypes.POINTER(KdaPlan), vp]
     L.kda_commit.restype = ctypes.c_int
     L.kda_commit.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp]
+    ip = ctypes.POINTER(KdaStateIndices)
+    L.kda_conv_verify_indexed.restype = ctypes.c_int
+    L.kda_conv_verify_indexed.argtypes = ([sp, ip] + args_common[1:]
+                                          + [ctypes.POINTER(KdaPlan), vp])
+    L.kda_commit_indexed.restype = ctypes.c_int
+    L.kda_commit_indexed.argtypes = [sp, ip, vp, vp, vp, vp, vp, vp, vp]
     L.kda_conv_verify_noalloc.restype = ctypes.c_int
     L.kda_conv_verify_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                           vp, vp, vp, vp]
@@ -198,6 +218,33 @@ def conv_verify_noalloc(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0,
 
 STATUS_TMA_TIMEOUT = 1
 STATUS_BAD_ACCEPT = 2
+STATUS_BAD_INDEX = 4
+
+
+def conv_verify_indexed(shape: KdaShape, idx: KdaStateIndices, mixed_qkv, conv_w, conv_state,
+                        A_log, dt_bias, a, b, S0, gate: str, o, inter_ssm, conv_snapshots,
+                        workspace, stream=None, plan=None) -> None:
+    """The verify over state pools (conv_state, S0, inter_ssm, conv_snapshots
+    are pools addressed through `idx`; see kda_state_indices)."""
+    gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
+    if isinstance(plan, str):
+        plan = parse_plan(plan)
+    rc = lib().kda_conv_verify_indexed(
+        ctypes.byref(shape), ctypes.byref(idx), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_state),
+        _ptr(A_log), _ptr(dt_bias), _ptr(a), _ptr(b), _ptr(S0), gm, _ptr(o), _ptr(inter_ssm),
+        _ptr(conv_snapshots), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(plan) if plan is not None else None, _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_conv_verify_indexed")
+
+
+def commit_indexed(shape: KdaShape, idx: KdaStateIndices, accepted, inter_ssm, conv_snapshots,
+                   S, conv_state, status=None, stream=None) -> None:
+    rc = lib().kda_commit_indexed(ctypes.byref(shape), ctypes.byref(idx), _ptr(accepted),
+                                  _ptr(inter_ssm), _ptr(conv_snapshots), _ptr(S),
+                                  _ptr(conv_state), _ptr(status), _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_commit_indexed")
 
 
 def commit(accepted, inter_ssm, conv_snapshots, S, conv_state, status=None, stream=None,

@@ -221,3 +221,30 @@ def test_commit_rejects_bad_arguments(kda):
     assert _commit(kda, s, cs=0x7f0300000000 + 16) == -5     # two outputs overlap
     assert _commit(kda, kda.make_shape(4, 0, 2, 2, 32, 32)) == -2
     assert _commit(kda, kda.make_shape(0, 3, 2, 2, 32, 32), acc=None, S=None) == 0
+
+
+# ---- state-pool indirection argument checks --------------------------------
+
+def _call_indexed(kda, shape, ptrs, idx, ws_bytes=1 << 20):
+    L = kda.lib()
+    v = lambda n: ctypes.c_void_p(ptrs[n]) if ptrs[n] is not None else None
+    return L.kda_conv_verify_indexed(
+        ctypes.byref(shape), ctypes.byref(idx), v("mixed_qkv"), v("conv_w"), v("conv_state"),
+        v("A_log"), v("dt_bias"), v("a"), v("b"), v("S0"), 0, v("o"), v("inter_ssm"),
+        v("conv_snapshots"), v("workspace"), ws_bytes, None, None)
+
+
+def test_indexed_rejects_bad_pools(kda):
+    s = kda.make_shape(4, 2, 2, 2, 32, 32)
+    ptrs = _fake_args(kda)
+    good_idx = 0x7e0000000000
+    # an index array with an empty pool
+    assert _call_indexed(kda, s, ptrs, kda.KdaStateIndices(good_idx, None, None, 0, 0, 0)) == -2
+    # misaligned index array
+    assert _call_indexed(kda, s, ptrs, kda.KdaStateIndices(good_idx + 2, None, None, 8, 0, 0)) == -4
+    # an index array inside an output buffer
+    inside = ptrs["inter_ssm"] + 64
+    assert _call_indexed(kda, s, ptrs, kda.KdaStateIndices(None, None, inside, 0, 0, 8)) == -5
+    # a pool larger than N makes the state buffers larger: S0 now overlaps the next buffer
+    big = kda.KdaStateIndices(good_idx, None, None, 1 << 20, 0, 0)
+    assert _call_indexed(kda, s, ptrs, big) == -5
