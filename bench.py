@@ -57,8 +57,9 @@ def parse():
                          "its sequences")
     ap.add_argument("--N", type=int, default=0,
                     help="override the number of sequences (small profiling cases)")
-    ap.add_argument("--op", default="verify", choices=["verify", "commit"],
-                    help="commit: time kda_commit (accept a random count per sequence) instead")
+    ap.add_argument("--op", default="verify", choices=["verify", "commit", "decode"],
+                    help="commit: time kda_commit (accept a random count per sequence); "
+                         "decode: time kda_conv_decode (no snapshots, state in place)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every point of the T x N x heads x gate sweep in both variants")
     ap.add_argument("--sweep-out", default="")
@@ -512,6 +513,50 @@ def run_commit(args, wl):
                       "peak_source": src, "timing": "median of per-launch CUDA events, L2 flushed"}))
 
 
+def run_decode(args, wl):
+    """Head-steps/s and HBM bandwidth of the plain decode (state in place)."""
+    import torch
+    from linear_attention_speculative_gb300 import kda
+    from linear_attention_speculative_gb300 import workloads as wk
+    dev = torch.device("cuda", 0)
+    s = wl.shape
+    inp = wk.make_inputs_on_device(wl, dev)
+    shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
+    ws = kda.alloc_workspace(shape, dev)
+    o = torch.empty((s.N, s.T, s.HV, s.V), dtype=s.torch_act, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kda.conv_decode(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
+                        inp["dt_bias"], inp["a"], inp["b"], inp["S0"], wl.gate, o, ws,
+                        stream=stream, shape=shape, plan=args.plan or None)
+    nbytes = (8 * s.N * s.HV * s.K * s.V + s.act_bytes * (
+        s.N * s.T * s.dim + 2 * s.N * s.dim * 3 + s.N * s.T * s.HV * s.K + s.N * s.T * s.HV
+        + s.N * s.T * s.HV * s.V + 4 * s.dim) + 4 * s.HV * (1 + s.K))
+    flush = nbytes < 2 * L2_BYTES
+    fbuf = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    for _ in range(max(3, args.warmup)):
+        step()
+    ev = []
+    for i in range(args.steps):
+        if flush:
+            fbuf.fill_(float(i))
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        ev.append((e0, e1))
+    torch.cuda.synchronize(dev)
+    us = 1e3 * sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
+    peak, src = measured_hbm_peak()
+    gbs = nbytes / (us / 1e6) / 1e9
+    print(json.dumps({"op": "decode", "workload": wl.name, "us": us, "bytes": nbytes,
+                      "head_steps_per_s": s.head_steps / (us / 1e6), "GB/s": gbs,
+                      "frac": gbs / peak, "peak_source": src,
+                      "timing": "median of per-launch CUDA events" + (", L2 flushed" if flush else "")}))
+
+
 def main():
     args = parse()
     if args.sweep:
@@ -519,6 +564,9 @@ def main():
         return
     if args.op == "commit":
         run_commit(args, workload(args.workload))
+        return
+    if args.op == "decode":
+        run_decode(args, workload(args.workload))
         return
     wl = workload(args.workload)
     if args.N:

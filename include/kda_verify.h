@@ -178,6 +178,21 @@ int kda_conv_verify_indexed(const kda_shape* s, const kda_state_indices* idx,
                             float* inter_ssm, void* conv_snapshots, void* workspace,
                             size_t workspace_bytes, const kda_plan* plan, kda_stream_t stream);
 
+/* Plain (non-speculative) decode: the same step without rollback snapshots.
+ * Runs the T tokens of every sequence exactly as kda_conv_verify does, but
+ * writes no inter_ssm and no conv_snapshots: the state after the last token
+ * replaces the persistent state in place (S is read, then overwritten; it
+ * equals the verify's inter_ssm[.., T-1] bit for bit), and conv_state is
+ * rolled.  idx may be NULL (dense) or give cache_indices / conv_state_indices
+ * pools (intermediate_state_indices is ignored); plan may be NULL or a
+ * SMALL_BATCH plan (LARGE_BATCH: KDA_ERR_VARIANT).  Traffic per
+ * sequence and head: the state read and written once.  Same error codes. */
+int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void* mixed_qkv,
+                    const void* conv_w, void* conv_state, const float* A_log,
+                    const float* dt_bias, const void* a, const void* b, float* S,
+                    kda_gate_mode gate_mode, void* o, void* workspace, size_t workspace_bytes,
+                    const kda_plan* plan, kda_stream_t stream);
+
 /* Commit / rollback after a verify: accept the first accepted[n] tokens of
  * every sequence ("[KDA] Fuse causal conv1d into MTP verify decode": the
  * verify writes per-token state and conv-window snapshots for rollback).

@@ -244,7 +244,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
                 const float* A_log, const float* dt_bias, const void* a, const void* b,
                 const float* S0, kda_gate_mode gate_mode, void* o, float* inter_ssm,
                 void* conv_snapshots, void* workspace, const kda_plan& plan, const Pools& pl,
-                kda_stream_t stream) {
+                kda_stream_t stream, float* S_out = nullptr) {
   const size_t N = s->N, H = s->H, HV = s->HV, K = s->K, V = s->V;
   const size_t dim = 2 * H * K + HV * V;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -272,6 +272,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.o = o;
   p.inter_ssm = inter_ssm;
   p.conv_snapshots = conv_snapshots;
+  p.S_out = S_out;
   p.counters = static_cast<int*>(workspace);
   p.status = static_cast<int*>(workspace) + N * H;
   p.num_items = plan.items;
@@ -296,6 +297,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   cfg.K = s->K;
   cfg.warps = plan.warps;
   cfg.ws = plan.variant == KDA_VARIANT_LARGE_BATCH;
+  cfg.decode = S_out != nullptr;
   cfg.grid = plan.grid;
   const int ab = s->act == KDA_F32 ? 4 : 2;
   cfg.smem = cfg.ws ? kda::ws_smem_bytes(s->T, s->K, plan.bv, ab)
@@ -404,6 +406,72 @@ int kda_conv_verify_indexed(const kda_shape* s, const kda_state_indices* idx,
   if (rc) return rc;
   return verify_with(s, pl, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
                      inter_ssm, conv_snapshots, workspace, workspace_bytes, plan, stream);
+}
+
+int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void* mixed_qkv,
+                    const void* conv_w, void* conv_state, const float* A_log,
+                    const float* dt_bias, const void* a, const void* b, float* S,
+                    kda_gate_mode gate_mode, void* o, void* workspace, size_t workspace_bytes,
+                    const kda_plan* plan, kda_stream_t stream) {
+  if (!s) return KDA_ERR_NULL;
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (gate_mode != KDA_GATE_SOFTPLUS && gate_mode != KDA_GATE_SAFE) return KDA_ERR_GATE;
+  Pools pl;
+  kda_state_indices no_inter;
+  if (idx) {  // decode writes no snapshots: the intermediate slots do not apply
+    no_inter = *idx;
+    no_inter.intermediate_state_indices = nullptr;
+  }
+  rc = pools_from(s, idx ? &no_inter : nullptr, &pl);
+  if (rc) return rc;
+  if (s->N == 0) return KDA_OK;
+  if (!mixed_qkv || !conv_w || !conv_state || !a || !b || !S || !o) return KDA_ERR_NULL;
+  if (gate_mode == KDA_GATE_SOFTPLUS && (!A_log || !dt_bias)) return KDA_ERR_GATE;
+  if (!workspace || workspace_bytes < kda_workspace_bytes(s)) return KDA_ERR_WORKSPACE;
+  const size_t ab = act_bytes(s);
+  const size_t N = s->N, T = s->T, H = s->H, HV = s->HV, K = s->K, V = s->V;
+  const size_t dim = 2 * H * K + HV * V;
+  auto al16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (!al16(mixed_qkv) || !al16(conv_w) || !al16(conv_state) || !al16(a) || !al16(S) ||
+      !al16(o) || !al16(workspace) || (reinterpret_cast<uintptr_t>(b) % ab) != 0)
+    return KDA_ERR_MISALIGNED;
+  if (gate_mode == KDA_GATE_SOFTPLUS && (!al16(A_log) || !al16(dt_bias))) return KDA_ERR_MISALIGNED;
+  auto span = [](const void* p, size_t bytes) {
+    Span sp;
+    sp.lo = reinterpret_cast<uintptr_t>(p);
+    sp.hi = sp.lo + (p ? bytes : 0);
+    return sp;
+  };
+  const Span in[] = {span(mixed_qkv, N * T * dim * ab), span(conv_w, dim * 4 * ab),
+                     span(gate_mode == KDA_GATE_SOFTPLUS ? A_log : nullptr, HV * 4),
+                     span(gate_mode == KDA_GATE_SOFTPLUS ? dt_bias : nullptr, HV * K * 4),
+                     span(a, N * T * HV * K * ab), span(b, N * T * HV * ab),
+                     span(pl.idx_state, N * 4), span(pl.idx_conv, N * 4)};
+  const Span wr[] = {span(conv_state, pl.n_conv * dim * 3 * ab), span(S, pl.n_state * HV * K * V * 4),
+                     span(o, N * T * HV * V * ab), span(workspace, kda_workspace_bytes(s))};
+  for (size_t i = 0; i < sizeof(wr) / sizeof(wr[0]); ++i) {
+    for (const Span& x : in)
+      if (overlap(wr[i], x)) return KDA_ERR_ALIAS;
+    for (size_t j = 0; j < sizeof(wr) / sizeof(wr[0]); ++j)
+      if (j != i && overlap(wr[i], wr[j])) return KDA_ERR_ALIAS;
+  }
+  // decode runs the one-item-per-CTA kernel only
+  if (plan && !(plan->variant == KDA_VARIANT_SMALL_BATCH && valid_tile_bv(plan->bv, s->V)))
+    return KDA_ERR_VARIANT;
+  int num_sms = 0;
+  rc = num_sms_of_current_device(&num_sms);
+  if (rc) return rc;
+  kda_plan p;
+  if (plan) {
+    p = *plan;
+    finish_plan(s, num_sms, &p, plan->grid, plan->prefetch);
+  } else {
+    rc = kda_make_plan(s, num_sms, KDA_VARIANT_AUTO, &p);
+    if (rc) return rc;
+  }
+  return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S, gate_mode, o,
+                     nullptr, nullptr, workspace, p, pl, stream, S);
 }
 
 int kda_conv_verify(const kda_shape* s, const void* mixed_qkv, const void* conv_w,

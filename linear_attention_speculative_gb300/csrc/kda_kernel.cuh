@@ -52,8 +52,9 @@ struct Params {
   const void* a;          // act [N, T, HV, K]
   const void* b;          // act [N, T, HV]
   void* o;                // act [N, T, HV, V]
-  float* inter_ssm;       // f32 [N, T, HV, K, V]
-  void* conv_snapshots;   // act [N, T, dim, 3]
+  float* inter_ssm;       // f32 [N, T, HV, K, V] (unused by the decode kernels)
+  void* conv_snapshots;   // act [N, T, dim, 3]   (unused by the decode kernels)
+  float* S_out;           // decode kernels: the final state, written in place over S0
   int* counters;          // [N * H]
   int* status;            // device status word
   long long num_items;    // N * HV * nvt
@@ -329,7 +330,7 @@ __device__ __forceinline__ float load_b(const Params& p, const Item& it, int t) 
 }
 
 // All conv / gate / beta tasks of one item, spread over `nthr` threads.
-template <typename Act, int K, int BV, typename Src>
+template <typename Act, int K, int BV, bool DEC = false, typename Src>
 __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, const Item& it,
                                               float* sQ, float* sK, float* sA, float* sV,
                                               float* sB, int tid, int nthr) {
@@ -340,7 +341,8 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
   const int n_conv = NCV * T;
   const int n_gate = NQ * T;
   // q/k snapshots are written once per group: by its first v-head, first tile
-  const bool qk_snap_owner = (it.hv % p.G == 0) && (it.vt == 0);
+  const bool qk_snap_owner = !DEC && (it.hv % p.G == 0) && (it.vt == 0);
+  constexpr bool v_snap = !DEC;  // decode writes no conv-window snapshots
   const float negA = p.gate_mode == 0 ? -expf(__ldg(p.A_log + it.hv)) : 0.0f;
   for (int task = tid; task < n_conv + n_gate + T; task += nthr) {
     if (task < n_conv) {
@@ -350,7 +352,7 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
       const int e0 = (cv - kind * NQ) * VEC;
       float* dst = kind == 0 ? sQ + t * K + e0 : (kind == 1 ? sK + t * K + e0 : sV + t * BV + e0);
       const int c = block_channel<K, BV>(p, it, kind) + e0;
-      conv_task<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 || qk_snap_owner, kind == 2);
+      conv_task<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
     } else if (task < n_conv + n_gate) {
       const int g = task - n_conv;
       const int t = g / NQ;
@@ -445,7 +447,7 @@ __device__ __forceinline__ void load_tile(const float* sbuf, float4 (&s)[K / 8],
   for (int i = 0; i < R; ++i) s[i] = *reinterpret_cast<const float4*>(src + i * BV);
 }
 
-template <typename Act, int K, int BV>
+template <typename Act, int K, int BV, bool DEC = false>
 __device__ __forceinline__ void consume(const Params& p, const Item& it, const float* sQ,
                                        const float* sK, const float* sA, const float* sV,
                                        const float* sB, float4 (&s)[K / 8], int warp, int lane) {
@@ -491,7 +493,8 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
     u.x = __fmul_rn(be, __fsub_rn(v4.x, acc.x)); u.y = __fmul_rn(be, __fsub_rn(v4.y, acc.y));
     u.z = __fmul_rn(be, __fsub_rn(v4.z, acc.z)); u.w = __fmul_rn(be, __fsub_rn(v4.w, acc.w));
     // rank-1 update, partial S^T q, streaming snapshot store
-    float* dst = p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + rg * R) * V + colg;
+    float* dst = DEC ? nullptr
+                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + rg * R) * V + colg;
     float4 oa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < R; i += 4) {
@@ -506,7 +509,7 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
         x.z = __fmaf_rn(kv[j], u.z, x.z); x.w = __fmaf_rn(kv[j], u.w, x.w);
         oa.x = __fmaf_rn(x.x, qv[j], oa.x); oa.y = __fmaf_rn(x.y, qv[j], oa.y);
         oa.z = __fmaf_rn(x.z, qv[j], oa.z); oa.w = __fmaf_rn(x.w, qv[j], oa.w);
-        st_stream_f4(dst + (size_t)(i + j) * V, x);
+        if constexpr (!DEC) st_stream_f4(dst + (size_t)(i + j) * V, x);
       }
     }
 #pragma unroll
@@ -520,6 +523,12 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
       Act* op = static_cast<Act*>(p.o) + (((size_t)it.n * T + t) * p.HV + it.hv) * V + colg;
       ActT<Act>::store4(op, oa);
     }
+  }
+  if constexpr (DEC) {
+    // decode: the state after the last token replaces the persistent state
+    float* dst = p.S_out + ((size_t)it.s_unit * K + rg * R) * V + colg;
+#pragma unroll
+    for (int i = 0; i < R; ++i) st_stream_f4(dst + (size_t)i * V, s[i]);
   }
 }
 
@@ -560,7 +569,7 @@ __device__ __forceinline__ void prefetch_item_l2(const Params& p, const CUtensor
 // ---------------------------------------------------------------------------
 // one item per CTA: every warp produces, then consumes
 // ---------------------------------------------------------------------------
-template <typename Act, int K, int WARPS>
+template <typename Act, int K, int WARPS, bool DEC = false>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     kda_tile_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
   constexpr int BV = WARPS * 16;
@@ -600,7 +609,7 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items)
     prefetch_item_l2<Act, K, BV>(p, &tmap_s0, item + p.prefetch, lane);
   const GlobalSrc<Act, K, BV> src{p, it};
-  produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, tid, NT);
+  produce_tasks<Act, K, BV, DEC>(src, p, it, sQ, sK, sA, sV, sB, tid, NT);
   __syncthreads();  // every conv_state read of this CTA is done, stage written
   if (tid == 0) sflag[0] = arrive_qk_group(p, it) ? 1 : 0;
   for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * K : sK + (r - T) * K, r < T, lane);
@@ -613,7 +622,7 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   }
   float4 s[R];
   load_tile<K, BV>(sbuf, s, warp, lane);
-  consume<Act, K, BV>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
+  consume<Act, K, BV, DEC>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
   if (sflag[0]) roll_qk<Act, K, BV>(src, p, it, tid, NT);
 }
 

@@ -29,7 +29,7 @@ MAX_T = 16
 
 # The names declared in include/kda_verify.h.
 EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan",
-            "kda_conv_verify_indexed", "kda_commit", "kda_commit_indexed",
+            "kda_conv_verify_indexed", "kda_conv_decode", "kda_commit", "kda_commit_indexed",
             "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan",
             "kda_read_status", "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
@@ -93,6 +93,9 @@ def _load():
     L.kda_conv_verify_indexed.restype = ctypes.c_int
     L.kda_conv_verify_indexed.argtypes = ([sp, ip] + args_common[1:]
                                           + [ctypes.POINTER(KdaPlan), vp])
+    L.kda_conv_decode.restype = ctypes.c_int
+    L.kda_conv_decode.argtypes = [sp, ip, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, vp, vp, sz,
+                                  ctypes.POINTER(KdaPlan), vp]
     L.kda_commit_indexed.restype = ctypes.c_int
     L.kda_commit_indexed.argtypes = [sp, ip, vp, vp, vp, vp, vp, vp, vp]
     L.kda_conv_verify_noalloc.restype = ctypes.c_int
@@ -236,6 +239,25 @@ def conv_verify_indexed(shape: KdaShape, idx: KdaStateIndices, mixed_qkv, conv_w
         ctypes.byref(plan) if plan is not None else None, _stream_handle(stream))
     if rc != 0:
         raise KdaError(rc, "kda_conv_verify_indexed")
+
+
+def conv_decode(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S, gate: str, o, workspace,
+                stream=None, plan=None, idx: Optional[KdaStateIndices] = None,
+                shape: Optional[KdaShape] = None) -> None:
+    """Plain decode: S (f32, the state pool or [N,HV,K,V]) is updated in place,
+    conv_state rolled, o written; no snapshots."""
+    if shape is None:
+        shape = shape_of(mixed_qkv, a, S if idx is None else S[: mixed_qkv.shape[0]])
+    gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
+    if isinstance(plan, str):
+        plan = parse_plan(plan)
+    rc = lib().kda_conv_decode(
+        ctypes.byref(shape), ctypes.byref(idx) if idx is not None else None, _ptr(mixed_qkv),
+        _ptr(conv_w), _ptr(conv_state), _ptr(A_log), _ptr(dt_bias), _ptr(a), _ptr(b), _ptr(S), gm,
+        _ptr(o), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        ctypes.byref(plan) if plan is not None else None, _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_conv_decode")
 
 
 def commit_indexed(shape: KdaShape, idx: KdaStateIndices, accepted, inter_ssm, conv_snapshots,

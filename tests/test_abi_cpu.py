@@ -248,3 +248,20 @@ def test_indexed_rejects_bad_pools(kda):
     # a pool larger than N makes the state buffers larger: S0 now overlaps the next buffer
     big = kda.KdaStateIndices(good_idx, None, None, 1 << 20, 0, 0)
     assert _call_indexed(kda, s, ptrs, big) == -5
+
+
+def test_decode_rejects_bad_arguments(kda):
+    L = kda.lib()
+    s = kda.make_shape(4, 2, 2, 2, 32, 32)
+    p = _fake_args(kda)
+    v = lambda x: ctypes.c_void_p(x) if x is not None else None
+
+    def call(S=p["S0"], o=p["o"], plan=None):
+        return L.kda_conv_decode(ctypes.byref(s), None, v(p["mixed_qkv"]), v(p["conv_w"]),
+                                 v(p["conv_state"]), v(p["A_log"]), v(p["dt_bias"]), v(p["a"]),
+                                 v(p["b"]), v(S), 0, v(o), v(p["workspace"]), 1 << 20,
+                                 ctypes.byref(plan) if plan is not None else None, None)
+    assert call(S=None) == -1
+    assert call(o=p["S0"] + 64) == -5                 # output inside the in/out state
+    assert call(plan=kda.parse_plan("large:32")) == -8
+    assert call(plan=kda.parse_plan("small:64")) == -8  # wider than V = 32
