@@ -376,7 +376,7 @@ def run_ours(args, wl):
         "scaling": args.scaling, "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "K": s.K,
                    "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
-                   "variant": {1: "small_batch", 2: "large_batch"}[plan.variant],
+                   "variant": {1: "small_batch", 2: "large_batch", 3: "smem_state"}[plan.variant],
                    "v_tile": plan.bv, "plan": args.plan or "auto",
                    "l2": ("L2 flushed between steps (256 MB write)" if flush_l2 else
                           f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB moved per step"),
@@ -400,7 +400,7 @@ def run_ours(args, wl):
 
 
 def plan_label(plan) -> str:
-    return f"{'large' if plan.variant == 2 else 'small'}:{plan.bv}"
+    return f"{ {1: 'small', 2: 'large', 3: 'smem'}[plan.variant] }:{plan.bv}"
 
 
 def run_sweep(args):

@@ -55,8 +55,10 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 typedef enum {
   KDA_VARIANT_AUTO = 0,
   KDA_VARIANT_SMALL_BATCH = 1, /* one CTA per (sequence, v-head, v-tile) */
-  KDA_VARIANT_LARGE_BATCH = 2  /* persistent CTAs over whole (sequence, v-head) units,
-                                  next state tile prefetched by TMA */
+  KDA_VARIANT_LARGE_BATCH = 2, /* persistent, warp-specialised CTAs; the next item's inputs
+                                  and state tile staged by TMA while the current one runs */
+  KDA_VARIANT_SMEM_STATE = 3   /* one item per CTA, the state kept in shared memory instead
+                                  of registers (more CTAs per SM; v-tile 64 or 128) */
 } kda_variant;
 
 /* Problem shape.  Supported: T in [1, KDA_MAX_T] (N == 0 is a no-op),

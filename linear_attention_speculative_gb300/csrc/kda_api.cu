@@ -44,6 +44,17 @@ int ctas_per_sm_for(int regs_limit, size_t smem) {
 
 bool valid_tile_bv(int bv, int V) { return (bv == 16 || bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
 bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
+bool valid_sms_bv(int bv, int V) { return (bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
+
+// A plan's tile width against its variant (decode: no persistent variant).
+bool valid_plan(const kda_plan* plan, int V, bool decode) {
+  switch (plan->variant) {
+    case KDA_VARIANT_SMALL_BATCH: return valid_tile_bv(plan->bv, V);
+    case KDA_VARIANT_LARGE_BATCH: return !decode && valid_ws_bv(plan->bv, V);
+    case KDA_VARIANT_SMEM_STATE: return valid_sms_bv(plan->bv, V);
+    default: return false;
+  }
+}
 
 // Fill the derived fields of a plan whose variant and bv are set.
 void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_grid,
@@ -61,7 +72,8 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
   } else {
     out->warps = out->bv / 16;
     const size_t smem = kda::tile_smem_bytes(s->T, s->K, out->bv);
-    out->ctas_per_sm = ctas_per_sm_for(16 / out->warps, smem);
+    const bool sms = out->variant == KDA_VARIANT_SMEM_STATE;
+    out->ctas_per_sm = ctas_per_sm_for(kda::tile_min_blocks(out->warps, sms), smem);
     out->grid = (int)std::max(1LL, out->items);
     // 3/8 of a wave of resident CTAs ahead: measured on GB300, any distance
     // between ~1/4 and ~5/8 of a wave is within 2 %; a full wave or more lets
@@ -130,21 +142,26 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
   if (!out) return KDA_ERR_NULL;
   if (num_sms < 1) return KDA_ERR_DEVICE;
   if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
-      variant != KDA_VARIANT_LARGE_BATCH)
+      variant != KDA_VARIANT_LARGE_BATCH && variant != KDA_VARIANT_SMEM_STATE)
     return KDA_ERR_VARIANT;
   const long long units = (long long)s->N * s->HV;
   std::memset(out, 0, sizeof(*out));
   if (variant == KDA_VARIANT_LARGE_BATCH) {
     out->variant = KDA_VARIANT_LARGE_BATCH;
     out->bv = s->V >= 64 ? 64 : s->V;
+  } else if (variant == KDA_VARIANT_SMEM_STATE) {
+    if (s->V < 64) return KDA_ERR_VARIANT;
+    out->variant = KDA_VARIANT_SMEM_STATE;
+    out->bv = std::min(s->V, 128);
   } else {
     // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
     // many threads for its producer tasks and the q/k conv is not repeated per
-    // v-tile.  Measured on GB300 (with the L2 prefetch), half states (BV = 64)
-    // win only single-token verifies of grouped heads, by a few per cent.
+    // v-tile.  Single-token calls over many units keep the state in shared
+    // memory instead (3 CTAs/SM instead of 2): measured on GB300 +4..10 % at
+    // T = 1, but slower from T = 2 on (two shared-memory passes per token).
     out->variant = KDA_VARIANT_SMALL_BATCH;
     out->bv = std::min(s->V, 128);
-    if (s->T == 1 && s->HV > s->H && units >= 4LL * num_sms && s->V >= 64) out->bv = 64;
+    if (s->T == 1 && s->V >= 128 && units >= 4LL * num_sms) out->variant = KDA_VARIANT_SMEM_STATE;
   }
   finish_plan(s, num_sms, out, 0, 0);
   return KDA_OK;
@@ -276,7 +293,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.counters = static_cast<int*>(workspace);
   p.status = static_cast<int*>(workspace) + N * H;
   p.num_items = plan.items;
-  p.prefetch = plan.variant == KDA_VARIANT_SMALL_BATCH ? plan.prefetch : 0;
+  p.prefetch = plan.variant == KDA_VARIANT_LARGE_BATCH ? 0 : plan.prefetch;
   p.idx_state = pl.idx_state;
   p.idx_conv = pl.idx_conv;
   p.idx_inter = pl.idx_inter;
@@ -298,6 +315,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   cfg.warps = plan.warps;
   cfg.ws = plan.variant == KDA_VARIANT_LARGE_BATCH;
   cfg.decode = S_out != nullptr;
+  cfg.sms = plan.variant == KDA_VARIANT_SMEM_STATE;
   cfg.grid = plan.grid;
   const int ab = s->act == KDA_F32 ? 4 : 2;
   cfg.smem = cfg.ws ? kda::ws_smem_bytes(s->T, s->K, plan.bv, ab)
@@ -323,7 +341,7 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
                             void* conv_snapshots, void* workspace, size_t workspace_bytes,
                             kda_variant variant, kda_stream_t stream) {
   if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
-      variant != KDA_VARIANT_LARGE_BATCH)
+      variant != KDA_VARIANT_LARGE_BATCH && variant != KDA_VARIANT_SMEM_STATE)
     return KDA_ERR_VARIANT;
   if (!s) return KDA_ERR_NULL;
   const Pools pl = dense_pools(s);
@@ -353,15 +371,7 @@ int verify_with(const kda_shape* s, const Pools& pl, const void* mixed_qkv, cons
   int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
                          o, inter_ssm, conv_snapshots, workspace, workspace_bytes, pl);
   if (rc || s->N == 0) return rc;
-  if (plan) {
-    if (plan->variant == KDA_VARIANT_SMALL_BATCH) {
-      if (!valid_tile_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
-    } else if (plan->variant == KDA_VARIANT_LARGE_BATCH) {
-      if (!valid_ws_bv(plan->bv, s->V)) return KDA_ERR_VARIANT;
-    } else {
-      return KDA_ERR_VARIANT;
-    }
-  }
+  if (plan && !valid_plan(plan, s->V, false)) return KDA_ERR_VARIANT;
   int num_sms = 0;
   rc = num_sms_of_current_device(&num_sms);
   if (rc) return rc;
@@ -456,9 +466,8 @@ int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void
     for (size_t j = 0; j < sizeof(wr) / sizeof(wr[0]); ++j)
       if (j != i && overlap(wr[i], wr[j])) return KDA_ERR_ALIAS;
   }
-  // decode runs the one-item-per-CTA kernel only
-  if (plan && !(plan->variant == KDA_VARIANT_SMALL_BATCH && valid_tile_bv(plan->bv, s->V)))
-    return KDA_ERR_VARIANT;
+  // decode runs the one-item-per-CTA kernels only
+  if (plan && !valid_plan(plan, s->V, true)) return KDA_ERR_VARIANT;
   int num_sms = 0;
   rc = num_sms_of_current_device(&num_sms);
   if (rc) return rc;

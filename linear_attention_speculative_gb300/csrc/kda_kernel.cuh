@@ -227,9 +227,11 @@ __device__ __forceinline__ void select_state(const Raw (&cs)[3 * VEC], int idx, 
 
 // One conv task: VEC channels of block `kind` at token t.  Writes SiLU(conv)
 // to dst[e], the snapshot of token t when `snap`, and at t = T-1 the rolled
-// state of these channels when `roll`.
+// state of these channels when `roll`.  This form unpacks every input value
+// into its own register (fewest instructions); conv_task_packed below does the
+// same arithmetic from packed words, for kernels with a tight register cap.
 template <typename Act, typename Src>
-__device__ __forceinline__ void conv_task(const Src& src, const Params& p, const Item& it,
+__device__ __forceinline__ void conv_task_unpacked(const Src& src, const Params& p, const Item& it,
                                           int kind, int e0, int c, int t, float* dst, bool snap,
                                           bool roll) {
   using AT = ActT<Act>;
@@ -289,6 +291,89 @@ __device__ __forceinline__ void conv_task(const Src& src, const Params& p, const
   }
 }
 
+// Raw value i (compile-time after unrolling) of a 16-byte word of
+// activations: 8 bf16 halves or 4 fp32 words.
+template <typename Act>
+__device__ __forceinline__ uint32_t raw_at(const uint4& w, int i) {
+  if constexpr (sizeof(Act) == 4) {
+    return i == 0 ? w.x : (i == 1 ? w.y : (i == 2 ? w.z : w.w));
+  } else {
+    const int q = i >> 1;
+    const uint32_t word = q == 0 ? w.x : (q == 1 ? w.y : (q == 2 ? w.z : w.w));
+    return (i & 1) ? (word >> 16) : (word & 0xffffu);
+  }
+}
+
+// The conv task of conv_task_unpacked with its inputs kept packed in 16-byte
+// words
+// (window positions, the old state [e][j], the taps [e][j]) and single values
+// are extracted where they are used.
+template <typename Act, typename Src>
+__device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p, const Item& it,
+                                          int kind, int e0, int c, int t, float* dst, bool snap,
+                                          bool roll) {
+  using AT = ActT<Act>;
+  using Raw = typename AT::Raw;
+  constexpr int VEC = AT::VEC;
+  const int T = p.T;
+  uint4 csw[3] = {};
+  if (t < kConvW - 1) {
+#pragma unroll
+    for (int m = 0; m < 3; ++m) csw[m] = src.cs(kind, e0, m);
+  }
+  // window x_ext[t .. t+3]: x_ext[i] = state[i] for i < 3, else token i-3
+  uint4 xw[kConvW] = {};
+#pragma unroll
+  for (int j = 0; j < kConvW; ++j)
+    if (t + j >= kConvW - 1) xw[j] = src.x(kind, t + j - (kConvW - 1), e0);
+  // raw value of channel e at window position j
+  auto xraw = [&](int j, int e) -> Raw {
+    const int idx = t + j;
+    if (idx >= kConvW - 1) return raw_at<Act>(xw[j], e);
+    const Raw s0 = raw_at<Act>(csw[(e * 3 + 0) / VEC], (e * 3 + 0) % VEC);
+    const Raw s1 = raw_at<Act>(csw[(e * 3 + 1) / VEC], (e * 3 + 1) % VEC);
+    const Raw s2 = raw_at<Act>(csw[(e * 3 + 2) / VEC], (e * 3 + 2) % VEC);
+    return idx == 0 ? s0 : (idx == 1 ? s1 : s2);
+  };
+  uint4 ww[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) ww[m] = src.w(kind, e0, m);
+  float y[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) {
+    float acc = __fmul_rn(AT::to_f(raw_at<Act>(ww[(e * 4) / VEC], (e * 4) % VEC)), AT::to_f(xraw(0, e)));
+#pragma unroll
+    for (int j = 1; j < kConvW; ++j)
+      acc = __fmaf_rn(AT::to_f(raw_at<Act>(ww[(e * 4 + j) / VEC], (e * 4 + j) % VEC)),
+                      AT::to_f(xraw(j, e)), acc);
+    y[e] = silu_f(acc);
+  }
+#pragma unroll
+  for (int e = 0; e < VEC; e += 4)
+    *reinterpret_cast<float4*>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+  const bool do_roll = roll && t == T - 1;
+  if (snap || do_roll) {
+    // the raw window after token t: x_ext[t+1 .. t+3], channel-major [e][j]
+    Raw r[3 * VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e)
+#pragma unroll
+      for (int j = 0; j < kConvW - 1; ++j) r[e * (kConvW - 1) + j] = xraw(j + 1, e);
+    if (snap) {
+      char* sp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_snapshots) +
+                                         (((size_t)it.im_row * T + t) * p.dim + c) * (kConvW - 1));
+#pragma unroll
+      for (int m = 0; m < 3; ++m) st_16(sp + 16 * m, AT::pack(r + m * VEC));
+    }
+    if (do_roll) {
+      char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
+                                         ((size_t)it.cs_row * p.dim + c) * (kConvW - 1));
+#pragma unroll
+      for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
+    }
+  }
+}
+
 // One gate task: alpha = exp(g) of VEC channels at token t.
 template <typename Act, typename Src>
 __device__ __forceinline__ void gate_task(const Src& src, int gate_mode, float negA, int t,
@@ -330,7 +415,7 @@ __device__ __forceinline__ float load_b(const Params& p, const Item& it, int t) 
 }
 
 // All conv / gate / beta tasks of one item, spread over `nthr` threads.
-template <typename Act, int K, int BV, bool DEC = false, typename Src>
+template <typename Act, int K, int BV, bool DEC = false, bool PACKED = false, typename Src>
 __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, const Item& it,
                                               float* sQ, float* sK, float* sA, float* sV,
                                               float* sB, int tid, int nthr) {
@@ -352,7 +437,10 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
       const int e0 = (cv - kind * NQ) * VEC;
       float* dst = kind == 0 ? sQ + t * K + e0 : (kind == 1 ? sK + t * K + e0 : sV + t * BV + e0);
       const int c = block_channel<K, BV>(p, it, kind) + e0;
-      conv_task<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
+      if constexpr (PACKED)
+        conv_task_packed<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
+      else
+        conv_task_unpacked<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
     } else if (task < n_conv + n_gate) {
       const int g = task - n_conv;
       const int t = g / NQ;
@@ -566,11 +654,109 @@ __device__ __forceinline__ void prefetch_item_l2(const Params& p, const CUtensor
   }
 }
 
+// The same recurrence with S kept in the shared-memory tile instead of
+// registers (about half the registers, so more CTAs per SM).  Each thread
+// owns exactly the elements the register consumer holds; per token, pass 1
+// decays them and forms the partial S^T k, pass 2 recomputes the decayed
+// value (the same fmul, hence the same bits), applies the rank-1 update, forms
+// the partial S^T q, stores the snapshot and writes the element back.  The
+// floating-point operations and their order are those of `consume`, so the
+// results are bit-identical.
+template <typename Act, int K, int BV, bool DEC = false>
+__device__ __forceinline__ void consume_smem(const Params& p, const Item& it, const float* sQ,
+                                            const float* sK, const float* sA, const float* sV,
+                                            const float* sB, float* sS, int warp, int lane) {
+  constexpr int R = K / 8;
+  const int rg = lane >> 2;
+  const int cg = lane & 3;
+  const int col = warp * 16 + cg * 4;
+  const int T = p.T;
+  const int V = p.V;
+  const size_t colg = (size_t)it.vt * BV + col;
+  float* own = sS + (rg * R) * BV + col;
+  for (int t = 0; t < T; ++t) {
+    const float* al = sA + t * K + rg * R;
+    const float* kk = sK + t * K + rg * R;
+    const float* qq = sQ + t * K + rg * R;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < R; i += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(al + i);
+      const float4 k4 = *reinterpret_cast<const float4*>(kk + i);
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float4 x = *reinterpret_cast<const float4*>(own + (i + j) * BV);
+        x.x = __fmul_rn(x.x, av[j]); x.y = __fmul_rn(x.y, av[j]);
+        x.z = __fmul_rn(x.z, av[j]); x.w = __fmul_rn(x.w, av[j]);
+        acc.x = __fmaf_rn(x.x, kv[j], acc.x); acc.y = __fmaf_rn(x.y, kv[j], acc.y);
+        acc.z = __fmaf_rn(x.z, kv[j], acc.z); acc.w = __fmaf_rn(x.w, kv[j], acc.w);
+      }
+    }
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+      acc.x = __fadd_rn(acc.x, __shfl_xor_sync(0xffffffffu, acc.x, off));
+      acc.y = __fadd_rn(acc.y, __shfl_xor_sync(0xffffffffu, acc.y, off));
+      acc.z = __fadd_rn(acc.z, __shfl_xor_sync(0xffffffffu, acc.z, off));
+      acc.w = __fadd_rn(acc.w, __shfl_xor_sync(0xffffffffu, acc.w, off));
+    }
+    const float4 v4 = *reinterpret_cast<const float4*>(sV + t * BV + col);
+    const float be = sB[t];
+    float4 u;
+    u.x = __fmul_rn(be, __fsub_rn(v4.x, acc.x)); u.y = __fmul_rn(be, __fsub_rn(v4.y, acc.y));
+    u.z = __fmul_rn(be, __fsub_rn(v4.z, acc.z)); u.w = __fmul_rn(be, __fsub_rn(v4.w, acc.w));
+    const bool last = t == T - 1;
+    float* dst = DEC ? (last ? p.S_out + ((size_t)it.s_unit * K + rg * R) * V + colg : nullptr)
+                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + rg * R) * V + colg;
+    float4 oa = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < R; i += 4) {
+      const float4 a4 = *reinterpret_cast<const float4*>(al + i);
+      const float4 k4 = *reinterpret_cast<const float4*>(kk + i);
+      const float4 q4 = *reinterpret_cast<const float4*>(qq + i);
+      const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+      const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
+      const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float4* ep = reinterpret_cast<float4*>(own + (i + j) * BV);
+        float4 x = *ep;
+        x.x = __fmul_rn(x.x, av[j]); x.y = __fmul_rn(x.y, av[j]);
+        x.z = __fmul_rn(x.z, av[j]); x.w = __fmul_rn(x.w, av[j]);
+        x.x = __fmaf_rn(kv[j], u.x, x.x); x.y = __fmaf_rn(kv[j], u.y, x.y);
+        x.z = __fmaf_rn(kv[j], u.z, x.z); x.w = __fmaf_rn(kv[j], u.w, x.w);
+        oa.x = __fmaf_rn(x.x, qv[j], oa.x); oa.y = __fmaf_rn(x.y, qv[j], oa.y);
+        oa.z = __fmaf_rn(x.z, qv[j], oa.z); oa.w = __fmaf_rn(x.w, qv[j], oa.w);
+        if (DEC ? last : true) st_stream_f4(dst + (size_t)(i + j) * V, x);
+        if (!last) *ep = x;
+      }
+    }
+#pragma unroll
+    for (int off = 4; off <= 16; off <<= 1) {
+      oa.x = __fadd_rn(oa.x, __shfl_xor_sync(0xffffffffu, oa.x, off));
+      oa.y = __fadd_rn(oa.y, __shfl_xor_sync(0xffffffffu, oa.y, off));
+      oa.z = __fadd_rn(oa.z, __shfl_xor_sync(0xffffffffu, oa.z, off));
+      oa.w = __fadd_rn(oa.w, __shfl_xor_sync(0xffffffffu, oa.w, off));
+    }
+    if (rg == 0) {
+      Act* op = static_cast<Act*>(p.o) + (((size_t)it.n * T + t) * p.HV + it.hv) * V + colg;
+      ActT<Act>::store4(op, oa);
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // one item per CTA: every warp produces, then consumes
 // ---------------------------------------------------------------------------
-template <typename Act, int K, int WARPS, bool DEC = false>
-__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
+// SMS: keep S in the shared-memory tile (consume_smem) instead of registers;
+// the register cap then allows 3 CTAs of 8 warps per SM.
+__host__ __device__ constexpr int tile_min_blocks(int warps, bool sms) {
+  return sms ? 24 / warps : 16 / warps;
+}
+
+template <typename Act, int K, int WARPS, bool DEC = false, bool SMS = false>
+__global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     kda_tile_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
   constexpr int BV = WARPS * 16;
   constexpr int NT = WARPS * 32;
@@ -609,7 +795,7 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
   if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items)
     prefetch_item_l2<Act, K, BV>(p, &tmap_s0, item + p.prefetch, lane);
   const GlobalSrc<Act, K, BV> src{p, it};
-  produce_tasks<Act, K, BV, DEC>(src, p, it, sQ, sK, sA, sV, sB, tid, NT);
+  produce_tasks<Act, K, BV, DEC, SMS>(src, p, it, sQ, sK, sA, sV, sB, tid, NT);
   __syncthreads();  // every conv_state read of this CTA is done, stage written
   if (tid == 0) sflag[0] = arrive_qk_group(p, it) ? 1 : 0;
   for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * K : sK + (r - T) * K, r < T, lane);
@@ -620,9 +806,13 @@ __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
     mbar_wait_bounded(mbar, 0, kWaitLimitNs);
     return;
   }
-  float4 s[R];
-  load_tile<K, BV>(sbuf, s, warp, lane);
-  consume<Act, K, BV, DEC>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
+  if constexpr (SMS) {
+    consume_smem<Act, K, BV, DEC>(p, it, sQ, sK, sA, sV, sB, sbuf, warp, lane);
+  } else {
+    float4 s[R];
+    load_tile<K, BV>(sbuf, s, warp, lane);
+    consume<Act, K, BV, DEC>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
+  }
   if (sflag[0]) roll_qk<Act, K, BV>(src, p, it, tid, NT);
 }
 

@@ -15,6 +15,7 @@ struct LaunchCfg {
   int warps;    // tile kernel: warps per CTA; ws kernel: consumer warps
   bool ws;      // warp-specialised persistent kernel
   bool decode;  // tile kernel without snapshots, final state written in place
+  bool sms;     // tile kernel with the state kept in shared memory
   int grid;     // CTAs
   size_t smem;  // dynamic shared memory bytes
 };
@@ -44,9 +45,9 @@ int configure_once(Fn fn, unsigned long long* configured) {
   return 0;
 }
 
-template <typename Act, int K, int WARPS, bool DEC>
+template <typename Act, int K, int WARPS, bool DEC, bool SMS = false>
 int launch_tile_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
-  auto fn = kda_tile_kernel<Act, K, WARPS, DEC>;
+  auto fn = kda_tile_kernel<Act, K, WARPS, DEC, SMS>;
   static unsigned long long configured = 0;  // bit per device ordinal (< 64)
   int rc = configure_once(fn, &configured);
   if (rc) return rc;
@@ -67,14 +68,20 @@ int launch_ws_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg
 template <typename Act>
 int launch_tile_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c, cudaStream_t st) {
 #define KDA_CASE(KK, WW)                                                         \
-  if (c.K == KK && c.warps == WW)                                                 \
+  if (c.K == KK && c.warps == WW && !c.sms)                                       \
     return c.decode ? launch_tile_one<Act, KK, WW, true>(tmap, p, c, st)          \
                     : launch_tile_one<Act, KK, WW, false>(tmap, p, c, st);
-#define KDA_CASES_K(KK) KDA_CASE(KK, 1) KDA_CASE(KK, 2) KDA_CASE(KK, 4) KDA_CASE(KK, 8)
+#define KDA_CASE_SMS(KK, WW)                                                     \
+  if (c.K == KK && c.warps == WW && c.sms)                                        \
+    return c.decode ? launch_tile_one<Act, KK, WW, true, true>(tmap, p, c, st)    \
+                    : launch_tile_one<Act, KK, WW, false, true>(tmap, p, c, st);
+#define KDA_CASES_K(KK) KDA_CASE(KK, 1) KDA_CASE(KK, 2) KDA_CASE(KK, 4) KDA_CASE(KK, 8) \
+  KDA_CASE_SMS(KK, 4) KDA_CASE_SMS(KK, 8)
   KDA_CASES_K(32)
   KDA_CASES_K(64)
   KDA_CASES_K(128)
 #undef KDA_CASES_K
+#undef KDA_CASE_SMS
 #undef KDA_CASE
   return -1;
 }

@@ -21,8 +21,9 @@ GATE_SAFE = 1
 VARIANT_AUTO = 0
 VARIANT_SMALL_BATCH = 1
 VARIANT_LARGE_BATCH = 2
+VARIANT_SMEM_STATE = 3
 VARIANTS = {"auto": VARIANT_AUTO, "small_batch": VARIANT_SMALL_BATCH,
-            "large_batch": VARIANT_LARGE_BATCH}
+            "large_batch": VARIANT_LARGE_BATCH, "smem_state": VARIANT_SMEM_STATE}
 F32 = 0
 BF16 = 1
 MAX_T = 16
@@ -166,12 +167,13 @@ def _stream_handle(stream) -> ctypes.c_void_p:
 
 
 def parse_plan(spec: str) -> KdaPlan:
-    """'small:32' / 'large:64' / 'large:64:300' / 'small:128:0:-1' (variant,
+    """'small:32' / 'large:64' / 'smem:128' / 'large:64:300' / 'small:128:0:-1' (variant,
     v-tile width, grid, L2 prefetch distance: -1 off, 0 default)."""
     parts = spec.split(":")
     plan = KdaPlan()
     plan.variant = {"small": VARIANT_SMALL_BATCH, "small_batch": VARIANT_SMALL_BATCH,
-                    "large": VARIANT_LARGE_BATCH, "large_batch": VARIANT_LARGE_BATCH}[parts[0]]
+                    "large": VARIANT_LARGE_BATCH, "large_batch": VARIANT_LARGE_BATCH,
+                    "smem": VARIANT_SMEM_STATE, "smem_state": VARIANT_SMEM_STATE}[parts[0]]
     plan.bv = int(parts[1])
     plan.grid = int(parts[2]) if len(parts) > 2 else 0
     plan.prefetch = int(parts[3]) if len(parts) > 3 else 0

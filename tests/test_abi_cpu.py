@@ -64,11 +64,13 @@ def test_plan_auto_uses_one_item_per_cta(kda):
     p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
     assert p.variant == kda.VARIANT_SMALL_BATCH
     assert p.bv == 128 and p.warps == 8 and p.items == 256 * 32 and p.grid == p.items
-    # single-token verifies of grouped heads over many units: half states
+    # single-token calls over many units: state kept in shared memory
     p2 = kda.make_plan(kda.make_shape(512, 1, 32, 64), 152)
-    assert p2.bv == 64 and p2.items == 512 * 64 * 2
-    assert kda.make_plan(kda.make_shape(512, 2, 32, 64), 152).bv == 128
-    assert kda.make_plan(kda.make_shape(512, 1, 32, 32), 152).bv == 128
+    assert p2.variant == kda.VARIANT_SMEM_STATE and p2.bv == 128 and p2.items == 512 * 64
+    assert p2.ctas_per_sm == 3
+    p3 = kda.make_plan(kda.make_shape(512, 2, 32, 64), 152)
+    assert p3.variant == kda.VARIANT_SMALL_BATCH and p3.bv == 128
+    assert kda.make_plan(kda.make_shape(2, 1, 16, 16), 152).variant == kda.VARIANT_SMALL_BATCH
     # L2 prefetch 3/8 of a wave of resident CTAs ahead
     assert p.prefetch == 152 * p.ctas_per_sm * 3 // 8 > 0
     # fewer units than SMs: whole states per CTA

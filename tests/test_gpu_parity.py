@@ -24,7 +24,7 @@ pytestmark = pytest.mark.gpu
 VARIANTS = ("auto", "small_batch", "large_batch")
 # every explicit plan of a V = 128 problem
 ALL_PLANS = ("small:16", "small:32", "small:64", "small:128", "small:128:0:-1", "small:64:0:7",
-             "large:32", "large:64", "large:128")
+             "large:32", "large:64", "large:128", "smem:64", "smem:128")
 
 
 @pytest.fixture(scope="module", autouse=True)
