@@ -58,11 +58,13 @@ typedef enum {
   KDA_VARIANT_LARGE_BATCH = 2, /* persistent, warp-specialised CTAs; the next item's inputs
                                   and state tile staged by TMA while the current one runs */
   KDA_VARIANT_SMEM_STATE = 3   /* one item per CTA, the state kept in shared memory instead
-                                  of registers (more CTAs per SM; v-tile 64 or 128) */
+                                  of registers (more CTAs per SM; v-tile 64 or 128; the
+                                  only variant for K = 256) */
 } kda_variant;
 
 /* Problem shape.  Supported: T in [1, KDA_MAX_T] (N == 0 is a no-op),
- * H >= 1, HV a multiple of H, W == 4, K and V in {32, 64, 128}. */
+ * H >= 1, HV a multiple of H, W == 4, K and V in {32, 64, 128, 256}.  K = 256
+ * runs on the shared-memory-state variant only (KDA_VARIANT_SMEM_STATE). */
 typedef struct {
   int N, T, H, HV, K, V, W;
   kda_dtype act;

@@ -20,7 +20,7 @@ using kda::Params;
 constexpr int kSmemPerSm = 233472;  // bytes of shared memory per SM (228 KB)
 constexpr int kSmemReservedPerCta = 1024;
 
-bool supported_dim(int x) { return x == 32 || x == 64 || x == 128; }
+bool supported_dim(int x) { return x == 32 || x == 64 || x == 128 || x == 256; }
 
 int check_shape(const kda_shape* s) {
   if (!s) return KDA_ERR_NULL;
@@ -46,11 +46,12 @@ bool valid_tile_bv(int bv, int V) { return (bv == 16 || bv == 32 || bv == 64 || 
 bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
 bool valid_sms_bv(int bv, int V) { return (bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
 
-// A plan's tile width against its variant (decode: no persistent variant).
-bool valid_plan(const kda_plan* plan, int V, bool decode) {
+// A plan's tile width against its variant (decode: no persistent variant;
+// K = 256: only the shared-memory state fits).
+bool valid_plan(const kda_plan* plan, int K, int V, bool decode) {
   switch (plan->variant) {
-    case KDA_VARIANT_SMALL_BATCH: return valid_tile_bv(plan->bv, V);
-    case KDA_VARIANT_LARGE_BATCH: return !decode && valid_ws_bv(plan->bv, V);
+    case KDA_VARIANT_SMALL_BATCH: return K <= 128 && valid_tile_bv(plan->bv, V);
+    case KDA_VARIANT_LARGE_BATCH: return K <= 128 && !decode && valid_ws_bv(plan->bv, V);
     case KDA_VARIANT_SMEM_STATE: return valid_sms_bv(plan->bv, V);
     default: return false;
   }
@@ -146,7 +147,13 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
     return KDA_ERR_VARIANT;
   const long long units = (long long)s->N * s->HV;
   std::memset(out, 0, sizeof(*out));
-  if (variant == KDA_VARIANT_LARGE_BATCH) {
+  if (s->K == 256) {
+    // 256 rows do not fit the register layout: state in shared memory, 64-wide tiles
+    if (variant == KDA_VARIANT_SMALL_BATCH || variant == KDA_VARIANT_LARGE_BATCH) return KDA_ERR_VARIANT;
+    if (s->V < 64) return KDA_ERR_VARIANT;
+    out->variant = KDA_VARIANT_SMEM_STATE;
+    out->bv = 64;
+  } else if (variant == KDA_VARIANT_LARGE_BATCH) {
     out->variant = KDA_VARIANT_LARGE_BATCH;
     out->bv = s->V >= 64 ? 64 : s->V;
   } else if (variant == KDA_VARIANT_SMEM_STATE) {
@@ -371,7 +378,7 @@ int verify_with(const kda_shape* s, const Pools& pl, const void* mixed_qkv, cons
   int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
                          o, inter_ssm, conv_snapshots, workspace, workspace_bytes, pl);
   if (rc || s->N == 0) return rc;
-  if (plan && !valid_plan(plan, s->V, false)) return KDA_ERR_VARIANT;
+  if (plan && !valid_plan(plan, s->K, s->V, false)) return KDA_ERR_VARIANT;
   int num_sms = 0;
   rc = num_sms_of_current_device(&num_sms);
   if (rc) return rc;
@@ -467,7 +474,7 @@ int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void
       if (j != i && overlap(wr[i], wr[j])) return KDA_ERR_ALIAS;
   }
   // decode runs the one-item-per-CTA kernels only
-  if (plan && !valid_plan(plan, s->V, true)) return KDA_ERR_VARIANT;
+  if (plan && !valid_plan(plan, s->K, s->V, true)) return KDA_ERR_VARIANT;
   int num_sms = 0;
   rc = num_sms_of_current_device(&num_sms);
   if (rc) return rc;

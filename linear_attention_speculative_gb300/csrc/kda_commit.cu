@@ -88,8 +88,8 @@ extern "C" int kda_commit_indexed(const kda_shape* s, const kda_state_indices* i
   if (!s) return KDA_ERR_NULL;
   if (s->act != KDA_F32 && s->act != KDA_BF16) return KDA_ERR_DTYPE;
   if (s->N < 0 || s->T < 1 || s->T > KDA_MAX_T || s->H < 1 || s->HV < s->H ||
-      s->HV % s->H != 0 || s->W != 4 || (s->K != 32 && s->K != 64 && s->K != 128) ||
-      (s->V != 32 && s->V != 64 && s->V != 128))
+      s->HV % s->H != 0 || s->W != 4 || (s->K != 32 && s->K != 64 && s->K != 128 && s->K != 256) ||
+      (s->V != 32 && s->V != 64 && s->V != 128 && s->V != 256))
     return KDA_ERR_SHAPE;
   if (s->N == 0) return KDA_OK;
   if (!accepted || !inter_ssm || !conv_snapshots || !S || !conv_state) return KDA_ERR_NULL;

@@ -761,7 +761,8 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   constexpr int BV = WARPS * 16;
   constexpr int NT = WARPS * 32;
   constexpr int R = K / 8;
-  static_assert(K % 32 == 0 && K <= 128, "K must be 32, 64 or 128");
+  // K = 256 keeps 32 rows x 4 columns per thread: only the shared-memory state fits
+  static_assert(K % 32 == 0 && (K <= 128 || (K == 256 && SMS)), "unsupported K for this variant");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);

@@ -80,6 +80,8 @@ int launch_tile_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchC
   KDA_CASES_K(32)
   KDA_CASES_K(64)
   KDA_CASES_K(128)
+  KDA_CASE_SMS(256, 4)
+  KDA_CASE_SMS(256, 8)
 #undef KDA_CASES_K
 #undef KDA_CASE_SMS
 #undef KDA_CASE

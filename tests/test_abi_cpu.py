@@ -96,7 +96,7 @@ def test_plan_small_heads(kda):
     assert small.variant == kda.VARIANT_SMALL_BATCH and small.bv in (16, 32)
 
 
-@pytest.mark.parametrize("bad", [dict(T=0), dict(T=17), dict(W=3), dict(K=96), dict(V=256),
+@pytest.mark.parametrize("bad", [dict(T=0), dict(T=17), dict(W=3), dict(K=96), dict(V=512),
                                  dict(H=3, HV=4), dict(HV=1, H=2)])
 def test_plan_rejects_bad_shapes(kda, bad):
     args = dict(N=2, T=2, H=2, HV=2, K=32, V=32, W=4)
@@ -267,3 +267,16 @@ def test_decode_rejects_bad_arguments(kda):
     assert call(o=p["S0"] + 64) == -5                 # output inside the in/out state
     assert call(plan=kda.parse_plan("large:32")) == -8
     assert call(plan=kda.parse_plan("small:64")) == -8  # wider than V = 32
+
+
+def test_plan_head_dim_256_uses_the_shared_memory_state(kda):
+    p = kda.make_plan(kda.make_shape(64, 4, 8, 16, K=256, V=256), 152)
+    assert p.variant == kda.VARIANT_SMEM_STATE and p.bv == 64 and p.items == 64 * 16 * 4
+    q = kda.make_plan(kda.make_shape(64, 4, 8, 16, K=128, V=256), 152)
+    assert q.variant == kda.VARIANT_SMALL_BATCH and q.bv == 128 and q.items == 64 * 16 * 2
+    for v in ("small_batch", "large_batch"):
+        with pytest.raises(kda.KdaError) as e:
+            kda.make_plan(kda.make_shape(4, 2, 1, 1, K=256, V=128), 152, v)
+        assert e.value.code == -8
+    s = kda.make_shape(2, 2, 1, 1, K=256, V=128)
+    assert _call_plan(kda, s, _fake_args(kda), kda.parse_plan("small:64")) == -8

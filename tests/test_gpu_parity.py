@@ -299,3 +299,32 @@ def test_parity_sweep_points(wl):
     out, cs = run_kernel(inp, wl.gate, "auto")
     assert_parity(out, cs, ref, seqs=seqs)
     conv_window_properties(inp, out, cs)
+
+
+HEAD256 = [
+    # N, T, H, HV, K, V, act, gate
+    (3, 2, 1, 2, 256, 256, "bf16", "softplus"),
+    (2, 4, 2, 2, 256, 64, "bf16", "safe"),
+    (3, 3, 2, 4, 128, 256, "bf16", "softplus"),
+    (2, 2, 1, 1, 256, 128, "f32", "softplus"),
+]
+
+
+@pytest.mark.parametrize("case", HEAD256, ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}".format(*c))
+def test_head_dim_256(case):
+    N, T, H, HV, K, V, act, gate = case
+    wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=300 + K + V + T)
+    inp = wk.make_inputs(wl)
+    ref = oracle.verify(inp, gate)
+    plans = ["auto"] + [p for p in ("smem:64", "smem:128") if int(p.split(":")[1]) <= V]
+    if K <= 128:
+        plans += ["small:128", "large:64"]
+    first = None
+    for plan in plans:
+        out, cs = run_kernel(inp, gate, plan)
+        assert_parity(out, cs, ref)
+        if first is None:
+            first = (out, cs)
+        else:
+            for key in ("o", "inter_ssm", "conv_snapshots"):
+                assert torch.equal(first[0][key], out[key]), (plan, key)
