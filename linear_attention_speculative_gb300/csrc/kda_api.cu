@@ -277,12 +277,15 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   std::memset(&tmap, 0, sizeof(tmap));
   cuuint64_t gdim[2] = {(cuuint64_t)V, (cuuint64_t)(pl.n_state * HV * K)};
   cuuint64_t gstride[1] = {(cuuint64_t)(V * sizeof(float))};
-  cuuint32_t box[2] = {(cuuint32_t)plan.bv, (cuuint32_t)K};
+  // the kernels load a tile as boxes of 32 columns (128 bytes) with the
+  // 128-byte swizzle, or as one row-major box when the tile is narrower
+  const bool swz = plan.bv >= 32;
+  cuuint32_t box[2] = {(cuuint32_t)kda::tile_box_cols(plan.bv), (cuuint32_t)K};
   cuuint32_t estride[2] = {1, 1};
   CUresult cr = encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(S0), gdim,
                        gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                       swz ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return KDA_ERR_DEVICE;
 
   Params p;

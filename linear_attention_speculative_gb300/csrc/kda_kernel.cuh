@@ -91,13 +91,64 @@ __host__ __device__ constexpr size_t raw_bytes(int T, int K, int BV, int ab) {
          4 * (size_t)K;
 }
 
-// dynamic shared memory of the two kernels
+// dynamic shared memory of the two kernels: 128 header bytes (mbarriers,
+// flags), up to 1023 bytes of padding so that the state tile starts on a
+// 1024-byte boundary (the 128-byte swizzle pattern repeats every 1024 bytes),
+// the tile, then the stage(s)
+constexpr size_t kSmemHeader = 128 + 1024;
 __host__ __device__ constexpr size_t tile_smem_bytes(int T, int K, int BV) {
-  return 128 + sizeof(float) * ((size_t)K * BV + stage_floats(T, K, BV));
+  return kSmemHeader + sizeof(float) * ((size_t)K * BV + stage_floats(T, K, BV));
 }
 __host__ __device__ constexpr size_t ws_smem_bytes(int T, int K, int BV, int ab) {
-  return 128 + sizeof(float) * ((size_t)K * BV + 2 * (size_t)stage_floats(T, K, BV)) +
+  return kSmemHeader + sizeof(float) * ((size_t)K * BV + 2 * (size_t)stage_floats(T, K, BV)) +
          round16(raw_bytes(T, K, BV, ab));
+}
+
+// ---------------------------------------------------------------------------
+// state-tile layout and row ownership
+// ---------------------------------------------------------------------------
+// Consumer thread (row group rg, column quad cg) owns rows 8 i + row_perm(rg),
+// i < K/8, with row_perm = 0 4 1 5 2 6 3 7: the two row groups that share a
+// shared-memory phase read rows four apart, which the 128-byte swizzle places
+// in opposite halves of the banks, so tile reads are conflict-free.  q, k and
+// alpha are staged in the matching order (stage_pos), so a thread's K/8 values
+// sit next to each other.
+__device__ __forceinline__ int row_perm(int rg) { return (rg >> 1) + 4 * (rg & 1); }
+__device__ __forceinline__ int own_row(int rg, int i) { return 8 * i + row_perm(rg); }
+template <int K>
+__device__ __forceinline__ int stage_pos(int k) {
+  const int m = k & 7;
+  const int g = m < 4 ? 2 * m : 2 * (m - 4) + 1;  // the row group that owns row k
+  return g * (K / 8) + (k >> 3);
+}
+
+// The tile as TMA leaves it: for BV >= 32, 32-column boxes of K rows x 128
+// bytes with the 128-byte swizzle (16-byte chunk c of row k stored at chunk
+// c ^ (k & 7)); narrower tiles row-major.
+__host__ __device__ constexpr int tile_box_cols(int BV) { return BV >= 32 ? 32 : BV; }
+template <int K, int BV>
+__device__ __forceinline__ int tile_index(int k, int col) {
+  if constexpr (BV >= 32) {
+    return (col >> 5) * (K * 32) + k * 32 + ((((col >> 2) & 7) ^ (k & 7)) << 2) + (col & 3);
+  } else {
+    return k * BV + col;
+  }
+}
+
+// Start of the state tile: after the header, on a 1024-byte boundary.
+__device__ __forceinline__ float* tile_base(unsigned char* smem) {
+  const uint32_t a = smem_u32(smem) + 128;
+  return reinterpret_cast<float*>(smem + 128 + ((1024u - (a & 1023u)) & 1023u));
+}
+
+// TMA loads of one tile (one per box), all completing on `bar`.
+template <int K, int BV>
+__device__ __forceinline__ void tma_load_tile(float* tile, const CUtensorMap* map, int vt,
+                                              long long s_unit, uint64_t* bar, uint64_t pol) {
+  constexpr int BOX = tile_box_cols(BV);
+#pragma unroll
+  for (int b = 0; b < BV / BOX; ++b)
+    tma_load_2d(tile + b * K * BOX, map, vt * BV + b * BOX, static_cast<int>(s_unit * K), bar, pol);
 }
 
 struct Item {
@@ -226,14 +277,14 @@ __device__ __forceinline__ void select_state(const Raw (&cs)[3 * VEC], int idx, 
 }
 
 // One conv task: VEC channels of block `kind` at token t.  Writes SiLU(conv)
-// to dst[e], the snapshot of token t when `snap`, and at t = T-1 the rolled
+// to y[e], the snapshot of token t when `snap`, and at t = T-1 the rolled
 // state of these channels when `roll`.  This form unpacks every input value
 // into its own register (fewest instructions); conv_task_packed below does the
 // same arithmetic from packed words, for kernels with a tight register cap.
 template <typename Act, typename Src>
 __device__ __forceinline__ void conv_task_unpacked(const Src& src, const Params& p, const Item& it,
-                                          int kind, int e0, int c, int t, float* dst, bool snap,
-                                          bool roll) {
+                                          int kind, int e0, int c, int t,
+                                          float (&y)[ActT<Act>::VEC], bool snap, bool roll) {
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
@@ -257,7 +308,6 @@ __device__ __forceinline__ void conv_task_unpacked(const Src& src, const Params&
   Raw wr[4 * VEC];
 #pragma unroll
   for (int m = 0; m < 4; ++m) AT::unpack(src.w(kind, e0, m), wr + m * VEC);
-  float y[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) {
     float acc = __fmul_rn(AT::to_f(wr[e * kConvW]), AT::to_f(win[0][e]));
@@ -265,9 +315,6 @@ __device__ __forceinline__ void conv_task_unpacked(const Src& src, const Params&
     for (int j = 1; j < kConvW; ++j) acc = __fmaf_rn(AT::to_f(wr[e * kConvW + j]), AT::to_f(win[j][e]), acc);
     y[e] = silu_f(acc);
   }
-#pragma unroll
-  for (int e = 0; e < VEC; e += 4)
-    *reinterpret_cast<float4*>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
   const bool do_roll = roll && t == T - 1;
   if (snap || do_roll) {
     // the raw window after token t: x_ext[t+1 .. t+3], channel-major [e][j]
@@ -310,8 +357,8 @@ __device__ __forceinline__ uint32_t raw_at(const uint4& w, int i) {
 // are extracted where they are used.
 template <typename Act, typename Src>
 __device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p, const Item& it,
-                                          int kind, int e0, int c, int t, float* dst, bool snap,
-                                          bool roll) {
+                                          int kind, int e0, int c, int t,
+                                          float (&y)[ActT<Act>::VEC], bool snap, bool roll) {
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
@@ -338,7 +385,6 @@ __device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p
   uint4 ww[4];
 #pragma unroll
   for (int m = 0; m < 4; ++m) ww[m] = src.w(kind, e0, m);
-  float y[VEC];
 #pragma unroll
   for (int e = 0; e < VEC; ++e) {
     float acc = __fmul_rn(AT::to_f(raw_at<Act>(ww[(e * 4) / VEC], (e * 4) % VEC)), AT::to_f(xraw(0, e)));
@@ -348,9 +394,6 @@ __device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p
                       AT::to_f(xraw(j, e)), acc);
     y[e] = silu_f(acc);
   }
-#pragma unroll
-  for (int e = 0; e < VEC; e += 4)
-    *reinterpret_cast<float4*>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
   const bool do_roll = roll && t == T - 1;
   if (snap || do_roll) {
     // the raw window after token t: x_ext[t+1 .. t+3], channel-major [e][j]
@@ -377,13 +420,12 @@ __device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p
 // One gate task: alpha = exp(g) of VEC channels at token t.
 template <typename Act, typename Src>
 __device__ __forceinline__ void gate_task(const Src& src, int gate_mode, float negA, int t,
-                                          int e0, float* dst) {
+                                          int e0, float (&al)[ActT<Act>::VEC]) {
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
   Raw r[VEC];
   AT::unpack(src.a(t, e0), r);
-  float al[VEC];
   if (gate_mode == 0) {
 #pragma unroll
     for (int e = 0; e < VEC; e += 4) {
@@ -399,9 +441,6 @@ __device__ __forceinline__ void gate_task(const Src& src, int gate_mode, float n
 #pragma unroll
     for (int e = 0; e < VEC; ++e) al[e] = expf(fminf(AT::to_f(r[e]), 0.0f));
   }
-#pragma unroll
-  for (int e = 0; e < VEC; e += 4)
-    *reinterpret_cast<float4*>(dst + e) = make_float4(al[e], al[e + 1], al[e + 2], al[e + 3]);
 }
 
 template <typename Act>
@@ -435,17 +474,29 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
       const int t = task - cv * T;
       const int kind = cv < NQ ? 0 : (cv < 2 * NQ ? 1 : 2);
       const int e0 = (cv - kind * NQ) * VEC;
-      float* dst = kind == 0 ? sQ + t * K + e0 : (kind == 1 ? sK + t * K + e0 : sV + t * BV + e0);
       const int c = block_channel<K, BV>(p, it, kind) + e0;
+      float y[VEC];
       if constexpr (PACKED)
-        conv_task_packed<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
+        conv_task_packed<Act>(src, p, it, kind, e0, c, t, y, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
       else
-        conv_task_unpacked<Act>(src, p, it, kind, e0, c, t, dst, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
+        conv_task_unpacked<Act>(src, p, it, kind, e0, c, t, y, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
+      if (kind == 2) {  // v: column order
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4)
+          *reinterpret_cast<float4*>(sV + t * BV + e0 + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+      } else {  // q, k: the consumers' row order
+        float* dst = (kind == 0 ? sQ : sK) + t * K;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) dst[stage_pos<K>(e0 + e)] = y[e];
+      }
     } else if (task < n_conv + n_gate) {
       const int g = task - n_conv;
       const int t = g / NQ;
       const int e0 = (g - t * NQ) * VEC;
-      gate_task<Act>(src, p.gate_mode, negA, t, e0, sA + t * K + e0);
+      float al[VEC];
+      gate_task<Act>(src, p.gate_mode, negA, t, e0, al);
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) sA[t * K + stage_pos<K>(e0 + e)] = al[e];
     } else {
       const int t = task - n_conv - n_gate;
       sB[t] = sigmoid_f(load_b<Act>(p, it, t));
@@ -530,9 +581,10 @@ template <int K, int BV>
 __device__ __forceinline__ void load_tile(const float* sbuf, float4 (&s)[K / 8], int warp, int lane) {
   constexpr int R = K / 8;
   const int rg = lane >> 2, cg = lane & 3;
-  const float* src = sbuf + (rg * R) * BV + warp * 16 + cg * 4;
+  const int col = warp * 16 + cg * 4;
 #pragma unroll
-  for (int i = 0; i < R; ++i) s[i] = *reinterpret_cast<const float4*>(src + i * BV);
+  for (int i = 0; i < R; ++i)
+    s[i] = *reinterpret_cast<const float4*>(sbuf + tile_index<K, BV>(own_row(rg, i), col));
 }
 
 template <typename Act, int K, int BV, bool DEC = false>
@@ -581,8 +633,11 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
     u.x = __fmul_rn(be, __fsub_rn(v4.x, acc.x)); u.y = __fmul_rn(be, __fsub_rn(v4.y, acc.y));
     u.z = __fmul_rn(be, __fsub_rn(v4.z, acc.z)); u.w = __fmul_rn(be, __fsub_rn(v4.w, acc.w));
     // rank-1 update, partial S^T q, streaming snapshot store
+    // this thread's rows are own_row(rg, i) = 8 i + row_perm(rg): start at row
+    // row_perm(rg), step 8 rows
     float* dst = DEC ? nullptr
-                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + rg * R) * V + colg;
+                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + row_perm(rg)) * V + colg;
+    const size_t step8 = (size_t)8 * V;
     float4 oa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < R; i += 4) {
@@ -597,7 +652,7 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
         x.z = __fmaf_rn(kv[j], u.z, x.z); x.w = __fmaf_rn(kv[j], u.w, x.w);
         oa.x = __fmaf_rn(x.x, qv[j], oa.x); oa.y = __fmaf_rn(x.y, qv[j], oa.y);
         oa.z = __fmaf_rn(x.z, qv[j], oa.z); oa.w = __fmaf_rn(x.w, qv[j], oa.w);
-        if constexpr (!DEC) st_stream_f4(dst + (size_t)(i + j) * V, x);
+        if constexpr (!DEC) st_stream_f4(dst + (size_t)(i + j) * step8, x);
       }
     }
 #pragma unroll
@@ -614,9 +669,9 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
   }
   if constexpr (DEC) {
     // decode: the state after the last token replaces the persistent state
-    float* dst = p.S_out + ((size_t)it.s_unit * K + rg * R) * V + colg;
+    float* dst = p.S_out + ((size_t)it.s_unit * K + row_perm(rg)) * V + colg;
 #pragma unroll
-    for (int i = 0; i < R; ++i) st_stream_f4(dst + (size_t)i * V, s[i]);
+    for (int i = 0; i < R; ++i) st_stream_f4(dst + (size_t)i * 8 * V, s[i]);
   }
 }
 
@@ -649,7 +704,10 @@ __device__ __forceinline__ void prefetch_item_l2(const Params& p, const CUtensor
                            ((((size_t)it.n * T + t) * p.HV + it.hv) * K) * AB,
                        K * AB);
     } else {
-      tma_prefetch_2d(tmap, it.vt * BV, static_cast<int>(it.s_unit * K));
+      constexpr int BOX = tile_box_cols(BV);
+#pragma unroll
+      for (int bx = 0; bx < BV / BOX; ++bx)
+        tma_prefetch_2d(tmap, it.vt * BV + bx * BOX, static_cast<int>(it.s_unit * K));
     }
   }
 }
@@ -673,7 +731,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
   const int T = p.T;
   const int V = p.V;
   const size_t colg = (size_t)it.vt * BV + col;
-  float* own = sS + (rg * R) * BV + col;
+
   for (int t = 0; t < T; ++t) {
     const float* al = sA + t * K + rg * R;
     const float* kk = sK + t * K + rg * R;
@@ -687,7 +745,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
       const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float4 x = *reinterpret_cast<const float4*>(own + (i + j) * BV);
+        float4 x = *reinterpret_cast<const float4*>(sS + tile_index<K, BV>(own_row(rg, i + j), col));
         x.x = __fmul_rn(x.x, av[j]); x.y = __fmul_rn(x.y, av[j]);
         x.z = __fmul_rn(x.z, av[j]); x.w = __fmul_rn(x.w, av[j]);
         acc.x = __fmaf_rn(x.x, kv[j], acc.x); acc.y = __fmaf_rn(x.y, kv[j], acc.y);
@@ -707,8 +765,9 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
     u.x = __fmul_rn(be, __fsub_rn(v4.x, acc.x)); u.y = __fmul_rn(be, __fsub_rn(v4.y, acc.y));
     u.z = __fmul_rn(be, __fsub_rn(v4.z, acc.z)); u.w = __fmul_rn(be, __fsub_rn(v4.w, acc.w));
     const bool last = t == T - 1;
-    float* dst = DEC ? (last ? p.S_out + ((size_t)it.s_unit * K + rg * R) * V + colg : nullptr)
-                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + rg * R) * V + colg;
+    float* dst = DEC ? (last ? p.S_out + ((size_t)it.s_unit * K + row_perm(rg)) * V + colg : nullptr)
+                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + row_perm(rg)) * V + colg;
+    const size_t step8 = (size_t)8 * V;
     float4 oa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < R; i += 4) {
@@ -720,7 +779,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
       const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float4* ep = reinterpret_cast<float4*>(own + (i + j) * BV);
+        float4* ep = reinterpret_cast<float4*>(sS + tile_index<K, BV>(own_row(rg, i + j), col));
         float4 x = *ep;
         x.x = __fmul_rn(x.x, av[j]); x.y = __fmul_rn(x.y, av[j]);
         x.z = __fmul_rn(x.z, av[j]); x.w = __fmul_rn(x.w, av[j]);
@@ -728,7 +787,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
         x.z = __fmaf_rn(kv[j], u.z, x.z); x.w = __fmaf_rn(kv[j], u.w, x.w);
         oa.x = __fmaf_rn(x.x, qv[j], oa.x); oa.y = __fmaf_rn(x.y, qv[j], oa.y);
         oa.z = __fmaf_rn(x.z, qv[j], oa.z); oa.w = __fmaf_rn(x.w, qv[j], oa.w);
-        if (DEC ? last : true) st_stream_f4(dst + (size_t)(i + j) * V, x);
+        if (DEC ? last : true) st_stream_f4(dst + (size_t)(i + j) * step8, x);
         if (!last) *ep = x;
       }
     }
@@ -767,7 +826,7 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);
   int* sflag = reinterpret_cast<int*>(smem + 8);
-  float* sbuf = reinterpret_cast<float*>(smem + 128);
+  float* sbuf = tile_base(smem);
   const int T = p.T;
   float* sQ = sbuf + K * BV;
   float* sK = sQ + T * K;
@@ -790,8 +849,7 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     fence_mbar_init();
     prefetch_tensormap(&tmap_s0);
     mbar_arrive_expect_tx(mbar, K * BV * sizeof(float));
-    tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.s_unit * K), mbar,
-                l2_policy_evict_first());
+    tma_load_tile<K, BV>(sbuf, &tmap_s0, it.vt, it.s_unit, mbar, l2_policy_evict_first());
   }
   if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items)
     prefetch_item_l2<Act, K, BV>(p, &tmap_s0, item + p.prefetch, lane);
@@ -921,7 +979,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
   extern __shared__ __align__(128) unsigned char smem[];
   WsBars* bars = reinterpret_cast<WsBars*>(smem);
   volatile int* abort_flag = &bars->abort_flag;
-  float* sbuf = reinterpret_cast<float*>(smem + 128);
+  float* sbuf = tile_base(smem);
   const int T = p.T;
   const int sf = stage_floats(T, K, BV);
   float* stage0 = sbuf + K * BV;
@@ -959,7 +1017,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
     if (lane == 0) {
       prefetch_tensormap(&tmap_s0);
       mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
-      tma_load_2d(sbuf, &tmap_s0, it.vt * BV, static_cast<int>(it.s_unit * K), &bars->tile_full, pol);
+      tma_load_tile<K, BV>(sbuf, &tmap_s0, it.vt, it.s_unit, &bars->tile_full, pol);
       mbar_arrive_expect_tx(&bars->raw_full, raw_tx_bytes<Act, K, BV>(p));
     }
     __syncwarp();
@@ -1005,7 +1063,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
       if (lane == 0) {
         fence_proxy_async_smem();
         mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
-        tma_load_2d(sbuf, &tmap_s0, nx.vt * BV, static_cast<int>(nx.s_unit * K), &bars->tile_full, pol);
+        tma_load_tile<K, BV>(sbuf, &tmap_s0, nx.vt, nx.s_unit, &bars->tile_full, pol);
       }
       tile_phase = j + 1;
       item = next;
