@@ -328,3 +328,41 @@ def test_head_dim_256(case):
         else:
             for key in ("o", "inter_ssm", "conv_snapshots"):
                 assert torch.equal(first[0][key], out[key]), (plan, key)
+
+
+def _random_cases(n=24, seed=2026):
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        K = int(rng.choice([32, 64, 128, 256]))
+        V = int(rng.choice([32, 64, 128, 256]))
+        H = int(rng.integers(1, 4))
+        HV = H * int(rng.choice([1, 2, 3, 4]))
+        T = int(rng.integers(1, 17))
+        N = int(rng.integers(1, 7))
+        act = str(rng.choice(["bf16", "f32"]))
+        gate = str(rng.choice(["softplus", "safe"]))
+        if K == 256:
+            plans = [p for p in ("smem:64", "smem:128") if int(p.split(":")[1]) <= V]
+        else:
+            plans = [p for p in ("small:16", "small:32", "small:64", "small:128", "large:32",
+                                 "large:64", "smem:64", "smem:128") if int(p.split(":")[1]) <= V]
+        if not plans:
+            continue
+        plan = str(rng.choice(plans))
+        cases.append((N, T, H, HV, K, V, act, gate, plan, 1000 + len(cases)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}_{}".format(*c[:9]))
+def test_random_shapes_and_plans(case):
+    N, T, H, HV, K, V, act, gate, plan, seed = case
+    wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=seed)
+    inp = wk.make_inputs(wl)
+    ref = oracle.verify(inp, gate)
+    out, cs = run_kernel(inp, gate, plan)
+    assert_parity(out, cs, ref)
+    auto, auto_cs = run_kernel(inp, gate, "auto")
+    for key in ("o", "inter_ssm", "conv_snapshots"):
+        assert torch.equal(out[key], auto[key]), key
+    assert torch.equal(cs, auto_cs)
