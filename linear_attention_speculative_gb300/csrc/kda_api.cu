@@ -72,7 +72,7 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
     out->grid = (int)std::max(1LL, std::min(out->items, grid));
   } else {
     out->warps = out->bv / 16;
-    const size_t smem = kda::tile_smem_bytes(s->T, s->K, out->bv);
+    const size_t smem = kda::tile_smem_bytes(s->T, s->K, out->bv, ab);
     const bool sms = out->variant == KDA_VARIANT_SMEM_STATE;
     out->ctas_per_sm = ctas_per_sm_for(kda::tile_min_blocks(out->warps, sms), smem);
     out->grid = (int)std::max(1LL, out->items);
@@ -163,12 +163,13 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
   } else {
     // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
     // many threads for its producer tasks and the q/k conv is not repeated per
-    // v-tile.  Single-token calls over many units keep the state in shared
-    // memory instead (3 CTAs/SM instead of 2): measured on GB300 +4..10 % at
-    // T = 1, but slower from T = 2 on (two shared-memory passes per token).
+    // v-tile.  Calls of one or two tokens over many units keep the state in
+    // shared memory instead (3 CTAs/SM instead of 2): measured on GB300
+    // +5..11 % at T = 1 and +3..5 % at T = 2, but slower from T = 3 on (two
+    // shared-memory passes per token).
     out->variant = KDA_VARIANT_SMALL_BATCH;
     out->bv = std::min(s->V, 128);
-    if (s->T == 1 && s->V >= 128 && units >= 4LL * num_sms) out->variant = KDA_VARIANT_SMEM_STATE;
+    if (s->T <= 2 && s->V >= 128 && units >= 4LL * num_sms) out->variant = KDA_VARIANT_SMEM_STATE;
   }
   finish_plan(s, num_sms, out, 0, 0);
   return KDA_OK;
@@ -329,7 +330,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   cfg.grid = plan.grid;
   const int ab = s->act == KDA_F32 ? 4 : 2;
   cfg.smem = cfg.ws ? kda::ws_smem_bytes(s->T, s->K, plan.bv, ab)
-                    : kda::tile_smem_bytes(s->T, s->K, plan.bv);
+                    : kda::tile_smem_bytes(s->T, s->K, plan.bv, ab);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int rc;
   if (s->act == KDA_BF16)

@@ -36,7 +36,11 @@
 // by G * (V / BV) items.  Each item arrives on a per-group counter after its
 // reads; the last arrival rolls the group's q/k conv_state and resets the
 // counter to zero.  Nothing ever waits on another CTA.  v channels belong to
-// exactly one item, which rolls them itself.
+// exactly one item, which rolls them itself.  In the one-item kernel, whose
+// threads read conv_state straight from global memory, the producer stages the
+// new windows in shared memory and every roll is stored after the barrier
+// that ends the CTA's conv_state reads; the warp-specialised kernel reads its
+// raw inputs from shared memory and rolls directly.
 #pragma once
 
 #include "kda_device.cuh"
@@ -78,9 +82,25 @@ constexpr int kStatusBadIndex = 4;                // KDA_STATUS_BAD_INDEX
 __host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
 __host__ __device__ constexpr size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
 
-// floats of one stage: q[T][K], k[T][K], alpha[T][K], v[T][BV], beta[round4(T)]
+// A staged K-vector (q, k or alpha of one token) is held as eight row-group
+// blocks of K/8 values (see stage_pos).  Blocks are stage_rs(K) floats apart:
+// K/8 rounded so that stride/4 is odd, which starts the eight blocks in eight
+// different 4-bank groups, so the consumers' 16-byte reads of them (one block
+// per row group) are conflict-free.
+__host__ __device__ constexpr int stage_rs(int K) { return K / 8 + (((K / 32) & 1) ? 0 : 4); }
+__host__ __device__ constexpr int stage_ks(int K) { return 8 * stage_rs(K); }
+
+// floats of one stage: q[T][KS], k[T][KS], alpha[T][KS], v[T][BV],
+// beta[round4(T)] with KS = stage_ks(K)
 __host__ __device__ constexpr int stage_floats(int T, int K, int BV) {
-  return 3 * T * K + T * BV + round4(T);
+  return 3 * T * stage_ks(K) + T * BV + round4(T);
+}
+
+// bytes of the one-item kernel's staged conv windows: x_ext[T .. T+2] of every
+// channel of the item (2K + BV channels x 3 values), written by the producer
+// and stored to conv_state once no reader of it is left
+__host__ __device__ constexpr size_t roll_stash_bytes(int K, int BV, int ab) {
+  return (size_t)(2 * K + BV) * 3 * ab;
 }
 
 // raw-input bytes of one item (warp-specialised kernel): x_q, x_k [T][K],
@@ -96,8 +116,9 @@ __host__ __device__ constexpr size_t raw_bytes(int T, int K, int BV, int ab) {
 // 1024-byte boundary (the 128-byte swizzle pattern repeats every 1024 bytes),
 // the tile, then the stage(s)
 constexpr size_t kSmemHeader = 128 + 1024;
-__host__ __device__ constexpr size_t tile_smem_bytes(int T, int K, int BV) {
-  return kSmemHeader + sizeof(float) * ((size_t)K * BV + stage_floats(T, K, BV));
+__host__ __device__ constexpr size_t tile_smem_bytes(int T, int K, int BV, int ab) {
+  return kSmemHeader + sizeof(float) * ((size_t)K * BV + stage_floats(T, K, BV)) +
+         roll_stash_bytes(K, BV, ab);
 }
 __host__ __device__ constexpr size_t ws_smem_bytes(int T, int K, int BV, int ab) {
   return kSmemHeader + sizeof(float) * ((size_t)K * BV + 2 * (size_t)stage_floats(T, K, BV)) +
@@ -119,7 +140,7 @@ template <int K>
 __device__ __forceinline__ int stage_pos(int k) {
   const int m = k & 7;
   const int g = m < 4 ? 2 * m : 2 * (m - 4) + 1;  // the row group that owns row k
-  return g * (K / 8) + (k >> 3);
+  return g * stage_rs(K) + (k >> 3);
 }
 
 // The tile as TMA leaves it: for BV >= 32, 32-column boxes of K rows x 128
@@ -277,14 +298,16 @@ __device__ __forceinline__ void select_state(const Raw (&cs)[3 * VEC], int idx, 
 }
 
 // One conv task: VEC channels of block `kind` at token t.  Writes SiLU(conv)
-// to y[e], the snapshot of token t when `snap`, and at t = T-1 the rolled
-// state of these channels when `roll`.  This form unpacks every input value
+// to y[e], the snapshot of token t when `snap`, at t = T-1 the rolled state of
+// these channels when `roll`, and the raw window after token t (three 16-byte
+// words) to `stash` when it is not null.  This form unpacks every input value
 // into its own register (fewest instructions); conv_task_packed below does the
 // same arithmetic from packed words, for kernels with a tight register cap.
 template <typename Act, typename Src>
 __device__ __forceinline__ void conv_task_unpacked(const Src& src, const Params& p, const Item& it,
                                           int kind, int e0, int c, int t,
-                                          float (&y)[ActT<Act>::VEC], bool snap, bool roll) {
+                                          float (&y)[ActT<Act>::VEC], bool snap, bool roll,
+                                          uint4* stash) {
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
@@ -316,7 +339,7 @@ __device__ __forceinline__ void conv_task_unpacked(const Src& src, const Params&
     y[e] = silu_f(acc);
   }
   const bool do_roll = roll && t == T - 1;
-  if (snap || do_roll) {
+  if (snap || do_roll || stash) {
     // the raw window after token t: x_ext[t+1 .. t+3], channel-major [e][j]
     Raw r[3 * VEC];
 #pragma unroll
@@ -334,6 +357,10 @@ __device__ __forceinline__ void conv_task_unpacked(const Src& src, const Params&
                                          ((size_t)it.cs_row * p.dim + c) * (kConvW - 1));
 #pragma unroll
       for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
+    }
+    if (stash) {
+#pragma unroll
+      for (int m = 0; m < 3; ++m) stash[m] = AT::pack(r + m * VEC);
     }
   }
 }
@@ -358,7 +385,8 @@ __device__ __forceinline__ uint32_t raw_at(const uint4& w, int i) {
 template <typename Act, typename Src>
 __device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p, const Item& it,
                                           int kind, int e0, int c, int t,
-                                          float (&y)[ActT<Act>::VEC], bool snap, bool roll) {
+                                          float (&y)[ActT<Act>::VEC], bool snap, bool roll,
+                                          uint4* stash) {
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
@@ -395,7 +423,7 @@ __device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p
     y[e] = silu_f(acc);
   }
   const bool do_roll = roll && t == T - 1;
-  if (snap || do_roll) {
+  if (snap || do_roll || stash) {
     // the raw window after token t: x_ext[t+1 .. t+3], channel-major [e][j]
     Raw r[3 * VEC];
 #pragma unroll
@@ -413,6 +441,10 @@ __device__ __forceinline__ void conv_task_packed(const Src& src, const Params& p
                                          ((size_t)it.cs_row * p.dim + c) * (kConvW - 1));
 #pragma unroll
       for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
+    }
+    if (stash) {
+#pragma unroll
+      for (int m = 0; m < 3; ++m) stash[m] = AT::pack(r + m * VEC);
     }
   }
 }
@@ -454,13 +486,18 @@ __device__ __forceinline__ float load_b(const Params& p, const Item& it, int t) 
 }
 
 // All conv / gate / beta tasks of one item, spread over `nthr` threads.
+// With `stash` null the v tile's conv_state is rolled here (its raw inputs
+// already sit in shared memory, so no reader is left in global memory);
+// otherwise the raw window after the last token of every channel vector cv is
+// staged at stash[3 cv .. 3 cv + 2] and the caller rolls after a barrier.
 template <typename Act, int K, int BV, bool DEC = false, bool PACKED = false, typename Src>
 __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, const Item& it,
                                               float* sQ, float* sK, float* sA, float* sV,
-                                              float* sB, int tid, int nthr) {
+                                              float* sB, uint4* stash, int tid, int nthr) {
   constexpr int VEC = ActT<Act>::VEC;
   constexpr int NQ = K / VEC;
   constexpr int NCV = 2 * NQ + BV / VEC;  // channel vectors of the item
+  constexpr int KS = stage_ks(K);
   const int T = p.T;
   const int n_conv = NCV * T;
   const int n_gate = NQ * T;
@@ -476,16 +513,18 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
       const int e0 = (cv - kind * NQ) * VEC;
       const int c = block_channel<K, BV>(p, it, kind) + e0;
       float y[VEC];
+      const bool roll_v = kind == 2 && !stash;
+      uint4* st = (stash && t == T - 1) ? stash + 3 * cv : nullptr;
       if constexpr (PACKED)
-        conv_task_packed<Act>(src, p, it, kind, e0, c, t, y, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
+        conv_task_packed<Act>(src, p, it, kind, e0, c, t, y, kind == 2 ? v_snap : qk_snap_owner, roll_v, st);
       else
-        conv_task_unpacked<Act>(src, p, it, kind, e0, c, t, y, kind == 2 ? v_snap : qk_snap_owner, kind == 2);
+        conv_task_unpacked<Act>(src, p, it, kind, e0, c, t, y, kind == 2 ? v_snap : qk_snap_owner, roll_v, st);
       if (kind == 2) {  // v: column order
 #pragma unroll
         for (int e = 0; e < VEC; e += 4)
           *reinterpret_cast<float4*>(sV + t * BV + e0 + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
       } else {  // q, k: the consumers' row order
-        float* dst = (kind == 0 ? sQ : sK) + t * K;
+        float* dst = (kind == 0 ? sQ : sK) + t * KS;
 #pragma unroll
         for (int e = 0; e < VEC; ++e) dst[stage_pos<K>(e0 + e)] = y[e];
       }
@@ -496,7 +535,7 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
       float al[VEC];
       gate_task<Act>(src, p.gate_mode, negA, t, e0, al);
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) sA[t * K + stage_pos<K>(e0 + e)] = al[e];
+      for (int e = 0; e < VEC; ++e) sA[t * KS + stage_pos<K>(e0 + e)] = al[e];
     } else {
       const int t = task - n_conv - n_gate;
       sB[t] = sigmoid_f(load_b<Act>(p, it, t));
@@ -504,14 +543,15 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
   }
 }
 
-// L2 norm of one K-vector by one warp (q additionally scaled by K^-1/2).
+// L2 norm of one staged K-vector by one warp (q additionally scaled by
+// K^-1/2); lane l takes channels l, l + 32, ...
 template <int K>
 __device__ __forceinline__ void l2norm_warp(float* x, bool is_q, int lane) {
   float xs[K / 32];
   float ss = 0.0f;
 #pragma unroll
   for (int m = 0; m < K / 32; ++m) {
-    xs[m] = x[lane + 32 * m];
+    xs[m] = x[stage_pos<K>(lane + 32 * m)];
     ss = __fmaf_rn(xs[m], xs[m], ss);
   }
 #pragma unroll
@@ -519,7 +559,7 @@ __device__ __forceinline__ void l2norm_warp(float* x, bool is_q, int lane) {
   float inv = rsqrtf(__fadd_rn(ss, kL2Eps));
   if (is_q) inv = __fmul_rn(inv, rsqrtf(static_cast<float>(K)));
 #pragma unroll
-  for (int m = 0; m < K / 32; ++m) x[lane + 32 * m] = __fmul_rn(xs[m], inv);
+  for (int m = 0; m < K / 32; ++m) x[stage_pos<K>(lane + 32 * m)] = __fmul_rn(xs[m], inv);
 }
 
 // Arrival of one item on its q/k group counter (one thread).  Returns true
@@ -536,7 +576,8 @@ __device__ __forceinline__ bool arrive_qk_group(const Params& p, const Item& it)
   return true;
 }
 
-// Roll the q/k conv_state of group (n, h) to x_ext[T .. T+2].
+// Roll the q/k conv_state of group (n, h) to x_ext[T .. T+2], re-reading the
+// raw inputs (warp-specialised kernel: from its shared-memory raw buffer).
 template <typename Act, int K, int BV, typename Src>
 __device__ __forceinline__ void roll_qk(const Src& src, const Params& p, const Item& it, int tid,
                                         int nthr) {
@@ -574,6 +615,26 @@ __device__ __forceinline__ void roll_qk(const Src& src, const Params& p, const I
   }
 }
 
+// Store the staged windows x_ext[T .. T+2] (produce_tasks' stash) as the new
+// conv_state: the item's v tile always, the q/k blocks of group (n, h) only
+// when `qk` (the group's last arrival).  Called after a barrier that follows
+// every conv_state read of the CTA.
+template <typename Act, int K, int BV>
+__device__ __forceinline__ void roll_staged(const Params& p, const Item& it, const uint4* stash,
+                                            bool qk, int tid, int nthr) {
+  constexpr int VEC = ActT<Act>::VEC;
+  constexpr int NQ = K / VEC;
+  constexpr int NCV = 2 * NQ + BV / VEC;
+  for (int cv = (qk ? 0 : 2 * NQ) + tid; cv < NCV; cv += nthr) {
+    const int kind = cv < NQ ? 0 : (cv < 2 * NQ ? 1 : 2);
+    const int c = block_channel<K, BV>(p, it, kind) + (cv - kind * NQ) * VEC;
+    char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
+                                       ((size_t)it.cs_row * p.dim + c) * (kConvW - 1));
+#pragma unroll
+    for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, stash[3 * cv + m]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // consumer: the recurrence on register-resident S
 // ---------------------------------------------------------------------------
@@ -592,6 +653,8 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
                                        const float* sK, const float* sA, const float* sV,
                                        const float* sB, float4 (&s)[K / 8], int warp, int lane) {
   constexpr int R = K / 8;
+  constexpr int RS = stage_rs(K);
+  constexpr int KS = stage_ks(K);
   const int rg = lane >> 2;
   const int cg = lane & 3;
   const int col = warp * 16 + cg * 4;  // column within the tile
@@ -599,9 +662,9 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
   const int V = p.V;
   const size_t colg = (size_t)it.vt * BV + col;  // column within the state
   for (int t = 0; t < T; ++t) {
-    const float* al = sA + t * K + rg * R;
-    const float* kk = sK + t * K + rg * R;
-    const float* qq = sQ + t * K + rg * R;
+    const float* al = sA + t * KS + rg * RS;
+    const float* kk = sK + t * KS + rg * RS;
+    const float* qq = sQ + t * KS + rg * RS;
     // decay, then partial S^T k over this thread's rows
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -725,6 +788,8 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
                                             const float* sK, const float* sA, const float* sV,
                                             const float* sB, float* sS, int warp, int lane) {
   constexpr int R = K / 8;
+  constexpr int RS = stage_rs(K);
+  constexpr int KS = stage_ks(K);
   const int rg = lane >> 2;
   const int cg = lane & 3;
   const int col = warp * 16 + cg * 4;
@@ -733,9 +798,9 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
   const size_t colg = (size_t)it.vt * BV + col;
 
   for (int t = 0; t < T; ++t) {
-    const float* al = sA + t * K + rg * R;
-    const float* kk = sK + t * K + rg * R;
-    const float* qq = sQ + t * K + rg * R;
+    const float* al = sA + t * KS + rg * RS;
+    const float* kk = sK + t * KS + rg * RS;
+    const float* qq = sQ + t * KS + rg * RS;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < R; i += 4) {
@@ -828,11 +893,13 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   int* sflag = reinterpret_cast<int*>(smem + 8);
   float* sbuf = tile_base(smem);
   const int T = p.T;
+  constexpr int KS = stage_ks(K);
   float* sQ = sbuf + K * BV;
-  float* sK = sQ + T * K;
-  float* sA = sK + T * K;
-  float* sV = sA + T * K;
+  float* sK = sQ + T * KS;
+  float* sA = sK + T * KS;
+  float* sV = sA + T * KS;
   float* sB = sV + T * BV;
+  uint4* sRoll = reinterpret_cast<uint4*>(sB + round4(T));
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
@@ -854,10 +921,13 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items)
     prefetch_item_l2<Act, K, BV>(p, &tmap_s0, item + p.prefetch, lane);
   const GlobalSrc<Act, K, BV> src{p, it};
-  produce_tasks<Act, K, BV, DEC, SMS>(src, p, it, sQ, sK, sA, sV, sB, tid, NT);
+  produce_tasks<Act, K, BV, DEC, SMS>(src, p, it, sQ, sK, sA, sV, sB, sRoll, tid, NT);
   __syncthreads();  // every conv_state read of this CTA is done, stage written
-  if (tid == 0) sflag[0] = arrive_qk_group(p, it) ? 1 : 0;
-  for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * K : sK + (r - T) * K, r < T, lane);
+  for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
+  // the arrival's fence and atomic run in the last warp, after its own rows
+  // (none while 2T < WARPS), so they overlap the other warps' norms and the
+  // wait for the state tile
+  if (tid == (WARPS - 1) * 32) sflag[0] = arrive_qk_group(p, it) ? 1 : 0;
   const bool ok = mbar_wait_bounded(mbar, 0, kWaitLimitNs);
   if (__syncthreads_or(!ok)) {
     // give up without hanging: report, let the copy in flight land, leave
@@ -872,7 +942,7 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     load_tile<K, BV>(sbuf, s, warp, lane);
     consume<Act, K, BV, DEC>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
   }
-  if (sflag[0]) roll_qk<Act, K, BV>(src, p, it, tid, NT);
+  roll_staged<Act, K, BV>(p, it, sRoll, sflag[0] != 0, tid, NT);
 }
 
 // ---------------------------------------------------------------------------
@@ -974,6 +1044,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
     kda_ws_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
   constexpr int BV = CW * 16;
   constexpr int R = K / 8;
+  constexpr int KS = stage_ks(K);
   static_assert(K % 32 == 0 && K <= 128, "K must be 32, 64 or 128");
 
   extern __shared__ __align__(128) unsigned char smem[];
@@ -1028,9 +1099,9 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
     for (int j = 0;; ++j) {
       const int s = j & 1;
       float* sQ = stage0 + s * sf;
-      float* sK = sQ + T * K;
-      float* sA = sK + T * K;
-      float* sV = sA + T * K;
+      float* sK = sQ + T * KS;
+      float* sA = sK + T * KS;
+      float* sV = sA + T * KS;
       float* sB = sV + T * BV;
       if (!ws_wait(&bars->raw_full, j & 1, abort_flag)) { failed = true; break; }
       if (j >= 2 && !ws_wait(&bars->stage_empty[s], ((j >> 1) + 1) & 1, abort_flag)) {
@@ -1038,7 +1109,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
         break;
       }
       const SmemSrc<Act, K, BV> src{raw, T};
-      produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, lane, 32);
+      produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, nullptr, lane, 32);
       __syncwarp();
       int last = 0;
       if (lane == 0) last = arrive_qk_group(p, it) ? 1 : 0;
@@ -1055,7 +1126,7 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
         issue_raw<Act, K, BV>(p, nx, raw, &bars->raw_full, lane);
         raw_phase = j + 1;
       }
-      for (int r = 0; r < 2 * T; ++r) l2norm_warp<K>(r < T ? sQ + r * K : sK + (r - T) * K, r < T, lane);
+      for (int r = 0; r < 2 * T; ++r) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
       mbar_arrive(&bars->stage_full[s]);
       if (!has_next) break;
       // hand the next state tile over as soon as the consumers hold this one
@@ -1087,8 +1158,8 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
       mbar_arrive(&bars->tile_empty);
       if (!ws_wait(&bars->stage_full[s], (j >> 1) & 1, abort_flag)) { ws_fail(p, abort_flag); return; }
       const float* st = stage0 + s * sf;
-      consume<Act, K, BV>(p, it, st, st + T * K, st + 2 * T * K, st + 3 * T * K,
-                          st + 3 * T * K + T * BV, sreg, warp, lane);
+      consume<Act, K, BV>(p, it, st, st + T * KS, st + 2 * T * KS, st + 3 * T * KS,
+                          st + 3 * T * KS + T * BV, sreg, warp, lane);
       mbar_arrive(&bars->stage_empty[s]);
     }
   }
