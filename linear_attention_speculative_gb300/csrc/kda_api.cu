@@ -163,13 +163,15 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
   } else {
     // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
     // many threads for its producer tasks and the q/k conv is not repeated per
-    // v-tile.  Calls of one or two tokens over many units keep the state in
-    // shared memory instead (3 CTAs/SM instead of 2): measured on GB300
-    // +5..11 % at T = 1 and +3..5 % at T = 2, but slower from T = 3 on (two
-    // shared-memory passes per token).
+    // v-tile.  Single-token calls over many units keep the state in shared
+    // memory instead (3 CTAs/SM instead of 2): measured on GB300 +5..11 % at
+    // T = 1.  At T = 2 the two are within a few per cent of each other, the
+    // shared-memory state ahead (+2 % on average) only from ~50 units per SM;
+    // from T = 3 on it is slower (two shared-memory passes per token).
     out->variant = KDA_VARIANT_SMALL_BATCH;
     out->bv = std::min(s->V, 128);
-    if (s->T <= 2 && s->V >= 128 && units >= 4LL * num_sms) out->variant = KDA_VARIANT_SMEM_STATE;
+    if (s->V >= 128 && ((s->T == 1 && units >= 4LL * num_sms) || (s->T == 2 && units >= 48LL * num_sms)))
+      out->variant = KDA_VARIANT_SMEM_STATE;
   }
   finish_plan(s, num_sms, out, 0, 0);
   return KDA_OK;

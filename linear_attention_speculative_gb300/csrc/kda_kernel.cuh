@@ -615,17 +615,16 @@ __device__ __forceinline__ void roll_qk(const Src& src, const Params& p, const I
   }
 }
 
-// Store the staged windows x_ext[T .. T+2] (produce_tasks' stash) as the new
-// conv_state: the item's v tile always, the q/k blocks of group (n, h) only
-// when `qk` (the group's last arrival).  Called after a barrier that follows
-// every conv_state read of the CTA.
+// Store the staged windows x_ext[T .. T+2] (produce_tasks' stash) of channel
+// vectors [cv0, cv1) as the new conv_state: the q/k blocks are vectors
+// [0, 2K/VEC), the item's v tile the rest.  Called after a barrier that
+// follows every conv_state read of the CTA.
 template <typename Act, int K, int BV>
 __device__ __forceinline__ void roll_staged(const Params& p, const Item& it, const uint4* stash,
-                                            bool qk, int tid, int nthr) {
+                                            int cv0, int cv1, int tid, int nthr) {
   constexpr int VEC = ActT<Act>::VEC;
   constexpr int NQ = K / VEC;
-  constexpr int NCV = 2 * NQ + BV / VEC;
-  for (int cv = (qk ? 0 : 2 * NQ) + tid; cv < NCV; cv += nthr) {
+  for (int cv = cv0 + tid; cv < cv1; cv += nthr) {
     const int kind = cv < NQ ? 0 : (cv < 2 * NQ ? 1 : 2);
     const int c = block_channel<K, BV>(p, it, kind) + (cv - kind * NQ) * VEC;
     char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
@@ -890,7 +889,6 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);
-  int* sflag = reinterpret_cast<int*>(smem + 8);
   float* sbuf = tile_base(smem);
   const int T = p.T;
   constexpr int KS = stage_ks(K);
@@ -924,14 +922,23 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   produce_tasks<Act, K, BV, DEC, SMS>(src, p, it, sQ, sK, sA, sV, sB, sRoll, tid, NT);
   __syncthreads();  // every conv_state read of this CTA is done, stage written
   for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
-  // the arrival's fence and atomic run in the last warp, after its own rows
-  // (none while 2T < WARPS), so they overlap the other warps' norms and the
-  // wait for the state tile
-  if (tid == (WARPS - 1) * 32) sflag[0] = arrive_qk_group(p, it) ? 1 : 0;
+  // Arrival on the q/k group counter by lane 0 of the last warp, after its
+  // own rows (none while 2T < WARPS).  The returned count is first used at
+  // the end of the CTA, so nothing waits here for the atomic's round trip.
+  constexpr int kRollWarp = WARPS - 1;
+  const int expected = p.G * p.nvt;
+  int* cnt = p.counters + (size_t)it.n * p.H + it.h;
+  int arrival = 0;
+  if (warp == kRollWarp && lane == 0 && expected > 1) {
+    __threadfence();  // the CTA's conv_state reads (before the barrier) come first
+    arrival = atomicAdd(cnt, 1);
+  }
   const bool ok = mbar_wait_bounded(mbar, 0, kWaitLimitNs);
   if (__syncthreads_or(!ok)) {
-    // give up without hanging: report, let the copy in flight land, leave
+    // give up without hanging: report, keep the counter protocol intact, let
+    // the copy in flight land, leave
     if (tid == 0) atomicOr(p.status, kStatusTmaTimeout);
+    if (warp == kRollWarp && lane == 0 && expected > 1 && arrival == expected - 1) atomicExch(cnt, 0);
     mbar_wait_bounded(mbar, 0, kWaitLimitNs);
     return;
   }
@@ -942,7 +949,21 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     load_tile<K, BV>(sbuf, s, warp, lane);
     consume<Act, K, BV, DEC>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
   }
-  roll_staged<Act, K, BV>(p, it, sRoll, sflag[0] != 0, tid, NT);
+  constexpr int NQV = 2 * K / ActT<Act>::VEC;  // q/k channel vectors
+  constexpr int NCV = NQV + BV / ActT<Act>::VEC;
+  roll_staged<Act, K, BV>(p, it, sRoll, NQV, NCV, tid, NT);  // v: owned by this item
+  if (warp == kRollWarp) {
+    // q/k: the group's last arrival resets the counter and rolls
+    const int last = __shfl_sync(0xffffffffu, expected == 1 || arrival == expected - 1 ? 1 : 0, 0);
+    if (last) {
+      if (lane == 0 && expected > 1) {
+        atomicExch(cnt, 0);
+        __threadfence();  // every other item's reads are ordered before the stores below
+      }
+      __syncwarp();
+      roll_staged<Act, K, BV>(p, it, sRoll, 0, NQV, lane, 32);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
