@@ -390,7 +390,8 @@ def run_ours(args, wl):
     plan = kda.make_plan(shape, torch.cuda.get_device_properties(dev).multi_processor_count,
                          args.variant)
     if args.plan:
-        plan = kda.parse_plan(args.plan)
+        plan = kda.resolve_plan(shape, torch.cuda.get_device_properties(dev).multi_processor_count,
+                                args.plan)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -399,6 +400,7 @@ def run_ours(args, wl):
                    "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
                    "variant": {1: "small_batch", 2: "large_batch", 3: "smem_state"}[plan.variant],
                    "v_tile": plan.bv, "plan": args.plan or "auto",
+                   "qk_roll": {1: "counter", 2: "kernel"}.get(plan.qk_roll, "counter"),
                    "l2": ("L2 flushed between steps (256 MB write)" if flush_l2 else
                           f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB moved per step"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
@@ -410,7 +412,7 @@ def run_ours(args, wl):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "steps": E,
                 "note": "pinned host buffers; two streams alternate steps so copies overlap"},
-        "gpu_launches": K,
+        "gpu_launches": K * max(1, plan.launches),
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:

@@ -84,7 +84,22 @@ typedef struct {
    * item this many items ahead (about one wave of resident CTAs).  In a plan
    * given to kda_conv_verify_plan: < 0 off, 0 the default, > 0 explicit. */
   int prefetch;
+  /* One-item-per-CTA variants, when G * (V / bv) > 1 items read the same q/k
+   * channels: who rolls their conv_state.  KDA_QK_ROLL_COUNTER: the last of
+   * those items to arrive on a counter in the workspace, inside the verify
+   * kernel (one launch).  KDA_QK_ROLL_KERNEL: a second, small kernel launched
+   * after the verify kernel on the same stream (no atomics in the verify
+   * kernel; faster on large launches).  In a plan given to
+   * kda_conv_verify_plan, KDA_QK_ROLL_AUTO (0) lets the dispatcher choose.
+   * The persistent variant always uses the counter. */
+  int qk_roll;
+  /* Kernels one call with this plan launches (1 or 2). */
+  int launches;
 } kda_plan;
+
+#define KDA_QK_ROLL_AUTO 0
+#define KDA_QK_ROLL_COUNTER 1
+#define KDA_QK_ROLL_KERNEL 2
 
 /* Error codes (negative: rejected on the host, nothing launched). */
 #define KDA_OK 0
@@ -263,6 +278,14 @@ size_t kda_workspace_bytes(const kda_shape* s);
  * Out: chosen variant, v-tile width bv (columns of V per CTA), warps per
  * CTA, grid size.  Returns 0 or a negative KDA_ERR_* code. */
 int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
+
+/* Fill the derived fields of a hand-written plan (variant, bv and the
+ * optional grid / prefetch / qk_roll requests set) exactly as
+ * kda_conv_verify_plan would before launching it: warps, grid, ctas_per_sm,
+ * items, prefetch, qk_roll, launches.  Host-only, no CUDA call.  `decode`
+ * non-zero checks the plan against kda_conv_decode's variants.  Returns 0 or
+ * KDA_ERR_SHAPE / KDA_ERR_VARIANT / KDA_ERR_NULL / KDA_ERR_DEVICE. */
+int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan);
 
 /* Same as kda_conv_verify with an explicit launch plan, e.g. one returned by
  * kda_make_plan and then edited.  Read from `plan`: variant (SMALL_BATCH or

@@ -42,6 +42,10 @@ int ctas_per_sm_for(int regs_limit, size_t smem) {
   return std::max(1, std::min(regs_limit, by_smem));
 }
 
+// Launches of at least this many waves of resident CTAs roll the shared q/k
+// conv_state with the second kernel instead of the counter.
+constexpr int kQkRollKernelWaves = 4;
+
 bool valid_tile_bv(int bv, int V) { return (bv == 16 || bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
 bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
 bool valid_sms_bv(int bv, int V) { return (bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
@@ -49,6 +53,7 @@ bool valid_sms_bv(int bv, int V) { return (bv == 64 || bv == 128) && bv <= V && 
 // A plan's tile width against its variant (decode: no persistent variant;
 // K = 256: only the shared-memory state fits).
 bool valid_plan(const kda_plan* plan, int K, int V, bool decode) {
+  if (plan->qk_roll < KDA_QK_ROLL_AUTO || plan->qk_roll > KDA_QK_ROLL_KERNEL) return false;
   switch (plan->variant) {
     case KDA_VARIANT_SMALL_BATCH: return K <= 128 && valid_tile_bv(plan->bv, V);
     case KDA_VARIANT_LARGE_BATCH: return K <= 128 && !decode && valid_ws_bv(plan->bv, V);
@@ -59,7 +64,7 @@ bool valid_plan(const kda_plan* plan, int K, int V, bool decode) {
 
 // Fill the derived fields of a plan whose variant and bv are set.
 void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_grid,
-                 int requested_prefetch) {
+                 int requested_prefetch, int requested_qk_roll) {
   const long long units = (long long)s->N * s->HV;
   const int ab = s->act == KDA_F32 ? 4 : 2;
   out->items = units * (s->V / out->bv);
@@ -82,6 +87,21 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
     const int dist = std::max(1, num_sms * out->ctas_per_sm * 3 / 8);
     out->prefetch = requested_prefetch < 0 ? 0 : (requested_prefetch > 0 ? requested_prefetch : dist);
   }
+  // q/k conv_state roll when several items share a group's q/k channels: the
+  // counter protocol costs the verify kernel a fence and an atomic round trip
+  // per item (measured on GB300: 6-14 % on launches of many waves), the second
+  // kernel a launch (~2-3 us, which dominates small launches)
+  const bool shared_qk = (long long)(s->HV / s->H) * (s->V / out->bv) > 1;
+  if (out->variant == KDA_VARIANT_LARGE_BATCH || !shared_qk) {
+    out->qk_roll = KDA_QK_ROLL_COUNTER;
+  } else if (requested_qk_roll != KDA_QK_ROLL_AUTO) {
+    out->qk_roll = requested_qk_roll;
+  } else {
+    out->qk_roll = out->items >= (long long)kQkRollKernelWaves * num_sms * out->ctas_per_sm
+                       ? KDA_QK_ROLL_KERNEL
+                       : KDA_QK_ROLL_COUNTER;
+  }
+  out->launches = (shared_qk && out->qk_roll == KDA_QK_ROLL_KERNEL) ? 2 : 1;
   if (units == 0) out->grid = 0;
 }
 
@@ -163,17 +183,26 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
   } else {
     // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
     // many threads for its producer tasks and the q/k conv is not repeated per
-    // v-tile.  Single-token calls over many units keep the state in shared
-    // memory instead (3 CTAs/SM instead of 2): measured on GB300 +5..11 % at
-    // T = 1.  At T = 2 the two are within a few per cent of each other, the
-    // shared-memory state ahead (+2 % on average) only from ~50 units per SM;
-    // from T = 3 on it is slower (two shared-memory passes per token).
+    // v-tile.  Calls of one or two tokens over many units keep the state in
+    // shared memory instead (3 CTAs/SM instead of 2): measured on GB300
+    // +9..17 % at T = 1 and +3..9 % at T = 2 from the unit counts below; from
+    // T = 3 on it is slower (two shared-memory passes per token).
     out->variant = KDA_VARIANT_SMALL_BATCH;
     out->bv = std::min(s->V, 128);
-    if (s->V >= 128 && ((s->T == 1 && units >= 4LL * num_sms) || (s->T == 2 && units >= 48LL * num_sms)))
+    if (s->V >= 128 && ((s->T == 1 && units >= 8LL * num_sms) || (s->T == 2 && units >= 16LL * num_sms)))
       out->variant = KDA_VARIANT_SMEM_STATE;
   }
-  finish_plan(s, num_sms, out, 0, 0);
+  finish_plan(s, num_sms, out, 0, 0, KDA_QK_ROLL_AUTO);
+  return KDA_OK;
+}
+
+int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan) {
+  int rc = check_shape(s);
+  if (rc) return rc;
+  if (!plan) return KDA_ERR_NULL;
+  if (num_sms < 1) return KDA_ERR_DEVICE;
+  if (!valid_plan(plan, s->K, s->V, decode != 0)) return KDA_ERR_VARIANT;
+  finish_plan(s, num_sms, plan, plan->grid, plan->prefetch, plan->qk_roll);
   return KDA_OK;
 }
 
@@ -322,6 +351,9 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.G = s->HV / s->H;
   p.nvt = s->V / plan.bv;
   p.gate_mode = gate_mode == KDA_GATE_SOFTPLUS ? 0 : 1;
+  const bool roll_kernel = plan.variant != KDA_VARIANT_LARGE_BATCH && plan.qk_roll == KDA_QK_ROLL_KERNEL &&
+                           p.G * p.nvt > 1;
+  p.qk_roll_kernel = roll_kernel ? 1 : 0;
 
   LaunchCfg cfg;
   cfg.K = s->K;
@@ -340,6 +372,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   else
     rc = cfg.ws ? kda::launch_ws_f32(tmap, p, cfg, st) : kda::launch_tile_f32(tmap, p, cfg, st);
   if (rc < 0) return KDA_ERR_SHAPE;
+  if (rc == 0 && roll_kernel) rc = kda::launch_qk_roll(p, s->K, s->act == KDA_BF16, st);
   return rc;
 }
 
@@ -394,7 +427,7 @@ int verify_with(const kda_shape* s, const Pools& pl, const void* mixed_qkv, cons
     if (rc) return rc;
   } else {
     p = *plan;
-    finish_plan(s, num_sms, &p, plan->grid, plan->prefetch);
+    finish_plan(s, num_sms, &p, plan->grid, plan->prefetch, plan->qk_roll);
   }
   return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode, o,
                      inter_ssm, conv_snapshots, workspace, p, pl, stream);
@@ -487,7 +520,7 @@ int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void
   kda_plan p;
   if (plan) {
     p = *plan;
-    finish_plan(s, num_sms, &p, plan->grid, plan->prefetch);
+    finish_plan(s, num_sms, &p, plan->grid, plan->prefetch, plan->qk_roll);
   } else {
     rc = kda_make_plan(s, num_sms, KDA_VARIANT_AUTO, &p);
     if (rc) return rc;

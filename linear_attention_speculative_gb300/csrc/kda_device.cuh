@@ -194,15 +194,29 @@ struct ActT<__nv_bfloat16> {
 // scalar math shared by every variant (same formula => bit-identical results)
 // ---------------------------------------------------------------------------
 
-__device__ __forceinline__ float silu_f(float y) { return __fdiv_rn(y, 1.0f + expf(-y)); }
+// The producer's activations sit on the critical path of every item, so they
+// use the hardware exponential / logarithm (__expf, __logf) and the
+// approximate divide: relative errors of a few 1e-7 up to ~1e-5 (exponent
+// magnitudes up to ~90), far inside the verify tolerance (2e-3), and
+// measured 1-4 % faster on whole calls than the IEEE-rounded forms.
+// Overflow is harmless: 1 + __expf(..) = inf makes the quotient 0.
 
-__device__ __forceinline__ float sigmoid_f(float x) { return __fdiv_rn(1.0f, 1.0f + expf(-x)); }
+__device__ __forceinline__ float silu_f(float y) { return __fdividef(y, 1.0f + __expf(-y)); }
 
-// softplus with threshold 20 as a real branch: expf is never evaluated where
-// it could overflow, so no 0 * inf can appear.
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
+
+// softplus with threshold 20 as a real branch: the exponential is never
+// evaluated where it could overflow, so no 0 * inf can appear.  Below the
+// threshold log(1 + e), e = exp(x): where e < 1e-3 the first two terms of the
+// series e - e^2/2 + e^3/3 - ... (relative truncation error < e^2/3 < 4e-7),
+// which keeps the tiny values that log(1 + e) rounds away; __logf elsewhere.
 __device__ __forceinline__ float softplus_f(float x) {
   if (x > 20.0f) return x;
-  return log1pf(expf(x));
+  const float e = __expf(x);
+  return e < 1e-3f ? __fmaf_rn(-0.5f * e, e, e) : __logf(1.0f + e);
 }
+
+// alpha = exp(g) of the gate (g <= 0)
+__device__ __forceinline__ float decay_f(float g) { return __expf(g); }
 
 }  // namespace kda

@@ -71,6 +71,9 @@ struct Params {
   int pool_state, pool_conv, pool_inter;
   int N, T, H, HV, V, dim, G, nvt;
   int gate_mode;          // 0 softplus, 1 safe
+  // one-item kernels with G * nvt > 1: 1 = the q/k conv_state is rolled by
+  // the separate roll kernel (no arrival counters), 0 = by the last arrival
+  int qk_roll_kernel;
 };
 
 constexpr int kConvW = 4;
@@ -466,12 +469,12 @@ __device__ __forceinline__ void gate_task(const Src& src, int gate_mode, float n
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float x = __fadd_rn(AT::to_f(r[e + j]), dd[j]);
-        al[e + j] = expf(__fmul_rn(negA, softplus_f(x)));
+        al[e + j] = decay_f(__fmul_rn(negA, softplus_f(x)));
       }
     }
   } else {
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) al[e] = expf(fminf(AT::to_f(r[e]), 0.0f));
+    for (int e = 0; e < VEC; ++e) al[e] = decay_f(fminf(AT::to_f(r[e]), 0.0f));
   }
 }
 
@@ -925,11 +928,13 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   // Arrival on the q/k group counter by lane 0 of the last warp, after its
   // own rows (none while 2T < WARPS).  The returned count is first used at
   // the end of the CTA, so nothing waits here for the atomic's round trip.
+  // With the separate roll kernel there is no arrival and no q/k roll here.
   constexpr int kRollWarp = WARPS - 1;
   const int expected = p.G * p.nvt;
+  const bool counted = expected > 1 && !p.qk_roll_kernel;
   int* cnt = p.counters + (size_t)it.n * p.H + it.h;
   int arrival = 0;
-  if (warp == kRollWarp && lane == 0 && expected > 1) {
+  if (warp == kRollWarp && lane == 0 && counted) {
     __threadfence();  // the CTA's conv_state reads (before the barrier) come first
     arrival = atomicAdd(cnt, 1);
   }
@@ -938,7 +943,7 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     // give up without hanging: report, keep the counter protocol intact, let
     // the copy in flight land, leave
     if (tid == 0) atomicOr(p.status, kStatusTmaTimeout);
-    if (warp == kRollWarp && lane == 0 && expected > 1 && arrival == expected - 1) atomicExch(cnt, 0);
+    if (warp == kRollWarp && lane == 0 && counted && arrival == expected - 1) atomicExch(cnt, 0);
     mbar_wait_bounded(mbar, 0, kWaitLimitNs);
     return;
   }
@@ -954,9 +959,9 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   roll_staged<Act, K, BV>(p, it, sRoll, NQV, NCV, tid, NT);  // v: owned by this item
   if (warp == kRollWarp) {
     // q/k: the group's last arrival resets the counter and rolls
-    const int last = __shfl_sync(0xffffffffu, expected == 1 || arrival == expected - 1 ? 1 : 0, 0);
+    const int last = __shfl_sync(0xffffffffu, expected == 1 || (counted && arrival == expected - 1) ? 1 : 0, 0);
     if (last) {
-      if (lane == 0 && expected > 1) {
+      if (lane == 0 && counted) {
         atomicExch(cnt, 0);
         __threadfence();  // every other item's reads are ordered before the stores below
       }

@@ -26,6 +26,9 @@ int launch_tile_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& 
 int launch_tile_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
 int launch_ws_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
 int launch_ws_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+// The q/k conv_state roll of a one-item-per-CTA launch run with
+// p.qk_roll_kernel set (kda_roll.cu), on the same stream after it.
+int launch_qk_roll(const Params& p, int K, bool bf16, cudaStream_t st);
 
 // Opt a kernel in to large dynamic shared memory once per device.
 template <typename Fn>

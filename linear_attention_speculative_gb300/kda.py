@@ -31,7 +31,7 @@ MAX_T = 16
 # The names declared in include/kda_verify.h.
 EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan",
             "kda_conv_verify_indexed", "kda_conv_decode", "kda_commit", "kda_commit_indexed",
-            "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan",
+            "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan", "kda_resolve_plan",
             "kda_read_status", "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
@@ -45,7 +45,8 @@ class KdaShape(ctypes.Structure):
 class KdaPlan(ctypes.Structure):
     _fields_ = [("variant", ctypes.c_int), ("bv", ctypes.c_int), ("warps", ctypes.c_int),
                 ("grid", ctypes.c_int), ("ctas_per_sm", ctypes.c_int),
-                ("items", ctypes.c_longlong), ("prefetch", ctypes.c_int)]
+                ("items", ctypes.c_longlong), ("prefetch", ctypes.c_int), ("qk_roll", ctypes.c_int),
+                ("launches", ctypes.c_int)]
 
 
 class KdaStateIndices(ctypes.Structure):
@@ -106,6 +107,8 @@ def _load():
     L.kda_workspace_bytes.argtypes = [sp]
     L.kda_make_plan.restype = ctypes.c_int
     L.kda_make_plan.argtypes = [sp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(KdaPlan)]
+    L.kda_resolve_plan.restype = ctypes.c_int
+    L.kda_resolve_plan.argtypes = [sp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(KdaPlan)]
     L.kda_read_status.restype = ctypes.c_int
     L.kda_read_status.argtypes = [sp, vp, ctypes.POINTER(ctypes.c_int), vp]
     L.kda_strerror.restype = ctypes.c_char_p
@@ -156,6 +159,16 @@ def make_plan(shape: KdaShape, num_sms: int, variant: str = "auto") -> KdaPlan:
     return plan
 
 
+def resolve_plan(shape: KdaShape, num_sms: int, plan, decode: bool = False) -> KdaPlan:
+    """A hand-written plan (KdaPlan or plan string) with its derived fields
+    filled in as the verify call would (launches, q/k roll, grid, ...)."""
+    p = parse_plan(plan) if isinstance(plan, str) else plan
+    rc = lib().kda_resolve_plan(ctypes.byref(shape), num_sms, int(decode), ctypes.byref(p))
+    if rc != 0:
+        raise KdaError(rc, "kda_resolve_plan")
+    return p
+
+
 def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
@@ -166,9 +179,13 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+QK_ROLL_AUTO, QK_ROLL_COUNTER, QK_ROLL_KERNEL = 0, 1, 2
+
+
 def parse_plan(spec: str) -> KdaPlan:
-    """'small:32' / 'large:64' / 'smem:128' / 'large:64:300' / 'small:128:0:-1' (variant,
-    v-tile width, grid, L2 prefetch distance: -1 off, 0 default)."""
+    """'small:32' / 'large:64' / 'smem:128' / 'large:64:300' / 'small:128:0:-1' /
+    'smem:128:0:0:kernel' (variant, v-tile width, grid, L2 prefetch distance: -1 off,
+    0 default, q/k conv_state roll: 'counter' or 'kernel', default the dispatcher's)."""
     parts = spec.split(":")
     plan = KdaPlan()
     plan.variant = {"small": VARIANT_SMALL_BATCH, "small_batch": VARIANT_SMALL_BATCH,
@@ -177,6 +194,8 @@ def parse_plan(spec: str) -> KdaPlan:
     plan.bv = int(parts[1])
     plan.grid = int(parts[2]) if len(parts) > 2 else 0
     plan.prefetch = int(parts[3]) if len(parts) > 3 else 0
+    plan.qk_roll = {"auto": QK_ROLL_AUTO, "counter": QK_ROLL_COUNTER,
+                    "kernel": QK_ROLL_KERNEL}[parts[4]] if len(parts) > 4 else QK_ROLL_AUTO
     return plan
 
 

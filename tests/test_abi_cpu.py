@@ -73,8 +73,42 @@ def test_plan_auto_uses_one_item_per_cta(kda):
     p3 = kda.make_plan(kda.make_shape(512, 3, 32, 64), 152)
     assert p3.variant == kda.VARIANT_SMALL_BATCH and p3.bv == 128
     assert kda.make_plan(kda.make_shape(2, 1, 16, 16), 152).variant == kda.VARIANT_SMALL_BATCH
+    assert kda.make_plan(kda.make_shape(32, 1, 16, 32), 152).variant == kda.VARIANT_SMALL_BATCH
     # L2 prefetch 3/8 of a wave of resident CTAs ahead
     assert p.prefetch == 152 * p.ctas_per_sm * 3 // 8 > 0
+
+
+def test_plan_picks_the_qk_roll(kda):
+    # one reader per q/k group: rolled inside the verify kernel, one launch
+    p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
+    assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
+    # two readers, many waves: the separate roll kernel
+    p = kda.make_plan(kda.make_shape(512, 1, 32, 64), 152)
+    assert p.qk_roll == kda.QK_ROLL_KERNEL and p.launches == 2
+    # two readers, a fraction of a wave: the counter, one launch
+    p = kda.make_plan(kda.make_shape(2, 1, 16, 32), 152)
+    assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
+    # the persistent variant always counts
+    p = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152, "large_batch")
+    assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
+
+
+def test_resolve_plan_fills_derived_fields(kda):
+    s = kda.make_shape(512, 1, 32, 64)
+    p = kda.resolve_plan(s, 152, "smem:128:0:0:counter")
+    assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1 and p.ctas_per_sm == 3
+    p = kda.resolve_plan(s, 152, "small:64")
+    assert p.qk_roll == kda.QK_ROLL_KERNEL and p.launches == 2 and p.items == 512 * 64 * 2
+    with pytest.raises(kda.KdaError):
+        kda.resolve_plan(s, 152, "large:64", decode=True)
+
+
+def test_plan_strings_carry_the_qk_roll(kda):
+    assert kda.parse_plan("small:64").qk_roll == kda.QK_ROLL_AUTO
+    assert kda.parse_plan("small:64:0:0:kernel").qk_roll == kda.QK_ROLL_KERNEL
+    assert kda.parse_plan("smem:128:0:-1:counter").qk_roll == kda.QK_ROLL_COUNTER
+    with pytest.raises(KeyError):
+        kda.parse_plan("small:64:0:0:sometimes")
     # fewer units than SMs: whole states per CTA
     p1 = kda.make_plan(kda.make_shape(1, 4, 16, 16), 152)
     assert p1.variant == kda.VARIANT_SMALL_BATCH and p1.bv == 128 and p1.warps == 8

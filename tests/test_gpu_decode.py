@@ -30,7 +30,8 @@ def _decode(kda, inp, gate, plan=None, idx=None):
     return o
 
 
-@pytest.mark.parametrize("plan", [None, "small:128", "small:32", "small:16:0:-1", "smem:128", "smem:64"])
+@pytest.mark.parametrize("plan", [None, "small:128", "small:32", "small:16:0:-1", "smem:128", "smem:64",
+                                  "small:32:0:0:kernel", "smem:64:0:0:kernel", "smem:128:0:0:counter"])
 @pytest.mark.parametrize("case", [(5, 4, 2, 4, 128, 128, "bf16", "softplus"),
                                   (3, 1, 2, 2, 128, 128, "bf16", "safe"),
                                   (4, 3, 1, 2, 64, 64, "f32", "softplus"),

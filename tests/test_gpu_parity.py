@@ -24,7 +24,10 @@ pytestmark = pytest.mark.gpu
 VARIANTS = ("auto", "small_batch", "large_batch")
 # every explicit plan of a V = 128 problem
 ALL_PLANS = ("small:16", "small:32", "small:64", "small:128", "small:128:0:-1", "small:64:0:7",
-             "large:32", "large:64", "large:128", "smem:64", "smem:128")
+             "large:32", "large:64", "large:128", "smem:64", "smem:128",
+             # both ways of rolling a q/k conv_state that several items read
+             "small:64:0:0:counter", "small:64:0:0:kernel", "smem:128:0:0:counter",
+             "smem:128:0:0:kernel", "smem:64:0:0:kernel")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -207,7 +210,8 @@ def test_workspace_is_left_zeroed():
     inp = to_device(wk.make_inputs(wl))
     shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
     ws = kda.alloc_workspace(shape, "cuda")
-    for v in ("small:16", "small:128", "large:32", "large:128"):
+    for v in ("small:16", "small:128", "large:32", "large:128", "small:128:0:0:counter",
+              "small:128:0:0:kernel"):
         kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate, plan=v, workspace=ws)
         torch.cuda.synchronize()
         assert int(ws.count_nonzero()) == 0

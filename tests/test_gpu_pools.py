@@ -64,7 +64,8 @@ def _run_indexed(kda, wl, inp, pl, plan=None):
                 idx=idx, slot=slot)
 
 
-@pytest.mark.parametrize("plan", [None, "small:128", "small:32", "large:64"])
+@pytest.mark.parametrize("plan", [None, "small:128", "small:32", "large:64", "small:128:0:0:kernel",
+                                  "small:32:0:0:counter", "smem:64:0:0:kernel"])
 def test_indexed_equals_dense_on_gathered_inputs(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(8, 3, 2, 4, 128, 128, seed=81)
@@ -111,13 +112,17 @@ def test_indexed_matches_the_oracle():
     assert_parity(out, cs, ref)
 
 
-def test_out_of_range_slot_skips_and_reports():
+@pytest.mark.parametrize("plan", [None, "small:128:0:0:counter", "small:128:0:0:kernel"])
+def test_out_of_range_slot_skips_and_reports(plan):
     from linear_attention_speculative_gb300 import kda
-    wl = wk.custom(4, 2, 2, 2, 128, 128, seed=83)
+    wl = wk.custom(4, 2, 2, 2, 128, 128, seed=83)  # two v-heads read each q/k head
     inp, live, pl = _pools(wl, seed=3, pad=())
     pl["slot_i"][2] = pl["PI"] + 7  # beyond the snapshot pool
-    got = _run_indexed(kda, wl, inp, pl)
+    got = _run_indexed(kda, wl, inp, pl, plan)
     assert bool((got["o"][2] == 5.0).all())
+    # the skipped sequence's conv_state slot is not rolled, by either q/k roll
+    c2 = int(pl["slot_c"][2])
+    assert torch.equal(got["cs_pool"][c2].cpu(), pl["cs_pool"][c2])
     assert kda.read_status(got["shape"], got["ws"]) == kda.STATUS_BAD_INDEX
 
 
