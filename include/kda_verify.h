@@ -250,13 +250,14 @@ int kda_commit_indexed(const kda_shape* s, const kda_state_indices* idx,
  * serving loop whose memory pool is fixed after start-up, code that must not
  * call cudaMalloc (it synchronises the device and can fail under a memory
  * cap).  Arguments are those of kda_conv_verify without the workspace: the
- * scratch (arrival counters) lives in a static device array of
+ * scratch (the status word and, on launches whose q/k conv_state is rolled
+ * by the counter, the arrival counters) lives in a static device array of
  * KDA_NOALLOC_MAX_SCRATCH_BYTES inside the library, held on every GPU that
  * loads the library until the process exits.  A shape whose
  * kda_workspace_bytes() exceeds that size is rejected with
  * KDA_ERR_SCRATCH_LIMIT (N*H up to 65532 fits).  The first call on a device,
  * with that device current, looks up the array's device address; make it
- * before any stream capture.  Each call clears the counters it needs on
+ * before any stream capture.  Each call clears the scratch it needs on
  * `stream`, then launches the same kernel as kda_conv_verify; it never
  * allocates or frees.  All calls share the one array: calls whose kernels
  * overlap on the GPU race and must be serialised by the caller. */
@@ -268,8 +269,9 @@ int kda_conv_verify_noalloc(const kda_shape* s, const void* mixed_qkv, const voi
                             void* conv_snapshots, kda_stream_t stream);
 
 /* Bytes of workspace a call with shape `s` needs (arrival counters for the
- * shared q/k conv_state write-back, N*H int32, plus a status word), rounded
- * up to 256.  Returns 0 for a NULL shape. */
+ * shared q/k conv_state write-back, N*H int32, used when the plan's qk_roll
+ * is the counter, plus a status word), rounded up to 256.  Returns 0 for a
+ * NULL shape. */
 size_t kda_workspace_bytes(const kda_shape* s);
 
 /* The launch plan the dispatcher picks; host-only, no CUDA call.

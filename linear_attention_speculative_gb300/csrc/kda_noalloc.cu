@@ -1,8 +1,8 @@
 // kda_noalloc.cu -- kda_conv_verify_noalloc: the verify decode for callers
 // that cannot allocate device memory.
 //
-// The regular entry point asks the caller for a workspace (the q/k arrival
-// counters and a status word).  Some callers have no way to provide one: a
+// The regular entry point asks the caller for a workspace (a status word and
+// the q/k arrival counters that small launches use).  Some callers have no way to provide one: a
 // plugin handed only its input and output buffers, a serving loop whose
 // memory pool is frozen after start-up, or code that must not call
 // cudaMalloc because it synchronises the device and can fail under a memory
@@ -13,13 +13,14 @@
 // Set-up: the first call on a device, with that device current, looks up the
 // array's device address with cudaGetSymbolAddress (the array's name in host
 // code is only a host-side stand-in, never a device address).  Make that
-// first call before any stream capture.  Each call then clears the counters
+// first call before any stream capture.  Each call then clears the scratch
 // it uses with cudaMemsetAsync on the caller's stream and launches the same
-// kernel as kda_conv_verify.  No call allocates or frees memory.
+// kernels as kda_conv_verify.  No call allocates or frees memory.
 //
 // Every call shares the one array: two calls whose kernels overlap on the GPU
 // (different streams, or different host threads on the same device) race on
-// the counters and give wrong conv_state write-backs.  Serialise them.
+// the counters and the status word and can give wrong conv_state write-backs.
+// Serialise them.
 #include <cuda_runtime.h>
 
 #include <mutex>

@@ -48,12 +48,18 @@ def test_rejects_shapes_beyond_the_built_in_scratch():
     assert "scratch" in kda.strerror(-10)
 
 
+# Four v-heads per q/k head in both.  The small launch rolls the shared q/k
+# conv_state with the arrival counters kept in the scratch array; the large one
+# uses the separate roll kernel, and the scratch holds only the status word.
+NOALLOC_CASES = [wk.custom(8, 4, 2, 8, 128, 128, gate="safe", seed=901), wk.GVA]
+
+
 @pytest.mark.gpu
-def test_noalloc_matches_the_regular_entry_point_on_two_calls_in_a_row():
+@pytest.mark.parametrize("wl", NOALLOC_CASES, ids=lambda w: w.name)
+def test_noalloc_matches_the_regular_entry_point_on_two_calls_in_a_row(wl):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     kda, L = _lib()
-    wl = wk.GVA  # four v-heads per q/k head: the arrival counters are used
     inp = to_device(wk.make_inputs(wl))
     shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
     assert kda.workspace_bytes(shape) <= kda.NOALLOC_MAX_SCRATCH_BYTES
