@@ -905,6 +905,9 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const long long item = blockIdx.x;
+  // a programmatic dependent launched after this grid (the q/k roll kernel)
+  // may be scheduled once every CTA has started; it waits for completion
+  asm volatile("griddepcontrol.launch_dependents;");
   if (item >= p.num_items) return;
   const Item it = decode_item(p, item);
   if (it.skip) {  // padding sequence: nothing to read or write

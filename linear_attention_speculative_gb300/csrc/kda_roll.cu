@@ -10,7 +10,11 @@
 //     conv_state[slot(n), c, j] <- x_ext_c[T + j],  j = 0..2,
 // for every q/k channel c, with x_ext_c = [conv_state[slot(n), c, :] ||
 // mixed_qkv[n, :, c]] as the verify kernel saw it.  Stream order is the only
-// synchronisation; the verify kernel needs no arrival counters for it.
+// synchronisation; the verify kernel needs no arrival counters for it.  The
+// launch is a programmatic dependent of the verify kernel: its CTAs may be
+// scheduled once every verify CTA has started, and each one first waits
+// (griddepcontrol.wait, a hardware dependency wait) until the verify grid has
+// completed and its writes are visible -- only the launch latency overlaps.
 //
 // One thread per 16-byte vector of channels (8 bf16 / 4 fp32): it reads the
 // vector's 3 old values per channel when T < 3 and the last min(T, 3) token
@@ -26,6 +30,7 @@ constexpr int kRollThreads = 256;
 
 template <typename Act>
 __global__ void __launch_bounds__(kRollThreads) kda_qk_roll_kernel(const Params p, int K) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the verify grid has completed
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
@@ -70,10 +75,19 @@ int launch_qk_roll(const Params& p, int K, bool bf16, cudaStream_t st) {
   if (threads == 0) return 0;
   const long long blocks = (threads + kRollThreads - 1) / kRollThreads;
   if (blocks > 0x7fffffffLL) return static_cast<int>(cudaErrorInvalidConfiguration);
-  if (bf16)
-    kda_qk_roll_kernel<__nv_bfloat16><<<(unsigned)blocks, kRollThreads, 0, st>>>(p, K);
-  else
-    kda_qk_roll_kernel<float><<<(unsigned)blocks, kRollThreads, 0, st>>>(p, K);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks);
+  cfg.blockDim = dim3(kRollThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = bf16 ? cudaLaunchKernelEx(&cfg, kda_qk_roll_kernel<__nv_bfloat16>, p, K)
+                             : cudaLaunchKernelEx(&cfg, kda_qk_roll_kernel<float>, p, K);
+  if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());
 }
 

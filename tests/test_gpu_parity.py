@@ -235,7 +235,10 @@ def test_side_streams_and_separate_workspaces():
         assert torch.equal(out["o"], ref["o"])
 
 
-def test_cuda_graph_replay():
+@pytest.mark.parametrize("plan", [None, "small:128:0:0:counter", "small:128:0:0:kernel"])
+def test_cuda_graph_replay(plan):
+    # two v-heads per q/k head: the q/k conv_state roll runs by either protocol
+    # (the roll kernel as a programmatic dependent launch inside the graph)
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(4, 3, 2, 4, 128, 128, seed=23)
     inp_cpu = wk.make_inputs(wl)
@@ -249,7 +252,7 @@ def test_cuda_graph_replay():
     def call():
         kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
                         inp["dt_bias"], inp["a"], inp["b"], inp["S0"], wl.gate, out["o"],
-                        out["inter_ssm"], out["conv_snapshots"], ws, shape=shape)
+                        out["inter_ssm"], out["conv_snapshots"], ws, shape=shape, plan=plan)
 
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
