@@ -508,7 +508,26 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
   const bool qk_snap_owner = !DEC && (it.hv % p.G == 0) && (it.vt == 0);
   constexpr bool v_snap = !DEC;  // decode writes no conv-window snapshots
   const float negA = p.gate_mode == 0 ? -expf(__ldg(p.A_log + it.hv)) : 0.0f;
-  for (int task = tid; task < n_conv + n_gate + T; task += nthr) {
+  // When the threads outnumber the tasks, conv, gate and beta tasks start on
+  // warp boundaries, so that no warp runs two of the three code paths one
+  // after the other: the producer's latency is the longest path, not a sum.
+  const int gate0 = (n_conv + 31) & ~31;
+  const int beta0 = gate0 + ((n_gate + 31) & ~31);
+  const bool spread = beta0 + T <= nthr;
+  const int n_slots = spread ? beta0 + T : n_conv + n_gate + T;
+  for (int slot = tid; slot < n_slots; slot += nthr) {
+    int task = slot;
+    if (spread) {
+      if (slot < n_conv) {
+        task = slot;
+      } else if (slot >= gate0 && slot < gate0 + n_gate) {
+        task = n_conv + (slot - gate0);
+      } else if (slot >= beta0) {
+        task = n_conv + n_gate + (slot - beta0);
+      } else {
+        continue;  // padding up to a warp boundary
+      }
+    }
     if (task < n_conv) {
       const int cv = task / T;
       const int t = task - cv * T;
