@@ -508,25 +508,18 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
   const bool qk_snap_owner = !DEC && (it.hv % p.G == 0) && (it.vt == 0);
   constexpr bool v_snap = !DEC;  // decode writes no conv-window snapshots
   const float negA = p.gate_mode == 0 ? -expf(__ldg(p.A_log + it.hv)) : 0.0f;
-  // When the threads outnumber the tasks, conv, gate and beta tasks start on
-  // warp boundaries, so that no warp runs two of the three code paths one
-  // after the other: the producer's latency is the longest path, not a sum.
+  // Beta of token t rides on the gate task of its first channel vector.  When
+  // the threads outnumber the tasks, the gate tasks start on a warp boundary,
+  // so that no warp runs the conv and the gate code paths one after the
+  // other: the producer's latency is the longer path, not the sum.
   const int gate0 = (n_conv + 31) & ~31;
-  const int beta0 = gate0 + ((n_gate + 31) & ~31);
-  const bool spread = beta0 + T <= nthr;
-  const int n_slots = spread ? beta0 + T : n_conv + n_gate + T;
+  const bool spread = gate0 + n_gate <= nthr;
+  const int n_slots = spread ? gate0 + n_gate : n_conv + n_gate;
   for (int slot = tid; slot < n_slots; slot += nthr) {
     int task = slot;
-    if (spread) {
-      if (slot < n_conv) {
-        task = slot;
-      } else if (slot >= gate0 && slot < gate0 + n_gate) {
-        task = n_conv + (slot - gate0);
-      } else if (slot >= beta0) {
-        task = n_conv + n_gate + (slot - beta0);
-      } else {
-        continue;  // padding up to a warp boundary
-      }
+    if (spread && slot >= n_conv) {
+      if (slot < gate0) continue;  // padding up to a warp boundary
+      task = n_conv + (slot - gate0);
     }
     if (task < n_conv) {
       const int cv = task / T;
@@ -550,17 +543,16 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
 #pragma unroll
         for (int e = 0; e < VEC; ++e) dst[stage_pos<K>(e0 + e)] = y[e];
       }
-    } else if (task < n_conv + n_gate) {
+    } else {
       const int g = task - n_conv;
       const int t = g / NQ;
       const int e0 = (g - t * NQ) * VEC;
+      const float braw = e0 == 0 ? load_b<Act>(p, it, t) : 0.0f;  // issued before the gate math
       float al[VEC];
       gate_task<Act>(src, p.gate_mode, negA, t, e0, al);
 #pragma unroll
       for (int e = 0; e < VEC; ++e) sA[t * KS + stage_pos<K>(e0 + e)] = al[e];
-    } else {
-      const int t = task - n_conv - n_gate;
-      sB[t] = sigmoid_f(load_b<Act>(p, it, t));
+      if (e0 == 0) sB[t] = sigmoid_f(braw);
     }
   }
 }
