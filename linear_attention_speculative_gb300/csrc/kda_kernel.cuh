@@ -33,10 +33,12 @@
 // Same floating-point operations in the same order => bit-identical outputs.
 //
 // Shared q/k conv_state write-back: the q/k channels of group (n, h) are read
-// by G * (V / BV) items.  Each item arrives on a per-group counter after its
-// reads; the last arrival rolls the group's q/k conv_state and resets the
-// counter to zero.  Nothing ever waits on another CTA.  v channels belong to
-// exactly one item, which rolls them itself.  In the one-item kernel, whose
+// by G * (V / BV) items.  With one reader it rolls them itself.  Otherwise
+// either a separate kernel launched after this one rolls them (kda_roll.cu;
+// Params::qk_roll_kernel), or each item arrives on a per-group counter after
+// its reads and the last arrival rolls the group's q/k conv_state and resets
+// the counter to zero.  Nothing ever waits on another CTA.  v channels belong
+// to exactly one item, which rolls them itself.  In the one-item kernel, whose
 // threads read conv_state straight from global memory, the producer stages the
 // new windows in shared memory and every roll is stored after the barrier
 // that ends the CTA's conv_state reads; the warp-specialised kernel reads its
