@@ -97,11 +97,17 @@ def measured_hbm_peak():
 
 
 def kernel_src_hash():
+    """Hash of the CUDA sources with comments and whitespace removed, so that a
+    comment-only edit keeps the committed ncu summaries valid."""
     d = os.path.join(ROOT, "linear_attention_speculative_gb300", "csrc")
     h = hashlib.sha256()
     for f in sorted(os.listdir(d)):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + b"\0" + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            code = fh.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        code = " ".join(code.split())
+        h.update(f.encode() + b"\0" + code.encode())
     return h.hexdigest()[:16]
 
 
