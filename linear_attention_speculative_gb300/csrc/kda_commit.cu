@@ -6,9 +6,12 @@
 // For each sequence n with 1 <= acc[n] <= T:
 //     S[n]          <- inter_ssm[n, acc[n]-1]        (fp32, HV x K x V)
 //     conv_state[n] <- conv_snapshots[n, acc[n]-1]   (act, dim x 3)
-// A pure HBM copy: one 16-byte streaming load and store per vector over a
-// flat, non-persistent grid.  Sequences whose count is out of range are left
-// untouched and reported in the status word.
+// A pure HBM copy of 16-byte vectors over a non-persistent grid: each CTA
+// copies one 16 KiB chunk of one sequence's state + conv window (the sequence
+// and chunk come from the block index, so no per-element division), every
+// thread issuing all four of its streaming loads before its four stores so
+// that 64 bytes per thread are in flight.  Sequences whose count is out of
+// range are left untouched and reported in the status word.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -35,43 +38,46 @@ struct CommitParams {
   int* status;
   long long state_vecs;  // 16-byte vectors of one sequence's state (HV*K*V/4)
   long long conv_vecs;   // 16-byte vectors of one sequence's conv window
-  long long total;       // N * (state_vecs + conv_vecs)
+  int chunks;            // CTAs per sequence: ceil((state_vecs + conv_vecs) / kCommitChunk)
   int T;
 };
 
+constexpr int kCommitChunk = kCommitThreads * kCommitUnroll;  // vectors per CTA
+
 __global__ void __launch_bounds__(kCommitThreads) kda_commit_kernel(const CommitParams p) {
+  const long long n = blockIdx.x / p.chunks;
+  const long long r0 = (long long)(blockIdx.x - n * p.chunks) * kCommitChunk + threadIdx.x;
+  const long long ss = p.idx_state ? __ldg(p.idx_state + n) : n;
+  const long long sc = p.idx_conv ? __ldg(p.idx_conv + n) : n;
+  const long long si = p.idx_inter ? __ldg(p.idx_inter + n) : n;
+  if (ss < 0 || sc < 0 || si < 0) return;  // padding sequence
+  const bool first = r0 == 0;               // one report per sequence
+  if (ss >= p.pool_state || sc >= p.pool_conv || si >= p.pool_inter) {
+    if (first && p.status) atomicOr(p.status, KDA_STATUS_BAD_INDEX);
+    return;
+  }
+  const int a = __ldg(p.acc + n);
+  if (a < 1 || a > p.T) {
+    if (first && p.status) atomicOr(p.status, KDA_STATUS_BAD_ACCEPT);
+    return;
+  }
   const long long per_seq = p.state_vecs + p.conv_vecs;
-  const long long base = (long long)blockIdx.x * kCommitThreads * kCommitUnroll + threadIdx.x;
+  const uint4* ssrc = reinterpret_cast<const uint4*>(p.inter_ssm) + (si * p.T + (a - 1)) * p.state_vecs;
+  uint4* sdst = reinterpret_cast<uint4*>(p.S) + ss * p.state_vecs;
+  const uint4* csrc = reinterpret_cast<const uint4*>(p.snaps) + (si * p.T + (a - 1)) * p.conv_vecs;
+  uint4* cdst = reinterpret_cast<uint4*>(p.conv_state) + sc * p.conv_vecs;
+  uint4 v[kCommitUnroll] = {};
 #pragma unroll
   for (int u = 0; u < kCommitUnroll; ++u) {
-    const long long v = base + (long long)u * kCommitThreads;
-    if (v >= p.total) return;
-    const long long n = v / per_seq;
-    const long long r = v - n * per_seq;
-    const long long ss = p.idx_state ? __ldg(p.idx_state + n) : n;
-    const long long sc = p.idx_conv ? __ldg(p.idx_conv + n) : n;
-    const long long si = p.idx_inter ? __ldg(p.idx_inter + n) : n;
-    if (ss < 0 || sc < 0 || si < 0) continue;  // padding sequence
-    if (ss >= p.pool_state || sc >= p.pool_conv || si >= p.pool_inter) {
-      if (r == 0 && p.status) atomicOr(p.status, KDA_STATUS_BAD_INDEX);
-      continue;
-    }
-    const int a = __ldg(p.acc + n);
-    if (a < 1 || a > p.T) {
-      if (r == 0 && p.status) atomicOr(p.status, KDA_STATUS_BAD_ACCEPT);
-      continue;
-    }
-    if (r < p.state_vecs) {
-      const float4* src = reinterpret_cast<const float4*>(p.inter_ssm) +
-                          ((si * p.T + (a - 1)) * p.state_vecs + r);
-      float4* dst = reinterpret_cast<float4*>(p.S) + (ss * p.state_vecs + r);
-      __stcs(dst, __ldcs(src));
-    } else {
-      const long long c = r - p.state_vecs;
-      const uint4* src = reinterpret_cast<const uint4*>(p.snaps) + ((si * p.T + (a - 1)) * p.conv_vecs + c);
-      uint4* dst = reinterpret_cast<uint4*>(p.conv_state) + (sc * p.conv_vecs + c);
-      __stcs(dst, __ldcs(src));
-    }
+    const long long r = r0 + (long long)u * kCommitThreads;
+    if (r < p.state_vecs) v[u] = __ldcs(ssrc + r);
+    else if (r < per_seq) v[u] = __ldcs(csrc + (r - p.state_vecs));
+  }
+#pragma unroll
+  for (int u = 0; u < kCommitUnroll; ++u) {
+    const long long r = r0 + (long long)u * kCommitThreads;
+    if (r < p.state_vecs) __stcs(sdst + r, v[u]);
+    else if (r < per_seq) __stcs(cdst + (r - p.state_vecs), v[u]);
   }
 }
 
@@ -139,11 +145,11 @@ extern "C" int kda_commit_indexed(const kda_shape* s, const kda_state_indices* i
   p.status = status;
   p.state_vecs = (long long)(HV * K * V / 4);
   p.conv_vecs = (long long)(dim * 3 * ab / 16);
-  p.total = (long long)N * (p.state_vecs + p.conv_vecs);
+  const long long chunks = (p.state_vecs + p.conv_vecs + kCommitChunk - 1) / kCommitChunk;
   p.T = s->T;
-  const long long per_block = (long long)kCommitThreads * kCommitUnroll;
-  const long long blocks = (p.total + per_block - 1) / per_block;
-  if (blocks > 0x7fffffffLL) return KDA_ERR_SHAPE;
+  const long long blocks = (long long)N * chunks;
+  if (chunks > 0x7fffffffLL || blocks > 0x7fffffffLL) return KDA_ERR_SHAPE;
+  p.chunks = (int)chunks;
   kda_commit_kernel<<<(unsigned)blocks, kCommitThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
   return static_cast<int>(cudaGetLastError());
 }
