@@ -210,9 +210,16 @@ def cpu_baseline(wl, inputs_cpu, cpu_seconds=12.0):
         dt += time.perf_counter() - t0
         passes += 1
     hs = passes * s.head_steps
+    # the same oracle on one core: the first min(N, 4) sequences, one pass
+    n1 = min(s.N, 4)
+    t0 = time.perf_counter()
+    oracle.verify(sub, wl.gate, seqs=list(range(n1)), threads=1)
+    dt1 = time.perf_counter() - t0
     return {"value": hs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "single_core_value": n1 * s.T * s.HV / dt1,
             "sample": f"{passes} full pass(es) over the {s.N} sequences of {wl.name} ({hs} head-steps), "
-                      f"fp64 C oracle, {cores} threads, {dt:.2f} s wall (~{dt * cores:.0f} s CPU)"}
+                      f"fp64 C oracle, {cores} threads, {dt:.2f} s wall (~{dt * cores:.0f} s CPU); "
+                      f"single_core_value: {n1} sequences on one thread"}
 
 
 def run_reference(args, wl):
