@@ -96,12 +96,23 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_src_hash():
-    """Hash of the CUDA sources with comments and whitespace removed, so that a
-    comment-only edit keeps the committed ncu summaries valid."""
+# CUDA sources each profiled kernel is built from (the verify kernels: every
+# source but the commit kernel's own file)
+COMMIT_SOURCES = ("kda_commit.cu", "kda_device.cuh")
+
+
+def kernel_src_hash(kernel="verify"):
+    """Hash of the CUDA sources of `kernel` ("verify" or "commit") with comments
+    and whitespace removed, so that a comment-only edit, or a change to another
+    kernel's file, keeps the committed ncu summaries valid."""
     d = os.path.join(ROOT, "linear_attention_speculative_gb300", "csrc")
+    names = sorted(os.listdir(d))
+    if kernel == "commit":
+        names = [f for f in names if f in COMMIT_SOURCES]
+    else:
+        names = [f for f in names if f != COMMIT_SOURCES[0]]
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
+    for f in names:
         with open(os.path.join(d, f), encoding="utf-8") as fh:
             code = fh.read()
         code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)

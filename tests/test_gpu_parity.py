@@ -373,3 +373,37 @@ def test_random_shapes_and_plans(case):
     for key in ("o", "inter_ssm", "conv_snapshots"):
         assert torch.equal(out[key], auto[key]), key
     assert torch.equal(cs, auto_cs)
+
+
+ROLL_CASES = [
+    # N, T, H, HV, K, V, act, gate: several items read each q/k group; T < 3
+    # makes the roll kernel read the old conv_state, T >= 3 only tokens
+    (4, 1, 2, 4, 128, 128, "bf16", "softplus"),
+    (3, 2, 2, 8, 64, 128, "bf16", "safe"),
+    (2, 3, 1, 2, 128, 64, "f32", "softplus"),
+    (3, 5, 2, 4, 32, 32, "bf16", "softplus"),
+    (2, 1, 1, 2, 256, 128, "bf16", "safe"),
+]
+
+
+@pytest.mark.parametrize("case", ROLL_CASES, ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}".format(*c))
+def test_qk_roll_kernel_and_counter_match_the_oracle(case):
+    N, T, H, HV, K, V, act, gate = case
+    wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=700 + T + K)
+    inp = wk.make_inputs(wl)
+    ref = oracle.verify(inp, gate)
+    kinds = ("smem",) if K == 256 else (("small", "smem") if V >= 64 else ("small",))
+    outs = []
+    for kind in kinds:
+        bv = min(V, 128)
+        for roll in ("counter", "kernel"):
+            plan = f"{kind}:{bv}:0:0:{roll}"
+            out, cs = run_kernel(inp, gate, plan)
+            assert_parity(out, cs, ref)
+            outs.append((plan, out, cs))
+    # every plan and roll gives the same bits
+    _, o0, c0 = outs[0]
+    for plan, o, c in outs[1:]:
+        assert torch.equal(c, c0), plan
+        for key in ("o", "inter_ssm", "conv_snapshots"):
+            assert torch.equal(o[key], o0[key]), (plan, key)
