@@ -183,14 +183,15 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
   } else {
     // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
     // many threads for its producer tasks and the q/k conv is not repeated per
-    // v-tile.  Calls of one or two tokens over many units keep the state in
+    // v-tile.  Calls of up to three tokens over many units keep the state in
     // shared memory instead (3 CTAs/SM instead of 2): measured on GB300
-    // +9..17 % at T = 1 and +3..9 % at T = 2 from the unit counts below; from
-    // T = 3 on it is slower (two shared-memory passes per token).
+    // +9..17 % at T = 1, +3..6 % at T = 2 and +2..4 % at T = 3 from the unit
+    // counts below (per SM: 8, 12, 24); from T = 4 on it is slower (two
+    // shared-memory passes per token).
     out->variant = KDA_VARIANT_SMALL_BATCH;
     out->bv = std::min(s->V, 128);
-    if (s->V >= 128 && ((s->T == 1 && units >= 8LL * num_sms) || (s->T == 2 && units >= 16LL * num_sms)))
-      out->variant = KDA_VARIANT_SMEM_STATE;
+    const long long sms_from = s->T == 1 ? 8 : (s->T == 2 ? 12 : (s->T == 3 ? 24 : 0));
+    if (s->V >= 128 && sms_from > 0 && units >= sms_from * num_sms) out->variant = KDA_VARIANT_SMEM_STATE;
   }
   finish_plan(s, num_sms, out, 0, 0, KDA_QK_ROLL_AUTO);
   return KDA_OK;

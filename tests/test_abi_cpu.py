@@ -69,8 +69,11 @@ def test_plan_auto_uses_one_item_per_cta(kda):
     assert p2.variant == kda.VARIANT_SMEM_STATE and p2.bv == 128 and p2.items == 512 * 64
     assert p2.ctas_per_sm == 3
     assert kda.make_plan(kda.make_shape(512, 2, 32, 64), 152).variant == kda.VARIANT_SMEM_STATE
-    assert kda.make_plan(kda.make_shape(32, 2, 32, 64), 152).variant == kda.VARIANT_SMALL_BATCH
-    p3 = kda.make_plan(kda.make_shape(512, 3, 32, 64), 152)
+    assert kda.make_plan(kda.make_shape(32, 2, 32, 64), 152).variant == kda.VARIANT_SMEM_STATE
+    assert kda.make_plan(kda.make_shape(32, 2, 16, 32), 152).variant == kda.VARIANT_SMALL_BATCH
+    assert kda.make_plan(kda.make_shape(512, 3, 32, 64), 152).variant == kda.VARIANT_SMEM_STATE
+    assert kda.make_plan(kda.make_shape(128, 3, 16, 16), 152).variant == kda.VARIANT_SMALL_BATCH
+    p3 = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152)
     assert p3.variant == kda.VARIANT_SMALL_BATCH and p3.bv == 128
     assert kda.make_plan(kda.make_shape(2, 1, 16, 16), 152).variant == kda.VARIANT_SMALL_BATCH
     assert kda.make_plan(kda.make_shape(32, 1, 16, 32), 152).variant == kda.VARIANT_SMALL_BATCH
