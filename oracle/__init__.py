@@ -48,11 +48,17 @@ def build(force: bool = False) -> str:
 
 
 def lib():
+    """The compiled oracle.  KDA_ORACLE_LIB, when set, names another build of
+    kda_oracle.c to load instead (the mutation tests plant mistakes in copies
+    of the source and check that the pins catch them)."""
     global _lib
     with _lock:
         if _lib is None:
-            build()
-            L = ctypes.CDLL(_LIB_PATH)
+            path = os.environ.get("KDA_ORACLE_LIB")
+            if not path:
+                build()
+                path = _LIB_PATH
+            L = ctypes.CDLL(path)
             for name in ("orc_silu", "orc_sigmoid", "orc_softplus", "orc_gate_safe"):
                 f = getattr(L, name)
                 f.restype = ctypes.c_double
