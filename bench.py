@@ -78,9 +78,17 @@ def dist_env():
 
 
 def workload(name):
+    """A named workload, a sweep point, or 'custom:N,T,H,HV,K,V[,act[,gate]]'
+    (decode distributions, seed 0)."""
     from linear_attention_speculative_gb300 import workloads as wk
     if name in wk.WORKLOADS:
         return wk.WORKLOADS[name]
+    if name.startswith("custom:"):
+        f = name[len("custom:"):].split(",")
+        nums = [int(x) for x in f[:6]]
+        act = f[6] if len(f) > 6 else "bf16"
+        gate = f[7] if len(f) > 7 else "softplus"
+        return wk.custom(*nums, act=act, gate=gate)
     for w in wk.sweep():
         if w.name == name:
             return w
