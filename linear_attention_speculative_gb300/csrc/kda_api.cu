@@ -46,18 +46,28 @@ int ctas_per_sm_for(int regs_limit, size_t smem) {
 // conv_state with the second kernel instead of the counter.
 constexpr int kQkRollKernelWaves = 4;
 
-bool valid_tile_bv(int bv, int V) { return (bv == 16 || bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
-bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
-bool valid_sms_bv(int bv, int V) { return (bv == 64 || bv == 128) && bv <= V && V % bv == 0; }
+// v-tile widths of the one-item kernels: 1, 2, 4 or 8 warps of warp_cols(K)
+// columns each (16 columns for K <= 128, 8 for K = 256); the shared-memory
+// state variant runs 4 or 8 warps.
+bool fits_v(int bv, int V) { return bv <= V && V % bv == 0; }
+bool valid_tile_bv(int bv, int K, int V) {
+  const int wc = kda::warp_cols(K);
+  return (bv == 2 * wc || bv == 4 * wc || bv == 8 * wc || (K <= 128 && bv == wc)) && fits_v(bv, V);
+}
+bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && fits_v(bv, V); }
+bool valid_sms_bv(int bv, int K, int V) {
+  const int wc = kda::warp_cols(K);
+  return (bv == 4 * wc || bv == 8 * wc) && fits_v(bv, V);
+}
 
 // A plan's tile width against its variant (decode: no persistent variant;
-// K = 256: only the shared-memory state fits).
+// the persistent variant is built for K <= 128).
 bool valid_plan(const kda_plan* plan, int K, int V, bool decode) {
   if (plan->qk_roll < KDA_QK_ROLL_AUTO || plan->qk_roll > KDA_QK_ROLL_KERNEL) return false;
   switch (plan->variant) {
-    case KDA_VARIANT_SMALL_BATCH: return K <= 128 && valid_tile_bv(plan->bv, V);
+    case KDA_VARIANT_SMALL_BATCH: return valid_tile_bv(plan->bv, K, V);
     case KDA_VARIANT_LARGE_BATCH: return K <= 128 && !decode && valid_ws_bv(plan->bv, V);
-    case KDA_VARIANT_SMEM_STATE: return valid_sms_bv(plan->bv, V);
+    case KDA_VARIANT_SMEM_STATE: return valid_sms_bv(plan->bv, K, V);
     default: return false;
   }
 }
@@ -69,14 +79,14 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
   const int ab = s->act == KDA_F32 ? 4 : 2;
   out->items = units * (s->V / out->bv);
   if (out->variant == KDA_VARIANT_LARGE_BATCH) {
-    out->warps = out->bv / 16;
+    out->warps = out->bv / kda::warp_cols(s->K);
     const size_t smem = kda::ws_smem_bytes(s->T, s->K, out->bv, ab);
     out->ctas_per_sm = ctas_per_sm_for(kda::ws_min_blocks(out->warps), smem);
     const long long cap = (long long)num_sms * out->ctas_per_sm;
     long long grid = requested_grid > 0 ? requested_grid : cap;
     out->grid = (int)std::max(1LL, std::min(out->items, grid));
   } else {
-    out->warps = out->bv / 16;
+    out->warps = out->bv / kda::warp_cols(s->K);
     const size_t smem = kda::tile_smem_bytes(s->T, s->K, out->bv, ab);
     const bool sms = out->variant == KDA_VARIANT_SMEM_STATE;
     out->ctas_per_sm = ctas_per_sm_for(kda::tile_min_blocks(out->warps, sms), smem);
@@ -167,31 +177,30 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
     return KDA_ERR_VARIANT;
   const long long units = (long long)s->N * s->HV;
   std::memset(out, 0, sizeof(*out));
-  if (s->K == 256) {
-    // 256 rows do not fit the register layout: state in shared memory, 64-wide tiles
-    if (variant == KDA_VARIANT_SMALL_BATCH || variant == KDA_VARIANT_LARGE_BATCH) return KDA_ERR_VARIANT;
-    if (s->V < 64) return KDA_ERR_VARIANT;
-    out->variant = KDA_VARIANT_SMEM_STATE;
-    out->bv = 64;
-  } else if (variant == KDA_VARIANT_LARGE_BATCH) {
+  // widest one-item tile: 8 warps (128 columns for K <= 128, 64 for K = 256)
+  const int full_bv = std::min(s->V, 8 * kda::warp_cols(s->K));
+  if (variant == KDA_VARIANT_LARGE_BATCH) {
+    if (s->K > 128) return KDA_ERR_VARIANT;
     out->variant = KDA_VARIANT_LARGE_BATCH;
     out->bv = s->V >= 64 ? 64 : s->V;
   } else if (variant == KDA_VARIANT_SMEM_STATE) {
-    if (s->V < 64) return KDA_ERR_VARIANT;
+    if (s->V < 4 * kda::warp_cols(s->K)) return KDA_ERR_VARIANT;
     out->variant = KDA_VARIANT_SMEM_STATE;
-    out->bv = std::min(s->V, 128);
+    out->bv = full_bv;
   } else {
-    // One item per CTA.  Whole states (BV = V) per 8-warp CTA: every CTA has
-    // many threads for its producer tasks and the q/k conv is not repeated per
-    // v-tile.  Calls of up to three tokens over many units keep the state in
-    // shared memory instead (3 CTAs/SM instead of 2): measured on GB300
-    // +9..17 % at T = 1, +3..6 % at T = 2 and +2..4 % at T = 3 from the unit
-    // counts below (per SM: 8, 12, 24); from T = 4 on it is slower (two
-    // shared-memory passes per token).
+    // One item per CTA.  Whole states (up to 8 warps' columns) per CTA: every
+    // CTA has many threads for its producer tasks and the q/k conv is not
+    // repeated per v-tile.  Calls of up to three tokens over many units keep
+    // the state in shared memory instead (3 CTAs/SM instead of 2): measured on
+    // GB300 +9..17 % at T = 1, +3..6 % at T = 2 and +2..4 % at T = 3 from the
+    // unit counts below (per SM: 8, 12, 24); from T = 4 on it is slower (two
+    // shared-memory passes per token).  K = 256 (16 rows x 4 columns per
+    // thread either way) measured faster on the register state at every T.
     out->variant = KDA_VARIANT_SMALL_BATCH;
-    out->bv = std::min(s->V, 128);
+    out->bv = full_bv;
     const long long sms_from = s->T == 1 ? 8 : (s->T == 2 ? 12 : (s->T == 3 ? 24 : 0));
-    if (s->V >= 128 && sms_from > 0 && units >= sms_from * num_sms) out->variant = KDA_VARIANT_SMEM_STATE;
+    if (s->K <= 128 && full_bv == 128 && sms_from > 0 && units >= sms_from * num_sms)
+      out->variant = KDA_VARIANT_SMEM_STATE;
   }
   finish_plan(s, num_sms, out, 0, 0, KDA_QK_ROLL_AUTO);
   return KDA_OK;

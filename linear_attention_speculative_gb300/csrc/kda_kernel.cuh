@@ -87,13 +87,23 @@ constexpr int kStatusBadIndex = 4;                // KDA_STATUS_BAD_INDEX
 __host__ __device__ constexpr int round4(int x) { return (x + 3) & ~3; }
 __host__ __device__ constexpr size_t round16(size_t x) { return (x + 15) & ~size_t(15); }
 
-// A staged K-vector (q, k or alpha of one token) is held as eight row-group
-// blocks of K/8 values (see stage_pos).  Blocks are stage_rs(K) floats apart:
-// K/8 rounded so that stride/4 is odd, which starts the eight blocks in eight
-// different 4-bank groups, so the consumers' 16-byte reads of them (one block
-// per row group) are conflict-free.
-__host__ __device__ constexpr int stage_rs(int K) { return K / 8 + (((K / 32) & 1) ? 0 : 4); }
-__host__ __device__ constexpr int stage_ks(int K) { return 8 * stage_rs(K); }
+// Consumer layout: a warp is RG row groups x CQ = 32 / RG column quads.
+// K <= 128 uses RG = 8 (16 columns per warp, K/8 rows per thread); K = 256
+// uses RG = 16 (8 columns per warp, 16 rows per thread), so a thread never
+// holds more than 16 x 4 fp32 state values (64 registers).
+__host__ __device__ constexpr int row_groups(int K) { return K > 128 ? 16 : 8; }
+__host__ __device__ constexpr int warp_cols(int K) { return 4 * (32 / row_groups(K)); }
+__host__ __device__ constexpr int rows_per_thread(int K) { return K / row_groups(K); }
+
+// A staged K-vector (q, k or alpha of one token) is held as RG row-group
+// blocks of K/RG values (see stage_pos).  Blocks are stage_rs(K) floats apart:
+// K/RG rounded so that stride/4 is odd, which spreads the blocks evenly over
+// the eight 16-byte bank groups, so the consumers' 16-byte reads of them (one
+// block per row group) take the fewest shared-memory wavefronts.
+__host__ __device__ constexpr int stage_rs(int K) {
+  return rows_per_thread(K) + (((rows_per_thread(K) / 4) & 1) ? 0 : 4);
+}
+__host__ __device__ constexpr int stage_ks(int K) { return row_groups(K) * stage_rs(K); }
 
 // floats of one stage: q[T][KS], k[T][KS], alpha[T][KS], v[T][BV],
 // beta[round4(T)] with KS = stage_ks(K)
@@ -133,19 +143,36 @@ __host__ __device__ constexpr size_t ws_smem_bytes(int T, int K, int BV, int ab)
 // ---------------------------------------------------------------------------
 // state-tile layout and row ownership
 // ---------------------------------------------------------------------------
-// Consumer thread (row group rg, column quad cg) owns rows 8 i + row_perm(rg),
-// i < K/8, with row_perm = 0 4 1 5 2 6 3 7: the two row groups that share a
-// shared-memory phase read rows four apart, which the 128-byte swizzle places
-// in opposite halves of the banks, so tile reads are conflict-free.  q, k and
-// alpha are staged in the matching order (stage_pos), so a thread's K/8 values
-// sit next to each other.
-__device__ __forceinline__ int row_perm(int rg) { return (rg >> 1) + 4 * (rg & 1); }
-__device__ __forceinline__ int own_row(int rg, int i) { return 8 * i + row_perm(rg); }
+// Consumer thread (row group rg, column quad cg) owns rows RG i + row_perm(rg),
+// i < K/RG.  RG = 8: row_perm = 0 4 1 5 2 6 3 7, so the two row groups that
+// share a shared-memory phase (8 lanes) read rows four apart, which the
+// 128-byte swizzle places in opposite halves of the banks.  RG = 16:
+// row_perm(8h + 4b + j) = 8h + 2j + b, so the four row groups of a phase read
+// rows whose (row mod 8) are b, b+2, b+4, b+6, four distinct swizzle offsets
+// for each of the phase's two column quads.  Either way tile reads are
+// conflict-free.  q, k and alpha are staged in the matching order
+// (stage_pos), so a thread's K/RG values sit next to each other.
+template <int K>
+__device__ __forceinline__ int row_perm(int rg) {
+  if constexpr (row_groups(K) == 8) {
+    return (rg >> 1) + 4 * (rg & 1);
+  } else {
+    return ((rg >> 2) & 1) + 2 * (rg & 3) + 8 * (rg >> 3);
+  }
+}
+template <int K>
+__device__ __forceinline__ int own_row(int rg, int i) { return row_groups(K) * i + row_perm<K>(rg); }
 template <int K>
 __device__ __forceinline__ int stage_pos(int k) {
-  const int m = k & 7;
-  const int g = m < 4 ? 2 * m : 2 * (m - 4) + 1;  // the row group that owns row k
-  return g * stage_rs(K) + (k >> 3);
+  constexpr int RG = row_groups(K);
+  const int m = k % RG;
+  int g;  // the row group that owns row k (inverse of row_perm)
+  if constexpr (RG == 8) {
+    g = m < 4 ? 2 * m : 2 * (m - 4) + 1;
+  } else {
+    g = 8 * (m >> 3) + 4 * (m & 1) + ((m >> 1) & 3);
+  }
+  return g * stage_rs(K) + k / RG;
 }
 
 // The tile as TMA leaves it: for BV >= 32, 32-column boxes of K rows x 128
@@ -654,25 +681,29 @@ __device__ __forceinline__ void roll_staged(const Params& p, const Item& it, con
 // consumer: the recurrence on register-resident S
 // ---------------------------------------------------------------------------
 template <int K, int BV>
-__device__ __forceinline__ void load_tile(const float* sbuf, float4 (&s)[K / 8], int warp, int lane) {
-  constexpr int R = K / 8;
-  const int rg = lane >> 2, cg = lane & 3;
-  const int col = warp * 16 + cg * 4;
+__device__ __forceinline__ void load_tile(const float* sbuf, float4 (&s)[rows_per_thread(K)], int warp,
+                                          int lane) {
+  constexpr int R = rows_per_thread(K);
+  constexpr int CQ = 32 / row_groups(K);
+  const int rg = lane / CQ, cg = lane % CQ;
+  const int col = warp * warp_cols(K) + cg * 4;
 #pragma unroll
   for (int i = 0; i < R; ++i)
-    s[i] = *reinterpret_cast<const float4*>(sbuf + tile_index<K, BV>(own_row(rg, i), col));
+    s[i] = *reinterpret_cast<const float4*>(sbuf + tile_index<K, BV>(own_row<K>(rg, i), col));
 }
 
 template <typename Act, int K, int BV, bool DEC = false>
 __device__ __forceinline__ void consume(const Params& p, const Item& it, const float* sQ,
                                        const float* sK, const float* sA, const float* sV,
-                                       const float* sB, float4 (&s)[K / 8], int warp, int lane) {
-  constexpr int R = K / 8;
+                                       const float* sB, float4 (&s)[rows_per_thread(K)], int warp,
+                                       int lane) {
+  constexpr int R = rows_per_thread(K);
+  constexpr int CQ = 32 / row_groups(K);
   constexpr int RS = stage_rs(K);
   constexpr int KS = stage_ks(K);
-  const int rg = lane >> 2;
-  const int cg = lane & 3;
-  const int col = warp * 16 + cg * 4;  // column within the tile
+  const int rg = lane / CQ;
+  const int cg = lane % CQ;
+  const int col = warp * warp_cols(K) + cg * 4;  // column within the tile
   const int T = p.T;
   const int V = p.V;
   const size_t colg = (size_t)it.vt * BV + col;  // column within the state
@@ -698,7 +729,7 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
       }
     }
 #pragma unroll
-    for (int off = 4; off <= 16; off <<= 1) {
+    for (int off = CQ; off <= 16; off <<= 1) {
       acc.x = __fadd_rn(acc.x, __shfl_xor_sync(0xffffffffu, acc.x, off));
       acc.y = __fadd_rn(acc.y, __shfl_xor_sync(0xffffffffu, acc.y, off));
       acc.z = __fadd_rn(acc.z, __shfl_xor_sync(0xffffffffu, acc.z, off));
@@ -711,11 +742,11 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
     u.x = __fmul_rn(be, __fsub_rn(v4.x, acc.x)); u.y = __fmul_rn(be, __fsub_rn(v4.y, acc.y));
     u.z = __fmul_rn(be, __fsub_rn(v4.z, acc.z)); u.w = __fmul_rn(be, __fsub_rn(v4.w, acc.w));
     // rank-1 update, partial S^T q, streaming snapshot store
-    // this thread's rows are own_row(rg, i) = 8 i + row_perm(rg): start at row
-    // row_perm(rg), step 8 rows
+    // this thread's rows are own_row(rg, i) = RG i + row_perm(rg): start at
+    // row row_perm(rg), step RG rows
     float* dst = DEC ? nullptr
-                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + row_perm(rg)) * V + colg;
-    const size_t step8 = (size_t)8 * V;
+                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + row_perm<K>(rg)) * V + colg;
+    const size_t step8 = (size_t)row_groups(K) * V;
     float4 oa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < R; i += 4) {
@@ -734,7 +765,7 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
       }
     }
 #pragma unroll
-    for (int off = 4; off <= 16; off <<= 1) {
+    for (int off = CQ; off <= 16; off <<= 1) {
       oa.x = __fadd_rn(oa.x, __shfl_xor_sync(0xffffffffu, oa.x, off));
       oa.y = __fadd_rn(oa.y, __shfl_xor_sync(0xffffffffu, oa.y, off));
       oa.z = __fadd_rn(oa.z, __shfl_xor_sync(0xffffffffu, oa.z, off));
@@ -747,9 +778,9 @@ __device__ __forceinline__ void consume(const Params& p, const Item& it, const f
   }
   if constexpr (DEC) {
     // decode: the state after the last token replaces the persistent state
-    float* dst = p.S_out + ((size_t)it.s_unit * K + row_perm(rg)) * V + colg;
+    float* dst = p.S_out + ((size_t)it.s_unit * K + row_perm<K>(rg)) * V + colg;
 #pragma unroll
-    for (int i = 0; i < R; ++i) st_stream_f4(dst + (size_t)i * 8 * V, s[i]);
+    for (int i = 0; i < R; ++i) st_stream_f4(dst + (size_t)i * row_groups(K) * V, s[i]);
   }
 }
 
@@ -802,12 +833,13 @@ template <typename Act, int K, int BV, bool DEC = false>
 __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, const float* sQ,
                                             const float* sK, const float* sA, const float* sV,
                                             const float* sB, float* sS, int warp, int lane) {
-  constexpr int R = K / 8;
+  constexpr int R = rows_per_thread(K);
+  constexpr int CQ = 32 / row_groups(K);
   constexpr int RS = stage_rs(K);
   constexpr int KS = stage_ks(K);
-  const int rg = lane >> 2;
-  const int cg = lane & 3;
-  const int col = warp * 16 + cg * 4;
+  const int rg = lane / CQ;
+  const int cg = lane % CQ;
+  const int col = warp * warp_cols(K) + cg * 4;
   const int T = p.T;
   const int V = p.V;
   const size_t colg = (size_t)it.vt * BV + col;
@@ -825,7 +857,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
       const float kv[4] = {k4.x, k4.y, k4.z, k4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float4 x = *reinterpret_cast<const float4*>(sS + tile_index<K, BV>(own_row(rg, i + j), col));
+        float4 x = *reinterpret_cast<const float4*>(sS + tile_index<K, BV>(own_row<K>(rg, i + j), col));
         x.x = __fmul_rn(x.x, av[j]); x.y = __fmul_rn(x.y, av[j]);
         x.z = __fmul_rn(x.z, av[j]); x.w = __fmul_rn(x.w, av[j]);
         acc.x = __fmaf_rn(x.x, kv[j], acc.x); acc.y = __fmaf_rn(x.y, kv[j], acc.y);
@@ -833,7 +865,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
       }
     }
 #pragma unroll
-    for (int off = 4; off <= 16; off <<= 1) {
+    for (int off = CQ; off <= 16; off <<= 1) {
       acc.x = __fadd_rn(acc.x, __shfl_xor_sync(0xffffffffu, acc.x, off));
       acc.y = __fadd_rn(acc.y, __shfl_xor_sync(0xffffffffu, acc.y, off));
       acc.z = __fadd_rn(acc.z, __shfl_xor_sync(0xffffffffu, acc.z, off));
@@ -845,9 +877,9 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
     u.x = __fmul_rn(be, __fsub_rn(v4.x, acc.x)); u.y = __fmul_rn(be, __fsub_rn(v4.y, acc.y));
     u.z = __fmul_rn(be, __fsub_rn(v4.z, acc.z)); u.w = __fmul_rn(be, __fsub_rn(v4.w, acc.w));
     const bool last = t == T - 1;
-    float* dst = DEC ? (last ? p.S_out + ((size_t)it.s_unit * K + row_perm(rg)) * V + colg : nullptr)
-                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + row_perm(rg)) * V + colg;
-    const size_t step8 = (size_t)8 * V;
+    float* dst = DEC ? (last ? p.S_out + ((size_t)it.s_unit * K + row_perm<K>(rg)) * V + colg : nullptr)
+                     : p.inter_ssm + ((((size_t)it.im_row * T + t) * p.HV + it.hv) * K + row_perm<K>(rg)) * V + colg;
+    const size_t step8 = (size_t)row_groups(K) * V;
     float4 oa = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < R; i += 4) {
@@ -859,7 +891,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
       const float qv[4] = {q4.x, q4.y, q4.z, q4.w};
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        float4* ep = reinterpret_cast<float4*>(sS + tile_index<K, BV>(own_row(rg, i + j), col));
+        float4* ep = reinterpret_cast<float4*>(sS + tile_index<K, BV>(own_row<K>(rg, i + j), col));
         float4 x = *ep;
         x.x = __fmul_rn(x.x, av[j]); x.y = __fmul_rn(x.y, av[j]);
         x.z = __fmul_rn(x.z, av[j]); x.w = __fmul_rn(x.w, av[j]);
@@ -872,7 +904,7 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
       }
     }
 #pragma unroll
-    for (int off = 4; off <= 16; off <<= 1) {
+    for (int off = CQ; off <= 16; off <<= 1) {
       oa.x = __fadd_rn(oa.x, __shfl_xor_sync(0xffffffffu, oa.x, off));
       oa.y = __fadd_rn(oa.y, __shfl_xor_sync(0xffffffffu, oa.y, off));
       oa.z = __fadd_rn(oa.z, __shfl_xor_sync(0xffffffffu, oa.z, off));
@@ -897,11 +929,10 @@ __host__ __device__ constexpr int tile_min_blocks(int warps, bool sms) {
 template <typename Act, int K, int WARPS, bool DEC = false, bool SMS = false>
 __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     kda_tile_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
-  constexpr int BV = WARPS * 16;
+  constexpr int BV = WARPS * warp_cols(K);
   constexpr int NT = WARPS * 32;
-  constexpr int R = K / 8;
-  // K = 256 keeps 32 rows x 4 columns per thread: only the shared-memory state fits
-  static_assert(K % 32 == 0 && (K <= 128 || (K == 256 && SMS)), "unsupported K for this variant");
+  constexpr int R = rows_per_thread(K);
+  static_assert(K == 32 || K == 64 || K == 128 || K == 256, "unsupported K");
 
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* mbar = reinterpret_cast<uint64_t*>(smem);
@@ -1084,8 +1115,8 @@ __device__ __forceinline__ long long next_live_item(const Params& p, long long i
 template <typename Act, int K, int CW>
 __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
     kda_ws_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
-  constexpr int BV = CW * 16;
-  constexpr int R = K / 8;
+  constexpr int BV = CW * warp_cols(K);
+  constexpr int R = rows_per_thread(K);
   constexpr int KS = stage_ks(K);
   static_assert(K % 32 == 0 && K <= 128, "K must be 32, 64 or 128");
 

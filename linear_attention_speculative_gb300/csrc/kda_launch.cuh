@@ -11,7 +11,7 @@
 namespace kda {
 
 struct LaunchCfg {
-  int K;        // 32, 64 or 128
+  int K;        // 32, 64, 128 or 256
   int warps;    // tile kernel: warps per CTA; ws kernel: consumer warps
   bool ws;      // warp-specialised persistent kernel
   bool decode;  // tile kernel without snapshots, final state written in place
@@ -83,6 +83,7 @@ int launch_tile_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchC
   KDA_CASES_K(32)
   KDA_CASES_K(64)
   KDA_CASES_K(128)
+  KDA_CASE(256, 2) KDA_CASE(256, 4) KDA_CASE(256, 8)
   KDA_CASE_SMS(256, 4)
   KDA_CASE_SMS(256, 8)
 #undef KDA_CASES_K

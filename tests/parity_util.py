@@ -116,3 +116,21 @@ def conv_window_properties(inputs_cpu, out, conv_state_dev):
     for t in range(T):
         assert torch.equal(snaps[:, t], xext[:, :, t + 1:t + 4]), f"snapshot {t}"
     assert torch.equal(conv_state_dev, xext[:, :, T:T + 3]), "rolled conv_state"
+
+
+def plan_built(plan, K, V, decode=False) -> bool:
+    """Whether an explicit plan string names a kernel the library builds for
+    head dims K x V: one-item tiles are 1/2/4/8 warps of 16 columns (K <= 128;
+    1 warp not for K = 256, whose warps hold 8 columns), the shared-memory
+    state 4 or 8 warps, the persistent kernel K <= 128 and no decode."""
+    if plan in (None, "auto"):
+        return True
+    kind, bv = plan.split(":")[0], int(plan.split(":")[1])
+    wc = 8 if K == 256 else 16
+    if bv > V or V % bv:
+        return False
+    if kind == "large":
+        return K <= 128 and not decode and bv in (32, 64, 128)
+    if kind == "smem":
+        return bv in (4 * wc, 8 * wc)
+    return bv in (2 * wc, 4 * wc, 8 * wc) or (K <= 128 and bv == wc)

@@ -308,14 +308,21 @@ def test_decode_rejects_bad_arguments(kda):
     assert call(plan=kda.parse_plan("small:64")) == -8  # wider than V = 32
 
 
-def test_plan_head_dim_256_uses_the_shared_memory_state(kda):
+def test_plan_head_dim_256_layout(kda):
+    # K = 256: 16 row groups x 2 column quads per warp, 8 columns per warp, so an
+    # 8-warp tile is 64 columns wide
     p = kda.make_plan(kda.make_shape(64, 4, 8, 16, K=256, V=256), 152)
-    assert p.variant == kda.VARIANT_SMEM_STATE and p.bv == 64 and p.items == 64 * 16 * 4
+    assert p.variant == kda.VARIANT_SMALL_BATCH and p.bv == 64 and p.warps == 8
+    assert p.items == 64 * 16 * 4
+    p1 = kda.make_plan(kda.make_shape(512, 1, 8, 16, K=256, V=256), 152)
+    assert p1.variant == kda.VARIANT_SMALL_BATCH and p1.bv == 64 and p1.warps == 8
     q = kda.make_plan(kda.make_shape(64, 4, 8, 16, K=128, V=256), 152)
     assert q.variant == kda.VARIANT_SMALL_BATCH and q.bv == 128 and q.items == 64 * 16 * 2
-    for v in ("small_batch", "large_batch"):
-        with pytest.raises(kda.KdaError) as e:
-            kda.make_plan(kda.make_shape(4, 2, 1, 1, K=256, V=128), 152, v)
-        assert e.value.code == -8
+    with pytest.raises(kda.KdaError) as e:
+        kda.make_plan(kda.make_shape(4, 2, 1, 1, K=256, V=128), 152, "large_batch")
+    assert e.value.code == -8
     s = kda.make_shape(2, 2, 1, 1, K=256, V=128)
-    assert _call_plan(kda, s, _fake_args(kda), kda.parse_plan("small:64")) == -8
+    assert kda.resolve_plan(s, 152, "small:32").warps == 4
+    assert kda.resolve_plan(s, 152, "smem:32").warps == 4
+    for bad in ("small:128", "smem:128", "small:8", "large:64"):  # 16 warps / 1 warp / persistent: not built
+        assert _call_plan(kda, s, _fake_args(kda), kda.parse_plan(bad)) == -8, bad

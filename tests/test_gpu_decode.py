@@ -6,7 +6,7 @@ import pytest
 import torch
 
 from linear_attention_speculative_gb300 import workloads as wk
-from parity_util import to_device
+from parity_util import plan_built, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -31,7 +31,8 @@ def _decode(kda, inp, gate, plan=None, idx=None):
 
 
 @pytest.mark.parametrize("plan", [None, "small:128", "small:32", "small:16:0:-1", "smem:128", "smem:64",
-                                  "small:32:0:0:kernel", "smem:64:0:0:kernel", "smem:128:0:0:counter"])
+                                  "small:32:0:0:kernel", "smem:64:0:0:kernel", "smem:128:0:0:counter",
+                                  "small:64", "smem:32"])
 @pytest.mark.parametrize("case", [(5, 4, 2, 4, 128, 128, "bf16", "softplus"),
                                   (3, 1, 2, 2, 128, 128, "bf16", "safe"),
                                   (4, 3, 1, 2, 64, 64, "f32", "softplus"),
@@ -40,10 +41,8 @@ def _decode(kda, inp, gate, plan=None, idx=None):
 def test_decode_equals_last_verify_snapshot(case, plan):
     from linear_attention_speculative_gb300 import kda
     N, T, H, HV, K, V, act, gate = case
-    if plan and int(plan.split(":")[1]) > V:
-        pytest.skip("tile wider than V")
-    if K == 256 and plan and not plan.startswith("smem"):
-        pytest.skip("K = 256 runs on the shared-memory-state variant only")
+    if not plan_built(plan, K, V, decode=True):
+        pytest.skip("no such kernel for this shape")
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=91 + T)
     inp = to_device(wk.make_inputs(wl))
     ver = dict(inp, conv_state=inp["conv_state"].clone())

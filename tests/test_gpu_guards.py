@@ -77,7 +77,8 @@ CASES = [
     (wk.custom(5, 3, 2, 4, 128, 128, seed=401), ("small:128", "small:16", "smem:128", "large:64",
                                                  "large:128:2", "small:128:0:0:kernel",
                                                  "smem:128:0:0:kernel", "small:64:0:0:counter")),
-    (wk.custom(3, 2, 1, 2, 256, 256, seed=402), ("smem:64", "smem:128")),
+    (wk.custom(3, 2, 1, 2, 256, 256, seed=402), ("smem:64", "smem:32", "small:64", "small:16",
+                                                 "small:64:0:0:kernel")),
     (wk.custom(4, 16, 2, 2, 32, 32, act="f32", seed=403), ("small:32", "small:16", "large:32")),
     (wk.custom(6, 1, 3, 6, 64, 128, gate="safe", seed=404), ("small:64", "smem:64", "large:32",
                                                               "small:64:0:0:kernel")),

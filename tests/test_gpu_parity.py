@@ -16,8 +16,8 @@ import torch
 
 import oracle
 from linear_attention_speculative_gb300 import workloads as wk
-from parity_util import (TOL, assert_parity, conv_window_properties, max_rel_err, rel_rmse,
-                         run_kernel, to_device)
+from parity_util import (TOL, assert_parity, conv_window_properties, max_rel_err, plan_built,
+                         rel_rmse, run_kernel, to_device)
 
 pytestmark = pytest.mark.gpu
 
@@ -323,9 +323,8 @@ def test_head_dim_256(case):
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=300 + K + V + T)
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, gate)
-    plans = ["auto"] + [p for p in ("smem:64", "smem:128") if int(p.split(":")[1]) <= V]
-    if K <= 128:
-        plans += ["small:128", "large:64"]
+    plans = ["auto"] + [p for p in ("smem:32", "smem:64", "smem:128", "small:16", "small:32", "small:64",
+                                      "small:128", "large:64") if plan_built(p, K, V)]
     first = None
     for plan in plans:
         out, cs = run_kernel(inp, gate, plan)
@@ -349,11 +348,8 @@ def _random_cases(n=24, seed=2026):
         N = int(rng.integers(1, 7))
         act = str(rng.choice(["bf16", "f32"]))
         gate = str(rng.choice(["softplus", "safe"]))
-        if K == 256:
-            plans = [p for p in ("smem:64", "smem:128") if int(p.split(":")[1]) <= V]
-        else:
-            plans = [p for p in ("small:16", "small:32", "small:64", "small:128", "large:32",
-                                 "large:64", "smem:64", "smem:128") if int(p.split(":")[1]) <= V]
+        plans = [p for p in ("small:16", "small:32", "small:64", "small:128", "large:32",
+                             "large:64", "smem:32", "smem:64", "smem:128") if plan_built(p, K, V)]
         if not plans:
             continue
         plan = str(rng.choice(plans))
@@ -392,10 +388,11 @@ def test_qk_roll_kernel_and_counter_match_the_oracle(case):
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=700 + T + K)
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, gate)
-    kinds = ("smem",) if K == 256 else (("small", "smem") if V >= 64 else ("small",))
+    full = min(V, 64 if K == 256 else 128)
+    kinds = ("small", "smem") if plan_built(f"smem:{full}", K, V) else ("small",)
     outs = []
     for kind in kinds:
-        bv = min(V, 128)
+        bv = full
         for roll in ("counter", "kernel"):
             plan = f"{kind}:{bv}:0:0:{roll}"
             out, cs = run_kernel(inp, gate, plan)
