@@ -58,13 +58,12 @@ typedef enum {
   KDA_VARIANT_LARGE_BATCH = 2, /* persistent, warp-specialised CTAs; the next item's inputs
                                   and state tile staged by TMA while the current one runs */
   KDA_VARIANT_SMEM_STATE = 3   /* one item per CTA, the state kept in shared memory instead
-                                  of registers (more CTAs per SM; v-tile 64 or 128; the
-                                  only variant for K = 256) */
+                                  of registers (more CTAs per SM; 4 or 8 warps) */
 } kda_variant;
 
 /* Problem shape.  Supported: T in [1, KDA_MAX_T] (N == 0 is a no-op),
- * H >= 1, HV a multiple of H, W == 4, K and V in {32, 64, 128, 256}.  K = 256
- * runs on the shared-memory-state variant only (KDA_VARIANT_SMEM_STATE). */
+ * H >= 1, HV a multiple of H, W == 4, K and V in {32, 64, 128, 256}.  The
+ * persistent variant (KDA_VARIANT_LARGE_BATCH) is built for K <= 128. */
 typedef struct {
   int N, T, H, HV, K, V, W;
   kda_dtype act;
@@ -290,11 +289,13 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
 int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan);
 
 /* Same as kda_conv_verify with an explicit launch plan, e.g. one returned by
- * kda_make_plan and then edited.  Read from `plan`: variant (SMALL_BATCH or
- * LARGE_BATCH), bv (v-tile width: 16, 32, 64 or 128 for SMALL_BATCH; 32, 64
- * or 128 for LARGE_BATCH; at most V and dividing V) and, for LARGE_BATCH,
- * grid (persistent CTAs; <= 0 picks the default), for SMALL_BATCH prefetch
- * (see kda_plan).  The other fields are recomputed.  An invalid plan returns KDA_ERR_VARIANT.  Every plan produces
+ * kda_make_plan and then edited.  Read from `plan`: variant, bv (v-tile
+ * width, at most V and dividing V: 1, 2, 4 or 8 warps of 16 columns for
+ * SMALL_BATCH, 4 or 8 for SMEM_STATE -- at K = 256 warps of 8 columns, and 2,
+ * 4 or 8 of them for SMALL_BATCH; 32, 64 or 128 for LARGE_BATCH), for
+ * LARGE_BATCH grid (persistent CTAs; <= 0 picks the default), for the
+ * one-item variants prefetch and qk_roll (see kda_plan).  The other fields are
+ * recomputed.  An invalid plan returns KDA_ERR_VARIANT.  Every plan produces
  * bit-identical outputs. */
 int kda_conv_verify_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
                          void* conv_state, const float* A_log, const float* dt_bias,
