@@ -358,6 +358,47 @@ def run_ours(args, wl):
     ms_per_step = kernel_ms / K
     value = global_head_steps * K / (kernel_ms / 1e3)
 
+    # the same step captured once in a CUDA graph and replayed (no host launch
+    # work per step); reported beside the stream-launched figure
+    G = min(K, 50)
+    gstream = torch.cuda.Stream(dev)
+    gstream.wait_stream(stream)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(gstream):
+        step_g = lambda: kda.conv_verify(
+            inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"], inp["dt_bias"],
+            inp["a"], inp["b"], inp["S0"], wl.gate, out["o"], out["inter_ssm"],
+            out["conv_snapshots"], ws, stream=gstream, variant=args.variant, shape=shape,
+            plan=args.plan or None)
+        step_g()  # outside capture: per-device attribute set-up
+    gstream.synchronize()
+    with torch.cuda.graph(graph, stream=gstream):
+        step_g()
+    barrier()
+    g_ms = 0.0
+    with torch.cuda.stream(gstream):
+        if flush_l2:
+            for i in range(G):
+                flush_buf.fill_(float(i))
+                a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a_ev.record(gstream)
+                graph.replay()
+                b_ev.record(gstream)
+                b_ev.synchronize()
+                g_ms += a_ev.elapsed_time(b_ev)
+        else:
+            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_ev.record(gstream)
+            for _ in range(G):
+                graph.replay()
+            b_ev.record(gstream)
+            b_ev.synchronize()
+            g_ms = a_ev.elapsed_time(b_ev)
+    barrier()
+    g_ms = max_over_ranks(g_ms, dev)
+    graph_line = {"ms_per_step": g_ms / G, "value": global_head_steps * G / (g_ms / 1e3), "steps": G}
+    del graph
+
     # end to end: pinned host inputs in, every output back, through the same
     # call.  Two streams with their own device buffers alternate steps, so one
     # step's device->host copy overlaps the next step's host->device copy and
@@ -445,6 +486,7 @@ def run_ours(args, wl):
                 "d2h_bytes_per_step": d2h, "steps": E,
                 "note": "pinned host buffers; two streams alternate steps so copies overlap"},
         "gpu_launches": K * max(1, plan.launches),
+        "graph": graph_line,
         "clocks": clocks.summary(),
     }
     if not args.no_cpu_baseline:
