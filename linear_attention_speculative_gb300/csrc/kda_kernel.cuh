@@ -3,21 +3,23 @@
 // request 107).
 //
 // Work item: (sequence n, value head hv, v-tile vt) = a K x BV slice of one
-// recurrent state, BV = 16 * (consumer warps).
+// recurrent state, BV = warp_cols(K) * (consumer warps).
 //
 //   producer  conv1d(W=4) + SiLU of the q/k channels of head h = hv / G and of
 //             the tile's v channels, one task per (8-channel vector, token);
 //             q/k L2 norm (q scaled by K^-1/2), alpha = exp(g) and beta,
 //             staged in shared memory; the raw conv windows are streamed out
 //             as snapshots and the conv_state is rolled.
-//   state     the item's S0 slice arrives in shared memory by one 2-D TMA
-//             tile load (mbarrier completion), then moves to registers.
-//   consumer  every warp owns 16 columns; lane = (row group rg in 0..7,
-//             column quad cg in 0..3) keeps rows [rg*K/8, (rg+1)*K/8) x 4
-//             columns of S in registers.  Per token: decay + S^T k partial
-//             sums, a 3-step xor butterfly across the row groups, the rank-1
-//             update fused with the S^T q partial sums and the 16-byte
-//             streaming store of the snapshot, a second butterfly, o.
+//   state     the item's S0 slice arrives in shared memory by 2-D TMA tile
+//             loads (mbarrier completion), then moves to registers (or stays
+//             in shared memory in the SMS variant).
+//   consumer  a warp is RG row groups x 32/RG column quads (RG = 8 for
+//             K <= 128: 16 columns per warp; RG = 16 for K = 256: 8 columns);
+//             lane (rg, cg) keeps rows RG i + row_perm(rg), i < K/RG, x 4
+//             columns of S.  Per token: decay + S^T k partial sums, an xor
+//             butterfly across the row groups, the rank-1 update fused with
+//             the S^T q partial sums and the 16-byte streaming store of the
+//             snapshot, a second butterfly, o.
 //
 // Two kernels run that same producer arithmetic and consumer code:
 //   kda_tile_kernel  one item per CTA; every warp produces, then consumes.
