@@ -473,7 +473,8 @@ def run_ours(args, wl):
                    "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
                    "variant": {1: "small_batch", 2: "large_batch", 3: "smem_state"}[plan.variant],
                    "v_tile": plan.bv, "plan": args.plan or "auto",
-                   "qk_roll": {1: "counter", 2: "kernel"}.get(plan.qk_roll, "counter"),
+                   "qk_roll": ("single reader" if (s.HV // s.H) * (s.V // plan.bv) == 1 else
+                               {1: "counter", 2: "kernel"}.get(plan.qk_roll, "counter")),
                    "l2": ("L2 flushed between steps (256 MB write)" if flush_l2 else
                           f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB moved per step"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
