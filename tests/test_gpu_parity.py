@@ -404,3 +404,31 @@ def test_qk_roll_kernel_and_counter_match_the_oracle(case):
         assert torch.equal(c, c0), plan
         for key in ("o", "inter_ssm", "conv_snapshots"):
             assert torch.equal(o[key], o0[key]), (plan, key)
+
+
+@pytest.mark.parametrize("gate", ("softplus", "safe"))
+def test_extreme_activation_inputs(gate):
+    # pre-activations far into the tails of SiLU, sigmoid and softplus: the
+    # hardware exponential overflows to inf there, which the producer's
+    # forms turn into the right limits (silu -> 0 or y, sigmoid -> 0 or 1,
+    # softplus -> linear above 20 and ~exp(x) far below 0)
+    wl = wk.custom(3, 4, 2, 4, 64, 64, gate=gate, seed=880)
+    inp = wk.make_inputs(wl)
+    g = torch.Generator().manual_seed(881)
+    x = inp["mixed_qkv"].float()
+    x = x * 60.0 * (torch.rand(x.shape, generator=g) < 0.2) + x
+    inp["mixed_qkv"] = x.to(inp["mixed_qkv"].dtype)
+    a = inp["a"].float()
+    if gate == "softplus":
+        a = a * 40.0  # a + dt_bias from about -160 to +160
+    else:
+        a = a * 30.0 - 20.0  # mostly far below 0 (log-decays), some above 0 (clamped)
+    inp["a"] = a.to(inp["a"].dtype)
+    b = inp["b"].float() * 50.0
+    inp["b"] = b.to(inp["b"].dtype)
+    ref = oracle.verify(inp, gate)
+    for plan in ("auto", "small:64", "smem:64", "small:32:0:0:kernel"):
+        out, cs = run_kernel(inp, gate, plan)
+        for key in ("o", "inter_ssm"):
+            assert torch.isfinite(out[key].float()).all(), (plan, key)
+        assert_parity(out, cs, ref)
