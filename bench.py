@@ -130,10 +130,11 @@ def kernel_src_hash(kernel="verify"):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(wl_name):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    or None when absent or taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"ncu_{wl_name}.md")
+def ncu_traffic(wl_name, kernel_tag):
+    """DRAM bytes per launch from the committed ncu summary of this kernel
+    (profiles/ncu_<kernel_tag>_<workload>.md), or None when absent or taken on
+    other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"ncu_{kernel_tag}_{wl_name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
@@ -479,7 +480,9 @@ def run_ours(args, wl):
                           f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB moved per step"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": ncu_traffic(wl.name),
+                     "frac": achieved / peak,
+                     "traffic": ncu_traffic(wl.name, {1: "kda_tile_kernel", 2: "kda_ws_kernel",
+                                                      3: "kda_tile_kernel_sms"}[plan.variant]),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                      "kernel": "kda_ws_kernel" if plan.variant == 2 else "kda_tile_kernel"},
