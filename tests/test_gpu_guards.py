@@ -5,7 +5,7 @@ workspace, the decode state, the commit outputs) is placed inside a larger
 allocation whose guard zones before and after it hold a sentinel pattern.
 After the call the guards must be untouched: any write outside a buffer's
 extent by any kernel, plan, pool mapping or shape shows up here.  This stands
-in for a memory checker, which is not available on this machine pool.
+in for a memory checker run.
 """
 import pytest
 import torch
