@@ -235,7 +235,9 @@ def cpu_baseline(wl, inputs_cpu, cpu_seconds=12.0):
     t0 = time.perf_counter()
     oracle.verify(sub, wl.gate, seqs=list(range(n1)), threads=1)
     dt1 = time.perf_counter() - t0
+    bytes_per_head_step = s.algorithmic_bytes() / s.head_steps
     return {"value": hs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "gb_per_s": hs / dt * bytes_per_head_step / 1e9,
             "single_core_value": n1 * s.T * s.HV / dt1,
             "sample": f"{passes} full pass(es) over the {s.N} sequences of {wl.name} ({hs} head-steps), "
                       f"fp64 C oracle, {cores} threads, {dt:.2f} s wall (~{dt * cores:.0f} s CPU); "
