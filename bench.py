@@ -52,6 +52,9 @@ def parse():
                     help="explicit launch plan, e.g. small:32 or large:64 (overrides --variant)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time the stream-launched kernel only: no graph, e2e or CPU legs, and no "
+                         "device buffers beyond the one workload (for profiler captures)")
     ap.add_argument("--scaling", default="weak", choices=["weak", "strong"],
                     help="weak: every rank runs the whole workload; strong: the ranks split "
                          "its sequences")
@@ -361,97 +364,104 @@ def run_ours(args, wl):
     ms_per_step = kernel_ms / K
     value = global_head_steps * K / (kernel_ms / 1e3)
 
-    # the same step captured once in a CUDA graph and replayed (no host launch
-    # work per step); reported beside the stream-launched figure
-    G = min(K, 50)
-    gstream = torch.cuda.Stream(dev)
-    gstream.wait_stream(stream)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(gstream):
-        step_g = lambda: kda.conv_verify(
-            inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"], inp["dt_bias"],
-            inp["a"], inp["b"], inp["S0"], wl.gate, out["o"], out["inter_ssm"],
-            out["conv_snapshots"], ws, stream=gstream, variant=args.variant, shape=shape,
-            plan=args.plan or None)
-        step_g()  # outside capture: per-device attribute set-up
-    gstream.synchronize()
-    with torch.cuda.graph(graph, stream=gstream):
-        step_g()
-    barrier()
-    g_ms = 0.0
-    with torch.cuda.stream(gstream):
-        if flush_l2:
-            for i in range(G):
-                flush_buf.fill_(float(i))
+    graph_line = None
+    if not args.kernel_only:
+        # the same step captured once in a CUDA graph and replayed (no host launch
+        # work per step); reported beside the stream-launched figure
+        G = min(K, 50)
+        gstream = torch.cuda.Stream(dev)
+        gstream.wait_stream(stream)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(gstream):
+            step_g = lambda: kda.conv_verify(
+                inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"], inp["dt_bias"],
+                inp["a"], inp["b"], inp["S0"], wl.gate, out["o"], out["inter_ssm"],
+                out["conv_snapshots"], ws, stream=gstream, variant=args.variant, shape=shape,
+                plan=args.plan or None)
+            step_g()  # outside capture: per-device attribute set-up
+        gstream.synchronize()
+        with torch.cuda.graph(graph, stream=gstream):
+            step_g()
+        barrier()
+        g_ms = 0.0
+        with torch.cuda.stream(gstream):
+            if flush_l2:
+                for i in range(G):
+                    flush_buf.fill_(float(i))
+                    a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a_ev.record(gstream)
+                    graph.replay()
+                    b_ev.record(gstream)
+                    b_ev.synchronize()
+                    g_ms += a_ev.elapsed_time(b_ev)
+            else:
                 a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a_ev.record(gstream)
-                graph.replay()
+                for _ in range(G):
+                    graph.replay()
                 b_ev.record(gstream)
                 b_ev.synchronize()
-                g_ms += a_ev.elapsed_time(b_ev)
-        else:
-            a_ev, b_ev = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a_ev.record(gstream)
-            for _ in range(G):
-                graph.replay()
-            b_ev.record(gstream)
-            b_ev.synchronize()
-            g_ms = a_ev.elapsed_time(b_ev)
-    barrier()
-    g_ms = max_over_ranks(g_ms, dev)
-    graph_line = {"ms_per_step": g_ms / G, "value": global_head_steps * G / (g_ms / 1e3), "steps": G}
-    del graph
+                g_ms = a_ev.elapsed_time(b_ev)
+        barrier()
+        g_ms = max_over_ranks(g_ms, dev)
+        graph_line = {"ms_per_step": g_ms / G, "value": global_head_steps * G / (g_ms / 1e3), "steps": G}
+        del graph
 
-    # end to end: pinned host inputs in, every output back, through the same
-    # call.  Two streams with their own device buffers alternate steps, so one
-    # step's device->host copy overlaps the next step's host->device copy and
-    # kernel (the copy engines of the two directions run concurrently).
-    E = max(2, min(args.e2e_steps, K))
-    host_in = {k: (v.pin_memory() if v is not None else None) for k, v in inputs_cpu.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
-    lanes = []
-    for r in range(2):
-        dev_in = inp if r == 0 else {k: (torch.empty_like(v) if v is not None else None)
-                                     for k, v in inp.items()}
-        dev_out = out if r == 0 else {k: torch.empty_like(v) for k, v in out.items()}
-        host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
-        host_out["conv_state"] = torch.empty(inp["conv_state"].shape,
-                                             dtype=inp["conv_state"].dtype).pin_memory()
-        lanes.append(dict(stream=stream if r == 0 else torch.cuda.Stream(dev), inp=dev_in,
-                          out=dev_out, host_out=host_out, ws=ws if r == 0 else
-                          kda.alloc_workspace(shape, dev)))
-    d2h = sum(v.numel() * v.element_size() for v in lanes[0]["host_out"].values())
+    e2e_line = None
+    if not args.kernel_only:
+        # end to end: pinned host inputs in, every output back, through the same
+        # call.  Two streams with their own device buffers alternate steps, so one
+        # step's device->host copy overlaps the next step's host->device copy and
+        # kernel (the copy engines of the two directions run concurrently).
+        E = max(2, min(args.e2e_steps, K))
+        host_in = {k: (v.pin_memory() if v is not None else None) for k, v in inputs_cpu.items()}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values() if v is not None)
+        lanes = []
+        for r in range(2):
+            dev_in = inp if r == 0 else {k: (torch.empty_like(v) if v is not None else None)
+                                         for k, v in inp.items()}
+            dev_out = out if r == 0 else {k: torch.empty_like(v) for k, v in out.items()}
+            host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in out.items()}
+            host_out["conv_state"] = torch.empty(inp["conv_state"].shape,
+                                                 dtype=inp["conv_state"].dtype).pin_memory()
+            lanes.append(dict(stream=stream if r == 0 else torch.cuda.Stream(dev), inp=dev_in,
+                              out=dev_out, host_out=host_out, ws=ws if r == 0 else
+                              kda.alloc_workspace(shape, dev)))
+        d2h = sum(v.numel() * v.element_size() for v in lanes[0]["host_out"].values())
 
-    def e2e_step(lane):
-        st, x, y, ho = lane["stream"], lane["inp"], lane["out"], lane["host_out"]
-        with torch.cuda.stream(st):
-            for k, v in host_in.items():
-                if v is not None:
-                    x[k].copy_(v, non_blocking=True)
-            kda.conv_verify(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"],
-                            x["dt_bias"], x["a"], x["b"], x["S0"], wl.gate, y["o"],
-                            y["inter_ssm"], y["conv_snapshots"], lane["ws"], stream=st,
-                            variant=args.variant, shape=shape, plan=args.plan or None)
-            for k in ("o", "inter_ssm", "conv_snapshots"):
-                ho[k].copy_(y[k], non_blocking=True)
-            ho["conv_state"].copy_(x["conv_state"], non_blocking=True)
+        def e2e_step(lane):
+            st, x, y, ho = lane["stream"], lane["inp"], lane["out"], lane["host_out"]
+            with torch.cuda.stream(st):
+                for k, v in host_in.items():
+                    if v is not None:
+                        x[k].copy_(v, non_blocking=True)
+                kda.conv_verify(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"],
+                                x["dt_bias"], x["a"], x["b"], x["S0"], wl.gate, y["o"],
+                                y["inter_ssm"], y["conv_snapshots"], lane["ws"], stream=st,
+                                variant=args.variant, shape=shape, plan=args.plan or None)
+                for k in ("o", "inter_ssm", "conv_snapshots"):
+                    ho[k].copy_(y[k], non_blocking=True)
+                ho["conv_state"].copy_(x["conv_state"], non_blocking=True)
 
-    for r in range(2):
-        e2e_step(lanes[r])
-    barrier()
-    f0 = torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    lanes[1]["stream"].wait_event(f0)
-    for i in range(E):
-        e2e_step(lanes[i % 2])
-    ends = []
-    for lane in lanes:
-        ev = torch.cuda.Event(enable_timing=True)
-        ev.record(lane["stream"])
-        ends.append(ev)
-    barrier()
-    e2e_ms = max_over_ranks(max(f0.elapsed_time(ev) for ev in ends), dev)
-    e2e_value = global_head_steps * E / (e2e_ms / 1e3)
+        for r in range(2):
+            e2e_step(lanes[r])
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        lanes[1]["stream"].wait_event(f0)
+        for i in range(E):
+            e2e_step(lanes[i % 2])
+        ends = []
+        for lane in lanes:
+            ev = torch.cuda.Event(enable_timing=True)
+            ev.record(lane["stream"])
+            ends.append(ev)
+        barrier()
+        e2e_ms = max_over_ranks(max(f0.elapsed_time(ev) for ev in ends), dev)
+        e2e_value = global_head_steps * E / (e2e_ms / 1e3)
+        e2e_line = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "steps": E,
+                    "note": "pinned host buffers; two streams alternate steps so copies overlap"}
 
     if rank == 0:
         clocks.stop()
@@ -488,14 +498,12 @@ def run_ours(args, wl):
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                      "kernel": "kda_ws_kernel" if plan.variant == 2 else "kda_tile_kernel"},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": E,
-                "note": "pinned host buffers; two streams alternate steps so copies overlap"},
+        "e2e": e2e_line,
         "gpu_launches": K * max(1, plan.launches),
         "graph": graph_line,
         "clocks": clocks.summary(),
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not args.kernel_only:
         line["cpu_baseline"] = cpu_baseline(wl, inputs_cpu)
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -261,11 +261,26 @@ int kda_commit_indexed(const kda_shape* s, const kda_state_indices* idx,
  * allocates or frees.  All calls share the one array: calls whose kernels
  * overlap on the GPU race and must be serialised by the caller. */
 #define KDA_NOALLOC_MAX_SCRATCH_BYTES (256 * 1024)
+/* An empty batch (N == 0) launches nothing and touches no scratch; its shape
+ * and gate mode are checked as kda_conv_verify checks them.  The address is
+ * kept per device together with the driver context it was looked up in; a
+ * call under another context (after cudaDeviceReset, or a context the caller
+ * made current) looks it up again. */
 int kda_conv_verify_noalloc(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
                             void* conv_state, const float* A_log, const float* dt_bias,
                             const void* a, const void* b, const float* S0,
                             kda_gate_mode gate_mode, void* o, float* inter_ssm,
                             void* conv_snapshots, kda_stream_t stream);
+
+/* Synchronously read (and clear) the device status word of the built-in
+ * scratch that kda_conv_verify_noalloc uses, on `stream`.  `s` is the shape
+ * of the call whose status is wanted (the word sits after that shape's
+ * arrival counters).  Read it before the next kda_conv_verify_noalloc call:
+ * every call clears the scratch it uses first.  *status receives KDA_STATUS_*
+ * bits (KDA_STATUS_TMA_TIMEOUT: a kernel gave up a bounded wait and its
+ * outputs are incomplete).  Returns 0, KDA_ERR_NULL, KDA_ERR_SCRATCH_LIMIT,
+ * KDA_ERR_DEVICE or a cudaError_t.  Allocates nothing. */
+int kda_noalloc_read_status(const kda_shape* s, int* status, kda_stream_t stream);
 
 /* Bytes of workspace a call with shape `s` needs (arrival counters for the
  * shared q/k conv_state write-back, N*H int32, used when the plan's qk_roll

@@ -31,8 +31,8 @@ MAX_T = 16
 # The names declared in include/kda_verify.h.
 EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan",
             "kda_conv_verify_indexed", "kda_conv_decode", "kda_commit", "kda_commit_indexed",
-            "kda_conv_verify_noalloc", "kda_workspace_bytes", "kda_make_plan", "kda_resolve_plan",
-            "kda_read_status", "kda_strerror", "kda_version")
+            "kda_conv_verify_noalloc", "kda_noalloc_read_status", "kda_workspace_bytes",
+            "kda_make_plan", "kda_resolve_plan", "kda_read_status", "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
 
@@ -103,6 +103,8 @@ def _load():
     L.kda_conv_verify_noalloc.restype = ctypes.c_int
     L.kda_conv_verify_noalloc.argtypes = [sp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int,
                                           vp, vp, vp, vp]
+    L.kda_noalloc_read_status.restype = ctypes.c_int
+    L.kda_noalloc_read_status.argtypes = [sp, ctypes.POINTER(ctypes.c_int), vp]
     L.kda_workspace_bytes.restype = sz
     L.kda_workspace_bytes.argtypes = [sp]
     L.kda_make_plan.restype = ctypes.c_int
@@ -238,6 +240,17 @@ def conv_verify_noalloc(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0,
         _ptr(conv_snapshots), _stream_handle(stream))
     if rc != 0:
         raise KdaError(rc, "kda_conv_verify_noalloc")
+
+
+def noalloc_read_status(shape: KdaShape, stream=None) -> int:
+    """Read and clear the status word of the allocation-free entry point's
+    built-in scratch (for the call of shape `shape`; synchronises `stream`)."""
+    st = ctypes.c_int(0)
+    rc = lib().kda_noalloc_read_status(ctypes.byref(shape), ctypes.byref(st),
+                                       _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_noalloc_read_status")
+    return st.value
 
 
 STATUS_TMA_TIMEOUT = 1

@@ -47,38 +47,45 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(L):
+    for name in ("orc_silu", "orc_sigmoid", "orc_softplus", "orc_gate_safe"):
+        f = getattr(L, name)
+        f.restype = ctypes.c_double
+        f.argtypes = [ctypes.c_double]
+    L.orc_gate_softplus.restype = ctypes.c_double
+    L.orc_gate_softplus.argtypes = [ctypes.c_double] * 3
+    L.orc_causal_conv1d_silu.restype = None
+    L.orc_causal_conv1d_silu.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp]
+    L.orc_l2norm.restype = None
+    L.orc_l2norm.argtypes = [ctypes.c_int, _dp, ctypes.c_double]
+    L.orc_delta_rule_step.restype = None
+    L.orc_delta_rule_step.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp,
+                                      ctypes.c_double, _dp, ctypes.c_double, _dp]
+    L.orc_commit_seq.restype = ctypes.c_int
+    L.orc_commit_seq.argtypes = [ctypes.c_int] * 7 + [_dp] * 4
+    L.orc_kda_conv_verify_seq.restype = ctypes.c_int
+    L.orc_kda_conv_verify_seq.argtypes = ([ctypes.c_int] * 7 + [ctypes.c_double]
+                                          + [_dp] * 12)
+    return L
+
+
 def lib():
-    """The compiled oracle.  KDA_ORACLE_LIB, when set, names another build of
-    kda_oracle.c to load instead (the mutation tests plant mistakes in copies
-    of the source and check that the pins catch them)."""
+    """The compiled oracle (built from kda_oracle.c on first use)."""
     global _lib
     with _lock:
         if _lib is None:
-            path = os.environ.get("KDA_ORACLE_LIB")
-            if not path:
-                build()
-                path = _LIB_PATH
-            L = ctypes.CDLL(path)
-            for name in ("orc_silu", "orc_sigmoid", "orc_softplus", "orc_gate_safe"):
-                f = getattr(L, name)
-                f.restype = ctypes.c_double
-                f.argtypes = [ctypes.c_double]
-            L.orc_gate_softplus.restype = ctypes.c_double
-            L.orc_gate_softplus.argtypes = [ctypes.c_double] * 3
-            L.orc_causal_conv1d_silu.restype = None
-            L.orc_causal_conv1d_silu.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp]
-            L.orc_l2norm.restype = None
-            L.orc_l2norm.argtypes = [ctypes.c_int, _dp, ctypes.c_double]
-            L.orc_delta_rule_step.restype = None
-            L.orc_delta_rule_step.argtypes = [ctypes.c_int, ctypes.c_int, _dp, _dp, _dp, _dp,
-                                              ctypes.c_double, _dp, ctypes.c_double, _dp]
-            L.orc_commit_seq.restype = ctypes.c_int
-            L.orc_commit_seq.argtypes = [ctypes.c_int] * 7 + [_dp] * 4
-            L.orc_kda_conv_verify_seq.restype = ctypes.c_int
-            L.orc_kda_conv_verify_seq.argtypes = ([ctypes.c_int] * 7 + [ctypes.c_double]
-                                                  + [_dp] * 12)
-            _lib = L
+            _lib = _bind(ctypes.CDLL(build()))
     return _lib
+
+
+def use_library(path: str) -> None:
+    """Load another build of kda_oracle.c in place of the default one, for the
+    rest of this process.  Only the mutation test's child process calls this:
+    it plants a mistake in a copy of the source and checks that the pins
+    catch it."""
+    global _lib
+    with _lock:
+        _lib = _bind(ctypes.CDLL(path))
 
 
 def _f64(x) -> np.ndarray:

@@ -104,6 +104,31 @@ def assert_parity(out, conv_state_dev, ref, seqs=None, tol=TOL):
     return e_o, e_s
 
 
+def assert_decode_parity(o, S_final, conv_state_dev, ref, seqs=None, t=-1, tol=TOL):
+    """Compare a plain decode (or one token of a chain) with the oracle's
+    verify of the same inputs: the state it leaves against the oracle's state
+    snapshot after token `t`, its o against the oracle's o (rounded check,
+    relative RMS), and the rolled conv_state bit for bit (None: not checked).
+    `o` holds the tokens the decode ran; `ref` the oracle's whole call."""
+    def pick(x):
+        x = x if seqs is None else x[list(seqs)]
+        return x.detach().to("cpu", torch.float64).numpy()
+
+    T = ref["o"].shape[1]
+    toks = list(range(T)) if o.shape[1] == T else [t % T]
+    y_o = ref["o"][:, toks]
+    x_o = pick(o)
+    e_o = max_rel_err_rounded(x_o, y_o, o.dtype)
+    r_o = rel_rmse(x_o, y_o)
+    e_s = max_rel_err(pick(S_final), ref["inter_ssm"][:, t])
+    assert e_o <= tol, f"o max rel err beyond output rounding {e_o:.3e} > {tol}"
+    assert r_o <= tol, f"o rel rmse {r_o:.3e} > {tol}"
+    assert e_s <= tol, f"state max rel err {e_s:.3e} > {tol}"
+    if conv_state_dev is not None:
+        assert np.array_equal(pick(conv_state_dev), ref["conv_state"]), "rolled conv_state differs"
+    return e_o, e_s
+
+
 def conv_window_properties(inputs_cpu, out, conv_state_dev):
     """Full-size check that holds at any size: every snapshot and the rolled
     state are the right raw window of [old conv_state || tokens] (pure

@@ -1,12 +1,16 @@
 """GPU parity of kda_conv_decode (plain decode: no snapshots, state updated
-in place).  Its state must equal the verify's last snapshot bit for bit, its
-o and rolled conv_state the verify's, and T single-token decodes must equal
+in place).  Every test compares the decode with the CPU oracle's verify of
+the same inputs (the state it leaves against the oracle's last state
+snapshot, o within the tolerance, the rolled conv_state bit for bit), and
+also checks that it equals the GPU verify bit for bit: its state the verify's
+last snapshot, its o and conv_state the verify's, and T single-token decodes
 one T-token verify."""
 import pytest
 import torch
 
+import oracle
 from linear_attention_speculative_gb300 import workloads as wk
-from parity_util import plan_built, to_device
+from parity_util import assert_decode_parity, plan_built, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -44,11 +48,14 @@ def test_decode_equals_last_verify_snapshot(case, plan):
     if not plan_built(plan, K, V, decode=True):
         pytest.skip("no such kernel for this shape")
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=91 + T)
-    inp = to_device(wk.make_inputs(wl))
+    inp_cpu = wk.make_inputs(wl)
+    orc = oracle.verify(inp_cpu, gate)
+    inp = to_device(inp_cpu)
     ver = dict(inp, conv_state=inp["conv_state"].clone())
     ref = kda.run(ver, gate)
     dec = dict(inp, conv_state=inp["conv_state"].clone(), S0=inp["S0"].clone())
     o = _decode(kda, dec, gate, plan)
+    assert_decode_parity(o, dec["S0"], dec["conv_state"], orc)
     assert torch.equal(dec["S0"], ref["inter_ssm"][:, -1])
     assert torch.equal(o, ref["o"])
     assert torch.equal(dec["conv_state"], ver["conv_state"])
@@ -58,7 +65,9 @@ def test_single_token_decodes_chain_to_one_verify():
     from linear_attention_speculative_gb300 import kda
     T = 4
     wl = wk.custom(6, T, 2, 4, 128, 128, seed=95)
-    inp = to_device(wk.make_inputs(wl))
+    inp_cpu = wk.make_inputs(wl)
+    orc = oracle.verify(inp_cpu, wl.gate)
+    inp = to_device(inp_cpu)
     ver = dict(inp, conv_state=inp["conv_state"].clone())
     ref = kda.run(ver, wl.gate)
     st = dict(inp, conv_state=inp["conv_state"].clone(), S0=inp["S0"].clone())
@@ -67,15 +76,19 @@ def test_single_token_decodes_chain_to_one_verify():
         for key in ("mixed_qkv", "a", "b"):
             step[key] = inp[key][:, t:t + 1].contiguous()
         o = _decode(kda, step, wl.gate)
+        # token t of the chain against token t of the oracle's one call
+        assert_decode_parity(o, st["S0"], None, orc, t=t)
         assert torch.equal(o[:, 0], ref["o"][:, t])
         assert torch.equal(st["S0"], ref["inter_ssm"][:, t])
+    assert_decode_parity(o, st["S0"], st["conv_state"], orc, t=T - 1)
     assert torch.equal(st["conv_state"], ver["conv_state"])
 
 
 def test_decode_over_state_pools():
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(5, 2, 2, 2, 128, 128, seed=96)
-    inp = to_device(wk.make_inputs(wl))
+    inp_cpu = wk.make_inputs(wl)
+    inp = to_device(inp_cpu)
     N = 5
     slot_s = torch.tensor([7, 0, -1, 3, 5], dtype=torch.int32, device="cuda")
     slot_c = torch.tensor([1, 4, 2, 0, 6], dtype=torch.int32, device="cuda")
@@ -97,6 +110,9 @@ def test_decode_over_state_pools():
     ref = kda.run(ver, wl.gate)
     torch.cuda.synchronize()
     live = [0, 1, 3, 4]
+    orc = oracle.verify(inp_cpu, wl.gate, seqs=live)
+    assert_decode_parity(o[live], torch.stack([S_pool[int(slot_s[n])] for n in live]),
+                         torch.stack([cs_pool[int(slot_c[n])] for n in live]), orc)
     for n in live:
         assert torch.equal(S_pool[slot_s[n]], ref["inter_ssm"][n, -1])
         assert torch.equal(cs_pool[slot_c[n]], ver["conv_state"][n])

@@ -148,9 +148,13 @@ def test_chain_of_single_token_calls_is_bit_exact(variant, gate):
     from linear_attention_speculative_gb300 import kda
     T = 4
     wl = wk.custom(6, T, 2, 4, 128, 128, gate=gate, seed=11)
-    inp = to_device(wk.make_inputs(wl))
+    inp_cpu = wk.make_inputs(wl)
+    orc = oracle.verify(inp_cpu, gate)
+    inp = to_device(inp_cpu)
     full_cs = inp["conv_state"].clone()
     full = kda.run(dict(inp, conv_state=full_cs), gate, variant=variant)
+    torch.cuda.synchronize()
+    assert_parity(full, full_cs, orc)
     S = inp["S0"].clone()
     cs = inp["conv_state"].clone()
     for t in range(T):
@@ -161,6 +165,12 @@ def test_chain_of_single_token_calls_is_bit_exact(variant, gate):
         step["S0"] = S
         step["conv_state"] = cs
         out = kda.run(step, gate, variant=variant)
+        torch.cuda.synchronize()
+        # token t of the chain against token t of the oracle's one T-token call
+        one = {"o": orc["o"][:, t:t + 1], "inter_ssm": orc["inter_ssm"][:, t:t + 1],
+               "conv_snapshots": orc["conv_snapshots"][:, t:t + 1],
+               "conv_state": orc["conv_snapshots"][:, t]}
+        assert_parity(out, cs, one)
         assert torch.equal(out["o"][:, 0], full["o"][:, t])
         assert torch.equal(out["inter_ssm"][:, 0], full["inter_ssm"][:, t])
         assert torch.equal(out["conv_snapshots"][:, 0], full["conv_snapshots"][:, t])
@@ -222,6 +232,7 @@ def test_side_streams_and_separate_workspaces():
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(8, 4, 2, 4, 128, 128, seed=21)
     inp_cpu = wk.make_inputs(wl)
+    orc = oracle.verify(inp_cpu, wl.gate)
     ref, _ = run_kernel(inp_cpu, wl.gate, "auto")
     streams = [torch.cuda.Stream() for _ in range(2)]
     results = []
@@ -231,6 +242,7 @@ def test_side_streams_and_separate_workspaces():
             results.append((kda.run(inp, wl.gate, stream=st), inp["conv_state"]))
     torch.cuda.synchronize()
     for out, cs in results:
+        assert_parity(out, cs, orc)
         assert torch.equal(out["inter_ssm"], ref["inter_ssm"])
         assert torch.equal(out["o"], ref["o"])
 
@@ -242,6 +254,7 @@ def test_cuda_graph_replay(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(4, 3, 2, 4, 128, 128, seed=23)
     inp_cpu = wk.make_inputs(wl)
+    orc = oracle.verify(inp_cpu, wl.gate)
     ref, ref_cs = run_kernel(inp_cpu, wl.gate, "auto")
     inp = to_device(inp_cpu)
     cs0 = inp["conv_state"].clone()
@@ -266,6 +279,7 @@ def test_cuda_graph_replay(plan):
         out["inter_ssm"].zero_()
         g.replay()
         torch.cuda.synchronize()
+        assert_parity(out, inp["conv_state"], orc)
         assert torch.equal(out["inter_ssm"], ref["inter_ssm"])
         assert torch.equal(out["o"], ref["o"])
         assert torch.equal(inp["conv_state"], ref_cs)

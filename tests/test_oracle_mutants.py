@@ -68,10 +68,9 @@ def _build(tmp_path, name, text):
 
 
 def _run_pins(lib):
-    env = dict(os.environ, KDA_ORACLE_LIB=lib)
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        "-x", "-q", "-p", "no:cacheprovider", "-k", "not frozen"],
-                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    # a child process loads the mutant build explicitly and runs the pins on it
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "tests", "mutant_pins_main.py"), lib],
+                       cwd=ROOT, capture_output=True, text=True, timeout=600)
     return r.returncode, r.stdout[-2000:]
 
 

@@ -48,6 +48,33 @@ def test_rejects_shapes_beyond_the_built_in_scratch():
     assert "scratch" in kda.strerror(-10)
 
 
+def test_empty_batch_is_checked_like_the_regular_entry_point():
+    # N == 0 launches nothing; the shape and gate mode are still checked, with
+    # the same codes as kda_conv_verify (no CUDA call is made either way)
+    kda, L = _lib()
+    s = kda.make_shape(0, 2, 2, 2)
+    none = {k: None for k in ("mixed_qkv", "conv_w", "A_log", "dt_bias", "a", "b", "S0",
+                              "o", "inter_ssm", "conv_snapshots")}
+    assert _noalloc(L, kda, s, none, "softplus", none, None, None) == 0
+    gm_bad = kda.KdaShape(0, 2, 2, 2, 128, 128, 4, kda.BF16)
+    rc = L.kda_conv_verify_noalloc(ctypes.byref(gm_bad), *([None] * 8), 7, None, None, None, None)
+    assert rc == -7
+    rc_regular = L.kda_conv_verify(ctypes.byref(gm_bad), *([None] * 8), 7, None, None, None, None, 0,
+                                   None)
+    assert rc == rc_regular
+    bad_shape = kda.make_shape(0, 0, 2, 2)  # T = 0
+    assert _noalloc(L, kda, bad_shape, none, "softplus", none, None, None) == -2
+
+
+def test_status_reader_rejects_bad_arguments_on_the_host():
+    kda, L = _lib()
+    st = ctypes.c_int(0)
+    assert L.kda_noalloc_read_status(None, ctypes.byref(st), None) == -1
+    assert L.kda_noalloc_read_status(ctypes.byref(kda.make_shape(4, 1, 1, 1)), None, None) == -1
+    assert L.kda_noalloc_read_status(ctypes.byref(kda.make_shape(70000, 1, 1, 1, 32, 32)),
+                                     ctypes.byref(st), None) == -10
+
+
 # Four v-heads per q/k head in both.  The small launch rolls the shared q/k
 # conv_state with the arrival counters kept in the scratch array; the large one
 # uses the separate roll kernel, and the scratch holds only the status word.
@@ -74,6 +101,8 @@ def test_noalloc_matches_the_regular_entry_point_on_two_calls_in_a_row(wl):
                for k, v in ref.items()}
         rc = _noalloc(L, kda, shape, inp, wl.gate, out, cs, stream)
         assert rc == 0, kda.strerror(rc)
+        # a clean call leaves no status bit (no bounded wait gave up)
+        assert kda.noalloc_read_status(shape, stream) == 0, f"call {call}: device status"
         torch.cuda.synchronize()
         o = out["o"].double().cpu().numpy()
         y = ref["o"].double().cpu().numpy()
