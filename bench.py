@@ -1,7 +1,7 @@
 """Benchmark of the fused causal-conv1d + KDA verify decode on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--variant auto|small_batch|large_batch]
+                    [--workload NAME] [--variant auto|one_item|pipelined]
 
 One step = one kda_conv_verify call over the whole workload (default: the
 large-batch verify, N=256 sequences, T=4 tokens, H=HV=32, K=V=128, bf16
@@ -49,7 +49,7 @@ def parse():
     ap.add_argument("--workload", default="large_bf16_n256_t4_h32")
     ap.add_argument("--variant", default="auto")
     ap.add_argument("--plan", default="",
-                    help="explicit launch plan, e.g. small:32 or large:64 (overrides --variant)")
+                    help="explicit launch plan, e.g. item:32 or pipe:64 (overrides --variant)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-only", action="store_true",
@@ -64,11 +64,11 @@ def parse():
                     help="commit: time kda_commit (accept a random count per sequence); "
                          "decode: time kda_conv_decode (no snapshots, state in place)")
     ap.add_argument("--sweep", action="store_true",
-                    help="time every point of the T x N x heads x gate sweep in both variants")
+                    help="time every point of the T x N x heads x gate sweep with every plan of --sweep-plans")
     ap.add_argument("--sweep-out", default="")
     ap.add_argument("--sweep-filter", default="",
                     help="regular expression: only sweep points whose name matches")
-    ap.add_argument("--sweep-plans", default="auto,small:16,small:32,small:64,small:128,large:64",
+    ap.add_argument("--sweep-plans", default="auto,item:32,item:64,item:128,smem:128,pipe:64,pipe:128",
                     help="plans timed at every sweep point")
     return ap.parse_args()
 
@@ -106,6 +106,9 @@ def measured_hbm_peak():
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
 
+
+# kernel that each plan variant launches (ONE_ITEM, PIPELINED, ONE_ITEM_SMEM)
+KERNEL_OF_VARIANT = {1: "kda_tile_kernel", 2: "kda_pipe_kernel", 3: "kda_tile_kernel_sms"}
 
 # CUDA sources each profiled kernel is built from (the verify kernels: every
 # source but the commit kernel's own file)
@@ -484,8 +487,8 @@ def run_ours(args, wl):
         "scaling": args.scaling, "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "K": s.K,
                    "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
-                   "variant": {1: "small_batch", 2: "large_batch", 3: "smem_state"}[plan.variant],
-                   "v_tile": plan.bv, "plan": args.plan or "auto",
+                   "variant": {1: "one_item", 2: "pipelined", 3: "one_item_smem"}[plan.variant],
+                   "v_tile": plan.bv, "plan": args.plan or f"auto ({plan_label(plan)})",
                    "qk_roll": ("single reader" if (s.HV // s.H) * (s.V // plan.bv) == 1 else
                                {1: "counter", 2: "kernel"}.get(plan.qk_roll, "counter")),
                    "l2": ("L2 flushed between steps (256 MB write)" if flush_l2 else
@@ -493,11 +496,10 @@ def run_ours(args, wl):
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": ncu_traffic(wl.name, {1: "kda_tile_kernel", 2: "kda_ws_kernel",
-                                                      3: "kda_tile_kernel_sms"}[plan.variant]),
+                     "traffic": ncu_traffic(wl.name, KERNEL_OF_VARIANT[plan.variant]),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
-                     "kernel": "kda_ws_kernel" if plan.variant == 2 else "kda_tile_kernel"},
+                     "kernel": KERNEL_OF_VARIANT[plan.variant]},
         "e2e": e2e_line,
         "gpu_launches": K * max(1, plan.launches),
         "graph": graph_line,
@@ -512,7 +514,8 @@ def run_ours(args, wl):
 
 
 def plan_label(plan) -> str:
-    return f"{ {1: 'small', 2: 'large', 3: 'smem'}[plan.variant] }:{plan.bv}"
+    from linear_attention_speculative_gb300 import kda
+    return kda.plan_label(plan)
 
 
 def run_sweep(args):

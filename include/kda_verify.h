@@ -51,19 +51,24 @@ typedef struct CUstream_st* kda_stream_t;
 typedef enum { KDA_GATE_SOFTPLUS = 0, KDA_GATE_SAFE = 1 } kda_gate_mode;
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
-/* Kernel variants.  AUTO picks from N*HV, T and the SM count. */
+/* Kernel variants, named after the kernel they run.  An item is one
+ * (sequence, v-head, v-tile) slice of a state.  AUTO picks from N*HV, T and
+ * the SM count. */
 typedef enum {
   KDA_VARIANT_AUTO = 0,
-  KDA_VARIANT_SMALL_BATCH = 1, /* one CTA per (sequence, v-head, v-tile) */
-  KDA_VARIANT_LARGE_BATCH = 2, /* persistent, warp-specialised CTAs; the next item's inputs
-                                  and state tile staged by TMA while the current one runs */
-  KDA_VARIANT_SMEM_STATE = 3   /* one item per CTA, the state kept in shared memory instead
-                                  of registers (more CTAs per SM; 4 or 8 warps) */
+  KDA_VARIANT_ONE_ITEM = 1,      /* one CTA per item, the state in registers; every warp
+                                    runs the item's producer arithmetic, then its recurrence */
+  KDA_VARIANT_PIPELINED = 2,     /* persistent, warp-specialised CTAs: producer warps stage the
+                                    next item (conv, norms, gate) while consumer warps write the
+                                    current item's snapshots; the next state tile arrives by TMA
+                                    meanwhile.  4 or 8 consumer warps, K <= 128 */
+  KDA_VARIANT_ONE_ITEM_SMEM = 3  /* one item per CTA, the state kept in shared memory instead
+                                    of registers (more CTAs per SM; 4 or 8 warps) */
 } kda_variant;
 
 /* Problem shape.  Supported: T in [1, KDA_MAX_T] (N == 0 is a no-op),
  * H >= 1, HV a multiple of H, W == 4, K and V in {32, 64, 128, 256}.  The
- * persistent variant (KDA_VARIANT_LARGE_BATCH) is built for K <= 128. */
+ * pipelined variant is built for K <= 128 and V >= 64. */
 typedef struct {
   int N, T, H, HV, K, V, W;
   kda_dtype act;
@@ -79,18 +84,19 @@ typedef struct {
   int grid;
   int ctas_per_sm;
   long long items;
-  /* SMALL_BATCH: each CTA prefetches into L2 the inputs and state tile of the
-   * item this many items ahead (about one wave of resident CTAs).  In a plan
-   * given to kda_conv_verify_plan: < 0 off, 0 the default, > 0 explicit. */
+  /* L2 prefetch distance of the one-item variants: each CTA prefetches into
+   * L2 the inputs and state tile of the item this many items ahead (default
+   * about 3/8 of a wave of resident CTAs).  In a plan given to
+   * kda_conv_verify_plan: < 0 off, 0 the default, > 0 explicit.  PIPELINED
+   * requests every input one item ahead itself and ignores it (0). */
   int prefetch;
-  /* One-item-per-CTA variants, when G * (V / bv) > 1 items read the same q/k
-   * channels: who rolls their conv_state.  KDA_QK_ROLL_COUNTER: the last of
-   * those items to arrive on a counter in the workspace, inside the verify
-   * kernel (one launch).  KDA_QK_ROLL_KERNEL: a second, small kernel launched
-   * after the verify kernel on the same stream (no atomics in the verify
-   * kernel; faster on large launches).  In a plan given to
-   * kda_conv_verify_plan, KDA_QK_ROLL_AUTO (0) lets the dispatcher choose.
-   * The persistent variant always uses the counter. */
+  /* When G * (V / bv) > 1 items read the same q/k channels: who rolls their
+   * conv_state.  KDA_QK_ROLL_COUNTER: the last of those items to arrive on a
+   * counter in the workspace, inside the verify kernel (one launch).
+   * KDA_QK_ROLL_KERNEL: a second, small kernel launched after the verify
+   * kernel on the same stream (no atomics in the verify kernel; faster on
+   * large launches).  In a plan given to kda_conv_verify_plan,
+   * KDA_QK_ROLL_AUTO (0) lets the dispatcher choose. */
   int qk_roll;
   /* Kernels one call with this plan launches (1 or 2). */
   int launches;
@@ -203,7 +209,7 @@ int kda_conv_verify_indexed(const kda_shape* s, const kda_state_indices* idx,
  * equals the verify's inter_ssm[.., T-1] bit for bit), and conv_state is
  * rolled.  idx may be NULL (dense) or give cache_indices / conv_state_indices
  * pools (intermediate_state_indices is ignored); plan may be NULL or a
- * SMALL_BATCH plan (LARGE_BATCH: KDA_ERR_VARIANT).  Traffic per
+ * ONE_ITEM / ONE_ITEM_SMEM plan (PIPELINED: KDA_ERR_VARIANT).  Traffic per
  * sequence and head: the state read and written once.  Same error codes. */
 int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void* mixed_qkv,
                     const void* conv_w, void* conv_state, const float* A_log,
@@ -306,12 +312,12 @@ int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan
 /* Same as kda_conv_verify with an explicit launch plan, e.g. one returned by
  * kda_make_plan and then edited.  Read from `plan`: variant, bv (v-tile
  * width, at most V and dividing V: 1, 2, 4 or 8 warps of 16 columns for
- * SMALL_BATCH, 4 or 8 for SMEM_STATE -- at K = 256 warps of 8 columns, and 2,
- * 4 or 8 of them for SMALL_BATCH; 32, 64 or 128 for LARGE_BATCH), for
- * LARGE_BATCH grid (persistent CTAs; <= 0 picks the default), for the
- * one-item variants prefetch and qk_roll (see kda_plan).  The other fields are
- * recomputed.  An invalid plan returns KDA_ERR_VARIANT.  Every plan produces
- * bit-identical outputs. */
+ * ONE_ITEM, 4 or 8 for ONE_ITEM_SMEM -- at K = 256 warps of 8 columns, and 2,
+ * 4 or 8 of them for ONE_ITEM; 64 or 128 for PIPELINED, whose shared memory
+ * must also fit one CTA: at T = 16 with fp32 activations only 64), for
+ * PIPELINED grid (persistent CTAs; <= 0 picks one wave of resident CTAs),
+ * prefetch and qk_roll (see kda_plan).  The other fields are recomputed.  An invalid plan
+ * returns KDA_ERR_VARIANT.  Every plan produces bit-identical outputs. */
 int kda_conv_verify_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w,
                          void* conv_state, const float* A_log, const float* dt_bias,
                          const void* a, const void* b, const float* S0, kda_gate_mode gate_mode,

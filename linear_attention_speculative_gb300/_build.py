@@ -20,8 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(LIB_DIR, "obj")
 LIB_PATH = os.path.join(LIB_DIR, "libkda_gb300.so")
-SOURCES = ("kda_api.cu", "kda_inst_tile_bf16.cu", "kda_inst_tile_f32.cu", "kda_inst_ws_bf16.cu",
-           "kda_inst_ws_f32.cu", "kda_roll.cu", "kda_commit.cu", "kda_noalloc.cu")
+SOURCES = ("kda_api.cu", "kda_inst_tile_bf16.cu", "kda_inst_tile_f32.cu", "kda_inst_pipe_bf16.cu",
+           "kda_inst_pipe_f32.cu", "kda_roll.cu", "kda_commit.cu", "kda_noalloc.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1,5 +1,5 @@
 // kda_api.cu -- the C ABI declared in include/kda_verify.h: argument
-// validation, the small/large-batch dispatcher, the TMA descriptor of the
+// validation, the dispatcher, the TMA descriptor of the
 // state tensor, and the launch.  Host code only; kernels live in
 // kda_kernel.cuh and are instantiated in kda_inst_*.cu.
 #include <cudaTypedefs.h>
@@ -19,6 +19,7 @@ using kda::Params;
 
 constexpr int kSmemPerSm = 233472;  // bytes of shared memory per SM (228 KB)
 constexpr int kSmemReservedPerCta = 1024;
+constexpr size_t kMaxSmemPerCta = 232448;  // opt-in dynamic shared memory per CTA (227 KB)
 
 bool supported_dim(int x) { return x == 32 || x == 64 || x == 128 || x == 256; }
 
@@ -54,20 +55,26 @@ bool valid_tile_bv(int bv, int K, int V) {
   const int wc = kda::warp_cols(K);
   return (bv == 2 * wc || bv == 4 * wc || bv == 8 * wc || (K <= 128 && bv == wc)) && fits_v(bv, V);
 }
-bool valid_ws_bv(int bv, int V) { return (bv == 32 || bv == 64 || bv == 128) && fits_v(bv, V); }
+bool valid_pipe_bv(int bv, int K, int V) {
+  return K <= 128 && (bv == 4 * kda::warp_cols(K) || bv == 8 * kda::warp_cols(K)) && fits_v(bv, V);
+}
 bool valid_sms_bv(int bv, int K, int V) {
   const int wc = kda::warp_cols(K);
   return (bv == 4 * wc || bv == 8 * wc) && fits_v(bv, V);
 }
 
-// A plan's tile width against its variant (decode: no persistent variant;
-// the persistent variant is built for K <= 128).
-bool valid_plan(const kda_plan* plan, int K, int V, bool decode) {
+// A plan's tile width against its variant (decode: no pipelined variant;
+// the pipelined variant is built for K <= 128 and needs its shared memory --
+// two raw-input buffers and two stages besides the tile -- to fit one CTA).
+bool valid_plan(const kda_plan* plan, const kda_shape* s, bool decode) {
   if (plan->qk_roll < KDA_QK_ROLL_AUTO || plan->qk_roll > KDA_QK_ROLL_KERNEL) return false;
+  const int K = s->K, V = s->V;
   switch (plan->variant) {
-    case KDA_VARIANT_SMALL_BATCH: return valid_tile_bv(plan->bv, K, V);
-    case KDA_VARIANT_LARGE_BATCH: return K <= 128 && !decode && valid_ws_bv(plan->bv, V);
-    case KDA_VARIANT_SMEM_STATE: return valid_sms_bv(plan->bv, K, V);
+    case KDA_VARIANT_ONE_ITEM: return valid_tile_bv(plan->bv, K, V);
+    case KDA_VARIANT_PIPELINED:
+      return !decode && valid_pipe_bv(plan->bv, K, V) &&
+             kda::pipe_smem_bytes(s->T, K, plan->bv, (int)act_bytes(s)) <= kMaxSmemPerCta;
+    case KDA_VARIANT_ONE_ITEM_SMEM: return valid_sms_bv(plan->bv, K, V);
     default: return false;
   }
 }
@@ -78,17 +85,19 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
   const long long units = (long long)s->N * s->HV;
   const int ab = s->act == KDA_F32 ? 4 : 2;
   out->items = units * (s->V / out->bv);
-  if (out->variant == KDA_VARIANT_LARGE_BATCH) {
+  if (out->variant == KDA_VARIANT_PIPELINED) {
     out->warps = out->bv / kda::warp_cols(s->K);
-    const size_t smem = kda::ws_smem_bytes(s->T, s->K, out->bv, ab);
-    out->ctas_per_sm = ctas_per_sm_for(kda::ws_min_blocks(out->warps), smem);
+    const size_t smem = kda::pipe_smem_bytes(s->T, s->K, out->bv, ab);
+    out->ctas_per_sm = ctas_per_sm_for(kda::pipe_min_blocks(out->warps), smem);
     const long long cap = (long long)num_sms * out->ctas_per_sm;
     long long grid = requested_grid > 0 ? requested_grid : cap;
     out->grid = (int)std::max(1LL, std::min(out->items, grid));
+    // the kernel requests every input one item ahead itself: no L2 prefetch
+    out->prefetch = 0;
   } else {
     out->warps = out->bv / kda::warp_cols(s->K);
     const size_t smem = kda::tile_smem_bytes(s->T, s->K, out->bv, ab);
-    const bool sms = out->variant == KDA_VARIANT_SMEM_STATE;
+    const bool sms = out->variant == KDA_VARIANT_ONE_ITEM_SMEM;
     out->ctas_per_sm = ctas_per_sm_for(kda::tile_min_blocks(out->warps, sms), smem);
     out->grid = (int)std::max(1LL, out->items);
     // 3/8 of a wave of resident CTAs ahead: measured on GB300, any distance
@@ -102,7 +111,7 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
   // per item (measured on GB300: 6-14 % on launches of many waves), the second
   // kernel a launch (~2-3 us, which dominates small launches)
   const bool shared_qk = (long long)(s->HV / s->H) * (s->V / out->bv) > 1;
-  if (out->variant == KDA_VARIANT_LARGE_BATCH || !shared_qk) {
+  if (!shared_qk) {
     out->qk_roll = KDA_QK_ROLL_COUNTER;
   } else if (requested_qk_roll != KDA_QK_ROLL_AUTO) {
     out->qk_roll = requested_qk_roll;
@@ -172,20 +181,23 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
   if (rc) return rc;
   if (!out) return KDA_ERR_NULL;
   if (num_sms < 1) return KDA_ERR_DEVICE;
-  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
-      variant != KDA_VARIANT_LARGE_BATCH && variant != KDA_VARIANT_SMEM_STATE)
+  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_ONE_ITEM &&
+      variant != KDA_VARIANT_PIPELINED && variant != KDA_VARIANT_ONE_ITEM_SMEM)
     return KDA_ERR_VARIANT;
   const long long units = (long long)s->N * s->HV;
   std::memset(out, 0, sizeof(*out));
   // widest one-item tile: 8 warps (128 columns for K <= 128, 64 for K = 256)
   const int full_bv = std::min(s->V, 8 * kda::warp_cols(s->K));
-  if (variant == KDA_VARIANT_LARGE_BATCH) {
-    if (s->K > 128) return KDA_ERR_VARIANT;
-    out->variant = KDA_VARIANT_LARGE_BATCH;
-    out->bv = s->V >= 64 ? 64 : s->V;
-  } else if (variant == KDA_VARIANT_SMEM_STATE) {
+  if (variant == KDA_VARIANT_PIPELINED) {
+    out->variant = KDA_VARIANT_PIPELINED;
+    out->bv = full_bv;
+    if (!valid_plan(out, s, false)) {  // K > 128, V < 64, or too much shared memory
+      out->bv = 4 * kda::warp_cols(s->K);
+      if (!valid_plan(out, s, false)) return KDA_ERR_VARIANT;
+    }
+  } else if (variant == KDA_VARIANT_ONE_ITEM_SMEM) {
     if (s->V < 4 * kda::warp_cols(s->K)) return KDA_ERR_VARIANT;
-    out->variant = KDA_VARIANT_SMEM_STATE;
+    out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
     out->bv = full_bv;
   } else {
     // One item per CTA.  Whole states (up to 8 warps' columns) per CTA: every
@@ -196,11 +208,11 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
     // unit counts below (per SM: 8, 12, 24); from T = 4 on it is slower (two
     // shared-memory passes per token).  K = 256 (16 rows x 4 columns per
     // thread either way) measured faster on the register state at every T.
-    out->variant = KDA_VARIANT_SMALL_BATCH;
+    out->variant = KDA_VARIANT_ONE_ITEM;
     out->bv = full_bv;
     const long long sms_from = s->T == 1 ? 8 : (s->T == 2 ? 12 : (s->T == 3 ? 24 : 0));
     if (s->K <= 128 && full_bv == 128 && sms_from > 0 && units >= sms_from * num_sms)
-      out->variant = KDA_VARIANT_SMEM_STATE;
+      out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
   }
   finish_plan(s, num_sms, out, 0, 0, KDA_QK_ROLL_AUTO);
   return KDA_OK;
@@ -211,7 +223,7 @@ int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan
   if (rc) return rc;
   if (!plan) return KDA_ERR_NULL;
   if (num_sms < 1) return KDA_ERR_DEVICE;
-  if (!valid_plan(plan, s->K, s->V, decode != 0)) return KDA_ERR_VARIANT;
+  if (!valid_plan(plan, s, decode != 0)) return KDA_ERR_VARIANT;
   finish_plan(s, num_sms, plan, plan->grid, plan->prefetch, plan->qk_roll);
   return KDA_OK;
 }
@@ -345,7 +357,7 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.counters = static_cast<int*>(workspace);
   p.status = static_cast<int*>(workspace) + N * H;
   p.num_items = plan.items;
-  p.prefetch = plan.variant == KDA_VARIANT_LARGE_BATCH ? 0 : plan.prefetch;
+  p.prefetch = plan.prefetch;
   p.idx_state = pl.idx_state;
   p.idx_conv = pl.idx_conv;
   p.idx_inter = pl.idx_inter;
@@ -361,26 +373,25 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.G = s->HV / s->H;
   p.nvt = s->V / plan.bv;
   p.gate_mode = gate_mode == KDA_GATE_SOFTPLUS ? 0 : 1;
-  const bool roll_kernel = plan.variant != KDA_VARIANT_LARGE_BATCH && plan.qk_roll == KDA_QK_ROLL_KERNEL &&
-                           p.G * p.nvt > 1;
+  const bool roll_kernel = plan.qk_roll == KDA_QK_ROLL_KERNEL && p.G * p.nvt > 1;
   p.qk_roll_kernel = roll_kernel ? 1 : 0;
 
   LaunchCfg cfg;
   cfg.K = s->K;
   cfg.warps = plan.warps;
-  cfg.ws = plan.variant == KDA_VARIANT_LARGE_BATCH;
+  cfg.pipe = plan.variant == KDA_VARIANT_PIPELINED;
   cfg.decode = S_out != nullptr;
-  cfg.sms = plan.variant == KDA_VARIANT_SMEM_STATE;
+  cfg.sms = plan.variant == KDA_VARIANT_ONE_ITEM_SMEM;
   cfg.grid = plan.grid;
   const int ab = s->act == KDA_F32 ? 4 : 2;
-  cfg.smem = cfg.ws ? kda::ws_smem_bytes(s->T, s->K, plan.bv, ab)
-                    : kda::tile_smem_bytes(s->T, s->K, plan.bv, ab);
+  cfg.smem = cfg.pipe ? kda::pipe_smem_bytes(s->T, s->K, plan.bv, ab)
+                      : kda::tile_smem_bytes(s->T, s->K, plan.bv, ab);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   int rc;
   if (s->act == KDA_BF16)
-    rc = cfg.ws ? kda::launch_ws_bf16(tmap, p, cfg, st) : kda::launch_tile_bf16(tmap, p, cfg, st);
+    rc = cfg.pipe ? kda::launch_pipe_bf16(tmap, p, cfg, st) : kda::launch_tile_bf16(tmap, p, cfg, st);
   else
-    rc = cfg.ws ? kda::launch_ws_f32(tmap, p, cfg, st) : kda::launch_tile_f32(tmap, p, cfg, st);
+    rc = cfg.pipe ? kda::launch_pipe_f32(tmap, p, cfg, st) : kda::launch_tile_f32(tmap, p, cfg, st);
   if (rc < 0) return KDA_ERR_SHAPE;
   if (rc == 0 && roll_kernel) rc = kda::launch_qk_roll(p, s->K, s->act == KDA_BF16, st);
   return rc;
@@ -396,8 +407,8 @@ int kda_conv_verify_variant(const kda_shape* s, const void* mixed_qkv, const voi
                             kda_gate_mode gate_mode, void* o, float* inter_ssm,
                             void* conv_snapshots, void* workspace, size_t workspace_bytes,
                             kda_variant variant, kda_stream_t stream) {
-  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_SMALL_BATCH &&
-      variant != KDA_VARIANT_LARGE_BATCH && variant != KDA_VARIANT_SMEM_STATE)
+  if (variant != KDA_VARIANT_AUTO && variant != KDA_VARIANT_ONE_ITEM &&
+      variant != KDA_VARIANT_PIPELINED && variant != KDA_VARIANT_ONE_ITEM_SMEM)
     return KDA_ERR_VARIANT;
   if (!s) return KDA_ERR_NULL;
   const Pools pl = dense_pools(s);
@@ -427,7 +438,7 @@ int verify_with(const kda_shape* s, const Pools& pl, const void* mixed_qkv, cons
   int rc = validate_call(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate_mode,
                          o, inter_ssm, conv_snapshots, workspace, workspace_bytes, pl);
   if (rc || s->N == 0) return rc;
-  if (plan && !valid_plan(plan, s->K, s->V, false)) return KDA_ERR_VARIANT;
+  if (plan && !valid_plan(plan, s, false)) return KDA_ERR_VARIANT;
   int num_sms = 0;
   rc = num_sms_of_current_device(&num_sms);
   if (rc) return rc;
@@ -523,7 +534,7 @@ int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void
       if (j != i && overlap(wr[i], wr[j])) return KDA_ERR_ALIAS;
   }
   // decode runs the one-item-per-CTA kernels only
-  if (plan && !valid_plan(plan, s->K, s->V, true)) return KDA_ERR_VARIANT;
+  if (plan && !valid_plan(plan, s, true)) return KDA_ERR_VARIANT;
   int num_sms = 0;
   rc = num_sms_of_current_device(&num_sms);
   if (rc) return rc;

@@ -120,14 +120,6 @@ __host__ __device__ constexpr size_t roll_stash_bytes(int K, int BV, int ab) {
   return (size_t)(2 * K + BV) * 3 * ab;
 }
 
-// raw-input bytes of one item (warp-specialised kernel): x_q, x_k [T][K],
-// x_v [T][BV], conv_state blocks [C][3], conv_w blocks [C][4] (C = 2K + BV
-// channels), a [T][K], dt_bias [K] fp32.
-__host__ __device__ constexpr size_t raw_bytes(int T, int K, int BV, int ab) {
-  return (size_t)ab * ((size_t)T * (2 * K + BV) + (size_t)(2 * K + BV) * 7 + (size_t)T * K) +
-         4 * (size_t)K;
-}
-
 // dynamic shared memory of the two kernels: 128 header bytes (mbarriers,
 // flags), up to 1023 bytes of padding so that the state tile starts on a
 // 1024-byte boundary (the 128-byte swizzle pattern repeats every 1024 bytes),
@@ -136,10 +128,6 @@ constexpr size_t kSmemHeader = 128 + 1024;
 __host__ __device__ constexpr size_t tile_smem_bytes(int T, int K, int BV, int ab) {
   return kSmemHeader + sizeof(float) * ((size_t)K * BV + stage_floats(T, K, BV)) +
          roll_stash_bytes(K, BV, ab);
-}
-__host__ __device__ constexpr size_t ws_smem_bytes(int T, int K, int BV, int ab) {
-  return kSmemHeader + sizeof(float) * ((size_t)K * BV + 2 * (size_t)stage_floats(T, K, BV)) +
-         round16(raw_bytes(T, K, BV, ab));
 }
 
 // ---------------------------------------------------------------------------
@@ -224,12 +212,17 @@ __device__ __forceinline__ int resolve_slot(const int* idx, int n, int pool, boo
   return sl;
 }
 
+// Items number fewer than 2^31 (N * HV * K < 2^31 is checked on the host and
+// V / BV <= 16), so the decode divides in 32 bits.
 __device__ __forceinline__ Item decode_item(const Params& p, long long item) {
   Item it;
-  it.unit = item / p.nvt;
-  it.vt = static_cast<int>(item - it.unit * p.nvt);
-  it.n = static_cast<int>(it.unit / p.HV);
-  it.hv = static_cast<int>(it.unit - (long long)it.n * p.HV);
+  const uint32_t i32 = static_cast<uint32_t>(item);
+  const uint32_t unit = i32 / static_cast<uint32_t>(p.nvt);
+  const uint32_t n = unit / static_cast<uint32_t>(p.HV);
+  it.unit = unit;
+  it.vt = static_cast<int>(i32 - unit * static_cast<uint32_t>(p.nvt));
+  it.n = static_cast<int>(n);
+  it.hv = static_cast<int>(unit - n * static_cast<uint32_t>(p.HV));
   it.h = it.hv / p.G;
   it.skip = it.bad = false;
   const int ss = resolve_slot(p.idx_state, it.n, p.pool_state, it.skip, it.bad);
@@ -281,7 +274,8 @@ struct GlobalSrc {
   }
 };
 
-// From the item's raw-input buffer in shared memory (warp-specialised kernel).
+// From an item's raw inputs staged in shared memory by 1-D bulk copies (the
+// pipelined kernel); same interface as GlobalSrc.
 template <typename Act, int K, int BV>
 struct SmemSrc {
   const unsigned char* raw;
@@ -314,6 +308,13 @@ struct SmemSrc {
     return *reinterpret_cast<const float4*>(raw + base_dt() + (size_t)e0 * 4);
   }
 };
+
+// bytes of one item's staged raw inputs (SmemSrc layout; dt only with the
+// softplus gate, but always reserved)
+__host__ __device__ constexpr size_t raw_bytes(int T, int K, int BV, int ab) {
+  return (size_t)ab * ((size_t)T * (2 * K + BV) + (size_t)(2 * K + BV) * 7 + (size_t)T * K) +
+         4 * (size_t)K;
+}
 
 // ---------------------------------------------------------------------------
 // producer arithmetic (shared by both kernels)
@@ -524,10 +525,14 @@ __device__ __forceinline__ float load_b(const Params& p, const Item& it, int t) 
 // already sit in shared memory, so no reader is left in global memory);
 // otherwise the raw window after the last token of every channel vector cv is
 // staged at stash[3 cv .. 3 cv + 2] and the caller rolls after a barrier.
+// ext_b / ext_negA, when not null, hold this item's beta logits b[t] and
+// -exp(A_log[hv]) (loaded ahead by the caller); otherwise they are read here.
 template <typename Act, int K, int BV, bool DEC = false, bool PACKED = false, typename Src>
 __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, const Item& it,
                                               float* sQ, float* sK, float* sA, float* sV,
-                                              float* sB, uint4* stash, int tid, int nthr) {
+                                              float* sB, uint4* stash, int tid, int nthr,
+                                              const float* ext_b = nullptr,
+                                              const float* ext_negA = nullptr) {
   constexpr int VEC = ActT<Act>::VEC;
   constexpr int NQ = K / VEC;
   constexpr int NCV = 2 * NQ + BV / VEC;  // channel vectors of the item
@@ -538,7 +543,6 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
   // q/k snapshots are written once per group: by its first v-head, first tile
   const bool qk_snap_owner = !DEC && (it.hv % p.G == 0) && (it.vt == 0);
   constexpr bool v_snap = !DEC;  // decode writes no conv-window snapshots
-  const float negA = p.gate_mode == 0 ? -expf(__ldg(p.A_log + it.hv)) : 0.0f;
   // Beta of token t rides on the gate task of its first channel vector.  When
   // the threads outnumber the tasks, the gate tasks start on a warp boundary,
   // so that no warp runs the conv and the gate code paths one after the
@@ -578,7 +582,9 @@ __device__ __forceinline__ void produce_tasks(const Src& src, const Params& p, c
       const int g = task - n_conv;
       const int t = g / NQ;
       const int e0 = (g - t * NQ) * VEC;
-      const float braw = e0 == 0 ? load_b<Act>(p, it, t) : 0.0f;  // issued before the gate math
+      // issued before the gate math
+      const float braw = e0 == 0 ? (ext_b ? ext_b[t] : load_b<Act>(p, it, t)) : 0.0f;
+      const float negA = p.gate_mode != 0 ? 0.0f : (ext_negA ? *ext_negA : -expf(__ldg(p.A_log + it.hv)));
       float al[VEC];
       gate_task<Act>(src, p.gate_mode, negA, t, e0, al);
 #pragma unroll
@@ -605,59 +611,6 @@ __device__ __forceinline__ void l2norm_warp(float* x, bool is_q, int lane) {
   if (is_q) inv = __fmul_rn(inv, rsqrtf(static_cast<float>(K)));
 #pragma unroll
   for (int m = 0; m < K / 32; ++m) x[stage_pos<K>(lane + 32 * m)] = __fmul_rn(xs[m], inv);
-}
-
-// Arrival of one item on its q/k group counter (one thread).  Returns true
-// for the last arrival, which also resets the counter.
-__device__ __forceinline__ bool arrive_qk_group(const Params& p, const Item& it) {
-  const int expected = p.G * p.nvt;
-  if (expected == 1) return true;
-  int* cnt = p.counters + (size_t)it.n * p.H + it.h;
-  __threadfence();  // this item's conv_state reads are complete (ordered before)
-  const int old = atomicAdd(cnt, 1);
-  if (old != expected - 1) return false;
-  atomicExch(cnt, 0);
-  __threadfence();
-  return true;
-}
-
-// Roll the q/k conv_state of group (n, h) to x_ext[T .. T+2], re-reading the
-// raw inputs (warp-specialised kernel: from its shared-memory raw buffer).
-template <typename Act, int K, int BV, typename Src>
-__device__ __forceinline__ void roll_qk(const Src& src, const Params& p, const Item& it, int tid,
-                                        int nthr) {
-  using AT = ActT<Act>;
-  using Raw = typename AT::Raw;
-  constexpr int VEC = AT::VEC;
-  constexpr int NQ = K / VEC;
-  const int T = p.T;
-  for (int task = tid; task < 2 * NQ; task += nthr) {
-    const int kind = task < NQ ? 0 : 1;
-    const int e0 = (task - kind * NQ) * VEC;
-    const int c = block_channel<K, BV>(p, it, kind) + e0;
-    Raw old[3 * VEC] = {};
-    if (T < kConvW - 1) {
-#pragma unroll
-      for (int m = 0; m < 3; ++m) AT::unpack(src.cs(kind, e0, m), old + m * VEC);
-    }
-    Raw r[3 * VEC];
-#pragma unroll
-    for (int j = 0; j < kConvW - 1; ++j) {
-      const int idx = T + j;
-      Raw xv[VEC];
-      if (idx >= kConvW - 1) {
-        AT::unpack(src.x(kind, idx - (kConvW - 1), e0), xv);
-      } else {
-        select_state<Raw, VEC>(old, idx, xv);
-      }
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) r[e * (kConvW - 1) + j] = xv[e];
-    }
-    char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
-                                       ((size_t)it.cs_row * p.dim + c) * (kConvW - 1));
-#pragma unroll
-    for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
-  }
 }
 
 // Store the staged windows x_ext[T .. T+2] (produce_tasks' stash) of channel
@@ -1021,19 +974,46 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
 }
 
 // ---------------------------------------------------------------------------
-// persistent, warp-specialised: warp CW produces, warps 0..CW-1 consume
+// persistent and warp-specialised: producer warps stage the next item while
+// consumer warps run the recurrence of the current one
 // ---------------------------------------------------------------------------
-struct WsBars {
-  uint64_t tile_full;       // TMA state tile landed (1 arrival + tx)
-  uint64_t tile_empty;      // consumers moved the tile to registers (CW*32)
-  uint64_t raw_full;        // raw inputs landed (1 arrival + tx)
-  uint64_t stage_full[2];   // producer staged q/k/alpha/v/beta (32)
-  uint64_t stage_empty[2];  // consumers done with the stage (CW*32)
-  int abort_flag;
+// Each CTA walks the items blockIdx.x, blockIdx.x + gridDim.x, ...  Every
+// input an item needs is requested one item ahead: its raw inputs (token
+// rows, conv_state / conv_w / gate rows) by 1-D bulk copies into one of two
+// raw buffers, its beta logits and A_log by plain loads into registers, its
+// state tile by a 2-D TMA load into the single tile buffer once the consumers
+// hold the previous tile in registers.  The producer warps then run the
+// producer arithmetic from shared memory into one of two stages while the
+// consumer warps stream the previous item's snapshots out, so per SM the
+// snapshot writes of one item overlap all the latency of the next.
+__host__ __device__ constexpr int pipe_producer_warps(int cw) { return cw; }
+__host__ __device__ constexpr int pipe_threads(int cw) { return (cw + pipe_producer_warps(cw)) * 32; }
+__host__ __device__ constexpr int pipe_min_blocks(int cw) { return cw >= 8 ? 1 : 2; }
+constexpr int kPipeStages = 2;       // stages and raw buffers (double-buffered)
+constexpr int kPipeProducerBar = 1;  // named barrier of the producer warps
+constexpr int kPipeConsumerBar = 2;  // named barrier of the consumer warps
+constexpr int kPipeExt = 20;         // floats per item of loaded-ahead scalars: b[0..15], -exp(A_log)
+constexpr int kPipeExtNegA = 16;
+
+struct PipeBars {
+  uint64_t tile_full;                  // the item's state tile landed (1 arrival + tx)
+  uint64_t raw_full[kPipeStages];      // the item's raw inputs landed (1 arrival + tx)
+  uint64_t stage_full[kPipeStages];    // producers staged the item (1 arrival)
+  uint64_t stage_empty[kPipeStages];   // consumers done with the stage (one arrival per warp)
+  int abort_flag;                      // set by a warp that gave up a bounded wait
+  int last_arrival;                    // q/k counter result, broadcast to the producers
 };
 
+// dynamic shared memory: header, tile, stages, staged conv windows, raw
+// buffers, loaded-ahead scalars
+__host__ __device__ constexpr size_t pipe_smem_bytes(int T, int K, int BV, int ab) {
+  return kSmemHeader + sizeof(float) * ((size_t)K * BV + kPipeStages * (size_t)stage_floats(T, K, BV)) +
+         round16(roll_stash_bytes(K, BV, ab)) + kPipeStages * round16(raw_bytes(T, K, BV, ab)) +
+         sizeof(float) * kPipeStages * kPipeExt;
+}
+
 // Bounded wait that also gives up when another warp of the CTA gave up.
-__device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool pipe_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -1045,9 +1025,33 @@ __device__ __forceinline__ bool ws_wait(uint64_t* bar, uint32_t parity, volatile
   }
 }
 
-__device__ __forceinline__ void ws_fail(const Params& p, volatile int* abort_flag) {
-  *abort_flag = 1;
-  atomicOr(p.status, kStatusTmaTimeout);
+// Named barrier over `count` threads that also ORs a predicate across them:
+// every participating thread learns whether any of them failed.
+template <int ID, int COUNT>
+__device__ __forceinline__ bool group_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u), "n"(ID), "n"(COUNT)
+      : "memory");
+  return r != 0;
+}
+
+template <int ID, int COUNT>
+__device__ __forceinline__ void group_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(COUNT) : "memory");
+}
+
+// First item at or after `item`, stepping by `stride`, that is not a padding
+// sequence (num_items when none is left).  Producers and consumers walk the
+// same items, so their mbarrier phases stay in step.
+__device__ __forceinline__ long long next_live_item(const Params& p, long long item, long long stride) {
+  while (item < p.num_items && decode_item(p, item).skip) item += stride;
+  return item;
 }
 
 template <typename Act, int K, int BV>
@@ -1057,27 +1061,29 @@ __device__ __forceinline__ uint32_t raw_tx_bytes(const Params& p) {
                                (p.gate_mode == 0 ? 4 * K : 0));
 }
 
-// 1-D bulk copies of one item's raw inputs into `raw`, spread over the lanes
-// of one warp (lane 0 has already posted raw_tx_bytes on `bar`).
+// 1-D bulk copies of one item's raw inputs into `raw` (SmemSrc layout):
+// copies first, first + step, ... of the 4T + 6 (+1 with the softplus gate).
+// The caller posts raw_tx_bytes on `bar` once per item.  Issuing a bulk copy
+// holds the issuing thread for a while, so the producer warps share them.
 template <typename Act, int K, int BV>
 __device__ __forceinline__ void issue_raw(const Params& p, const Item& it, unsigned char* raw,
-                                          uint64_t* bar, int lane) {
+                                          uint64_t* bar, int first, int step) {
   constexpr int AB = sizeof(Act);
   const int T = p.T;
   const SmemSrc<Act, K, BV> L{raw, T};
   const int ncopy = 4 * T + 6 + (p.gate_mode == 0 ? 1 : 0);
-  const char* xq = static_cast<const char*>(p.mixed_qkv);
-  for (int c = lane; c < ncopy; c += 32) {
+  for (int c = first; c < ncopy; c += step) {
     const char* src;
     unsigned char* dst;
     uint32_t bytes;
-    if (c < 3 * T) {
+    if (c < 3 * T) {  // token rows of the q, k and v blocks
       const int t = c / 3, kind = c - 3 * t;
-      src = xq + (((size_t)it.n * T + t) * p.dim + block_channel<K, BV>(p, it, kind)) * AB;
+      src = static_cast<const char*>(p.mixed_qkv) +
+            (((size_t)it.n * T + t) * p.dim + block_channel<K, BV>(p, it, kind)) * AB;
       dst = raw + L.off_x(kind, t);
       bytes = (kind == 2 ? BV : K) * AB;
-    } else if (c < 3 * T + 6) {
-      const int q = c - 3 * T;  // 0..2 conv_state blocks, 3..5 conv_w blocks
+    } else if (c < 3 * T + 6) {  // conv_state and conv_w blocks
+      const int q = c - 3 * T;
       const int kind = q % 3;
       const int ch = block_channel<K, BV>(p, it, kind);
       const int nch = kind == 2 ? BV : K;
@@ -1090,12 +1096,12 @@ __device__ __forceinline__ void issue_raw(const Params& p, const Item& it, unsig
         dst = raw + L.base_w() + (size_t)L.blk(kind) * 4 * AB;
         bytes = nch * 4 * AB;
       }
-    } else if (c < 4 * T + 6) {
+    } else if (c < 4 * T + 6) {  // gate rows
       const int t = c - 3 * T - 6;
       src = static_cast<const char*>(p.a) + ((((size_t)it.n * T + t) * p.HV + it.hv) * K) * AB;
       dst = raw + L.base_a() + (size_t)t * K * AB;
       bytes = K * AB;
-    } else {
+    } else {  // dt_bias row (softplus gate)
       src = reinterpret_cast<const char*>(p.dt_bias + (size_t)it.hv * K);
       dst = raw + L.base_dt();
       bytes = K * 4;
@@ -1104,35 +1110,56 @@ __device__ __forceinline__ void issue_raw(const Params& p, const Item& it, unsig
   }
 }
 
-__host__ __device__ constexpr int ws_min_blocks(int cw) { return cw >= 8 ? 1 : (cw >= 4 ? 3 : 5); }
-
-// First item at or after `item`, stepping by `stride`, that is not a padding
-// sequence (num_items when none is left).  Producer and consumers walk the
-// same sequence of items, so their mbarrier phases stay in step.
-__device__ __forceinline__ long long next_live_item(const Params& p, long long item, long long stride) {
-  while (item < p.num_items && decode_item(p, item).skip) item += stride;
-  return item;
+// Raw bits of the scalars an item's gate tasks need, loaded by one lane each
+// (lane t < T: b[n, t, hv]; lane kPipeExtNegA: A_log[hv]); to_ext converts
+// them once they are needed, so the loads stay in flight meanwhile.
+template <typename Act>
+__device__ __forceinline__ uint32_t load_ext_bits(const Params& p, const Item& it, int lane) {
+  if (lane < p.T) {
+    const Act* bp = static_cast<const Act*>(p.b) + ((size_t)it.n * p.T + lane) * p.HV + it.hv;
+    if constexpr (sizeof(Act) == 4) return __float_as_uint(__ldg(reinterpret_cast<const float*>(bp)));
+    else return static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(bp)));
+  }
+  if (lane == kPipeExtNegA && p.gate_mode == 0) return __float_as_uint(__ldg(p.A_log + it.hv));
+  return 0u;
+}
+template <typename Act>
+__device__ __forceinline__ void store_ext(const Params& p, uint32_t bits, float* ext, int lane) {
+  if (lane < p.T) ext[lane] = ActT<Act>::to_f(bits);
+  else if (lane == kPipeExtNegA) ext[lane] = p.gate_mode == 0 ? -expf(__uint_as_float(bits)) : 0.0f;
 }
 
 template <typename Act, int K, int CW>
-__global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
-    kda_ws_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
+__global__ void __launch_bounds__(pipe_threads(CW), pipe_min_blocks(CW))
+    kda_pipe_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
   constexpr int BV = CW * warp_cols(K);
   constexpr int R = rows_per_thread(K);
   constexpr int KS = stage_ks(K);
+  constexpr int PW = pipe_producer_warps(CW);
+  constexpr int NP = PW * 32;
+  constexpr int NC = CW * 32;
+  constexpr int AB = sizeof(Act);
+  constexpr int NQV = 2 * K / ActT<Act>::VEC;  // q/k channel vectors
+  constexpr int NCV = NQV + BV / ActT<Act>::VEC;
   static_assert(K % 32 == 0 && K <= 128, "K must be 32, 64 or 128");
 
   extern __shared__ __align__(128) unsigned char smem[];
-  WsBars* bars = reinterpret_cast<WsBars*>(smem);
+  PipeBars* bars = reinterpret_cast<PipeBars*>(smem);
   volatile int* abort_flag = &bars->abort_flag;
   float* sbuf = tile_base(smem);
   const int T = p.T;
   const int sf = stage_floats(T, K, BV);
   float* stage0 = sbuf + K * BV;
-  unsigned char* raw = reinterpret_cast<unsigned char*>(stage0 + 2 * sf);
+  uint4* stash = reinterpret_cast<uint4*>(stage0 + kPipeStages * sf);
+  const size_t raw_stride = round16(raw_bytes(T, K, BV, AB));
+  unsigned char* raw0 = reinterpret_cast<unsigned char*>(stash) + round16(roll_stash_bytes(K, BV, AB));
+  float* ext0 = reinterpret_cast<float*>(raw0 + kPipeStages * raw_stride);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long stride = gridDim.x;
+  // a programmatic dependent launched after this grid (the q/k roll kernel)
+  // may be scheduled once every CTA has started; it waits for completion
+  asm volatile("griddepcontrol.launch_dependents;");
   const long long first = next_live_item(p, blockIdx.x, stride);
   if (threadIdx.x == 0) {  // report out-of-range slots of this CTA's items
     for (long long i = blockIdx.x; i < p.num_items; i += stride) {
@@ -1144,98 +1171,137 @@ __global__ void __launch_bounds__((CW + 1) * 32, ws_min_blocks(CW))
 
   if (threadIdx.x == 0) {
     mbar_init(&bars->tile_full, 1);
-    mbar_init(&bars->tile_empty, CW * 32);
-    mbar_init(&bars->raw_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->stage_full[s], 32);
-      mbar_init(&bars->stage_empty[s], CW * 32);
+    for (int s = 0; s < kPipeStages; ++s) {
+      mbar_init(&bars->raw_full[s], 1);
+      mbar_init(&bars->stage_full[s], 1);
+      mbar_init(&bars->stage_empty[s], CW);
     }
     bars->abort_flag = 0;
     fence_mbar_init();
+    prefetch_tensormap(&tmap_s0);
+    const Item it = decode_item(p, first);
+    mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
+    tma_load_tile<K, BV>(sbuf, &tmap_s0, it.vt, it.s_unit, &bars->tile_full, l2_policy_evict_first());
   }
   __syncthreads();
 
-  if (warp == CW) {
-    // ------------------------------ producer ------------------------------
-    const uint64_t pol = l2_policy_evict_first();
+  if (warp >= CW) {
+    // ------------------------------ producers ------------------------------
+    const int ptid = threadIdx.x - NC;
+    const int pwarp = warp - CW;
+    const int expected = p.G * p.nvt;
     long long item = first;
-    Item it = decode_item(p, item);
-    if (lane == 0) {
-      prefetch_tensormap(&tmap_s0);
-      mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
-      tma_load_tile<K, BV>(sbuf, &tmap_s0, it.vt, it.s_unit, &bars->tile_full, pol);
-      mbar_arrive_expect_tx(&bars->raw_full, raw_tx_bytes<Act, K, BV>(p));
+    int raws = 0;  // raw-input copies issued
+    if (pwarp == 0) {  // the first item's inputs: raw buffer 0, scalars now
+      const Item it = decode_item(p, item);
+      if (lane == 0) mbar_arrive_expect_tx(&bars->raw_full[0], raw_tx_bytes<Act, K, BV>(p));
+      issue_raw<Act, K, BV>(p, it, raw0, &bars->raw_full[0], lane, 32);
+      store_ext<Act>(p, load_ext_bits<Act>(p, it, lane), ext0, lane);
     }
-    __syncwarp();
-    issue_raw<Act, K, BV>(p, it, raw, &bars->raw_full, lane);
-    int raw_phase = 0;   // phase of raw_full that the newest raw copy completes
-    int tile_phase = 0;  // phase of tile_full that the newest tile load completes
+    raws = 1;
     bool failed = false;
-    for (int j = 0;; ++j) {
-      const int s = j & 1;
+    for (int j = 0; item < p.num_items; ++j) {
+      const int s = j % kPipeStages;  // stage, raw buffer and scalar slot of this item
       float* sQ = stage0 + s * sf;
       float* sK = sQ + T * KS;
       float* sA = sK + T * KS;
       float* sV = sA + T * KS;
       float* sB = sV + T * BV;
-      if (!ws_wait(&bars->raw_full, j & 1, abort_flag)) { failed = true; break; }
-      if (j >= 2 && !ws_wait(&bars->stage_empty[s], ((j >> 1) + 1) & 1, abort_flag)) {
-        failed = true;
-        break;
-      }
-      const SmemSrc<Act, K, BV> src{raw, T};
-      produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, nullptr, lane, 32);
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = arrive_qk_group(p, it) ? 1 : 0;
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) roll_qk<Act, K, BV>(src, p, it, lane, 32);
-      __syncwarp();  // every lane is done with the raw buffer
+      const Item it = decode_item(p, item);
       const long long next = next_live_item(p, item + stride, stride);
-      const bool has_next = next < p.num_items;
-      const Item nx = has_next ? decode_item(p, next) : it;
-      if (has_next) {
-        fence_proxy_async_smem();
-        if (lane == 0) mbar_arrive_expect_tx(&bars->raw_full, raw_tx_bytes<Act, K, BV>(p));
-        __syncwarp();
-        issue_raw<Act, K, BV>(p, nx, raw, &bars->raw_full, lane);
-        raw_phase = j + 1;
+      // this item's raw inputs, and its stage free (the consumers are done
+      // with item j - 2)
+      // order this thread's reads of the other raw buffer (item j - 1) before
+      // the bulk copies that refill it below
+      fence_proxy_async_smem();
+      bool ok = pipe_wait(&bars->raw_full[s], (j / kPipeStages) & 1, abort_flag);
+      if (ok && j >= kPipeStages)
+        ok = pipe_wait(&bars->stage_empty[s], ((j / kPipeStages) - 1) & 1, abort_flag);
+      if (group_sync_or<kPipeProducerBar, NP>(!ok)) { failed = true; break; }
+      // request the next item's inputs: its raw buffer was last read by item
+      // j - 1, whose tasks ended before the previous iteration's last barrier
+      // (lane 0 of every producer warp issues its share of the copies)
+      uint32_t ext_bits = 0;
+      if (next < p.num_items) {
+        const Item nx = decode_item(p, next);
+        if (lane == 0) {
+          if (pwarp == 0) mbar_arrive_expect_tx(&bars->raw_full[s ^ 1], raw_tx_bytes<Act, K, BV>(p));
+          issue_raw<Act, K, BV>(p, nx, raw0 + (s ^ 1) * raw_stride, &bars->raw_full[s ^ 1], pwarp, PW);
+        }
+        if (pwarp == PW - 1) ext_bits = load_ext_bits<Act>(p, nx, lane);
       }
-      for (int r = 0; r < 2 * T; ++r) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
-      mbar_arrive(&bars->stage_full[s]);
-      if (!has_next) break;
-      // hand the next state tile over as soon as the consumers hold this one
-      if (!ws_wait(&bars->tile_empty, j & 1, abort_flag)) { failed = true; break; }
-      if (lane == 0) {
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
-        tma_load_tile<K, BV>(sbuf, &tmap_s0, nx.vt, nx.s_unit, &bars->tile_full, pol);
+      if (next < p.num_items) ++raws;
+      const SmemSrc<Act, K, BV> src{raw0 + s * raw_stride, T};
+      const float* ext = ext0 + s * kPipeExt;
+      produce_tasks<Act, K, BV>(src, p, it, sQ, sK, sA, sV, sB, stash, ptid, NP, ext, ext + kPipeExtNegA);
+      group_sync<kPipeProducerBar, NP>();  // every conv_state read of the item is done
+      for (int r = pwarp; r < 2 * T; r += PW) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
+      roll_staged<Act, K, BV>(p, it, stash, NQV, NCV, ptid, NP);  // v: owned by this item
+      if (expected == 1) {
+        roll_staged<Act, K, BV>(p, it, stash, 0, NQV, ptid, NP);  // the only reader of its q/k
+      } else if (!p.qk_roll_kernel) {
+        // q/k shared by several items: the last one to arrive on the group's
+        // counter resets it and rolls (no CTA ever waits on another)
+        if (ptid == 0) {
+          int* cnt = p.counters + (size_t)it.n * p.H + it.h;
+          __threadfence();  // this item's conv_state reads come first
+          const int last = atomicAdd(cnt, 1) == expected - 1;
+          if (last) {
+            atomicExch(cnt, 0);
+            __threadfence();  // every other item's reads come before the stores below
+          }
+          bars->last_arrival = last;
+        }
+        group_sync<kPipeProducerBar, NP>();
+        if (bars->last_arrival) roll_staged<Act, K, BV>(p, it, stash, 0, NQV, ptid, NP);
       }
-      tile_phase = j + 1;
+      if (pwarp == PW - 1 && next < p.num_items) store_ext<Act>(p, ext_bits, ext0 + (s ^ 1) * kPipeExt, lane);
+      group_sync<kPipeProducerBar, NP>();  // stage complete; stash free; next scalars visible
+      if (ptid == 0) mbar_arrive(&bars->stage_full[s]);
       item = next;
-      it = nx;
     }
-    if (failed) {
-      // report, then let the newest copies in flight land before leaving
-      ws_fail(p, abort_flag);
-      mbar_wait_bounded(&bars->raw_full, raw_phase & 1, kWaitLimitNs);
-      mbar_wait_bounded(&bars->tile_full, tile_phase & 1, kWaitLimitNs);
+    if (failed && ptid == 0) {
+      // report, then let the newest raw copy in flight land before leaving
+      *abort_flag = 1;
+      atomicOr(p.status, kStatusTmaTimeout);
+      const int r = raws - 1;
+      mbar_wait_bounded(&bars->raw_full[r % kPipeStages], (r / kPipeStages) & 1, kWaitLimitNs);
     }
   } else {
-    // ------------------------------ consumers -----------------------------
+    // ------------------------------ consumers ------------------------------
     long long item = first;
-    for (int j = 0; item < p.num_items; ++j, item = next_live_item(p, item + stride, stride)) {
-      const int s = j & 1;
+    int tiles = 1;  // state tile loads issued (the first one above)
+    bool failed = false;
+    for (int j = 0; item < p.num_items; ++j) {
+      const int s = j % kPipeStages;
+      const long long next = next_live_item(p, item + stride, stride);
       const Item it = decode_item(p, item);
-      if (!ws_wait(&bars->tile_full, j & 1, abort_flag)) { ws_fail(p, abort_flag); return; }
+      bool ok = pipe_wait(&bars->tile_full, j & 1, abort_flag);
       float4 sreg[R];
-      load_tile<K, BV>(sbuf, sreg, warp, lane);
-      mbar_arrive(&bars->tile_empty);
-      if (!ws_wait(&bars->stage_full[s], (j >> 1) & 1, abort_flag)) { ws_fail(p, abort_flag); return; }
+      if (ok) load_tile<K, BV>(sbuf, sreg, warp, lane);
+      fence_proxy_async_smem();  // these tile reads come before the next tile's TMA writes
+      if (group_sync_or<kPipeConsumerBar, NC>(!ok)) { failed = true; break; }
+      // every consumer holds its part of the tile: load the next item's
+      if (threadIdx.x == 0 && next < p.num_items) {
+        const Item nx = decode_item(p, next);
+        mbar_arrive_expect_tx(&bars->tile_full, K * BV * sizeof(float));
+        tma_load_tile<K, BV>(sbuf, &tmap_s0, nx.vt, nx.s_unit, &bars->tile_full, l2_policy_evict_first());
+      }
+      if (next < p.num_items) ++tiles;
+      ok = pipe_wait(&bars->stage_full[s], (j / kPipeStages) & 1, abort_flag);
+      if (group_sync_or<kPipeConsumerBar, NC>(!ok)) { failed = true; break; }
       const float* st = stage0 + s * sf;
       consume<Act, K, BV>(p, it, st, st + T * KS, st + 2 * T * KS, st + 3 * T * KS,
                           st + 3 * T * KS + T * BV, sreg, warp, lane);
-      mbar_arrive(&bars->stage_empty[s]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->stage_empty[s]);
+      item = next;
+    }
+    if (failed && threadIdx.x == 0) {
+      // report, then let the newest tile load in flight land before leaving
+      *abort_flag = 1;
+      atomicOr(p.status, kStatusTmaTimeout);
+      mbar_wait_bounded(&bars->tile_full, (tiles - 1) & 1, kWaitLimitNs);
     }
   }
 }

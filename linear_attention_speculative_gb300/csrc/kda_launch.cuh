@@ -12,8 +12,8 @@ namespace kda {
 
 struct LaunchCfg {
   int K;        // 32, 64, 128 or 256
-  int warps;    // tile kernel: warps per CTA; ws kernel: consumer warps
-  bool ws;      // warp-specialised persistent kernel
+  int warps;    // tile kernel: warps per CTA; pipelined kernel: consumer warps
+  bool pipe;    // persistent warp-specialised (pipelined) kernel
   bool decode;  // tile kernel without snapshots, final state written in place
   bool sms;     // tile kernel with the state kept in shared memory
   int grid;     // CTAs
@@ -24,8 +24,8 @@ struct LaunchCfg {
 // or -1 when no instantiation matches.
 int launch_tile_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
 int launch_tile_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
-int launch_ws_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
-int launch_ws_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+int launch_pipe_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+int launch_pipe_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
 // The q/k conv_state roll of a one-item-per-CTA launch run with
 // p.qk_roll_kernel set (kda_roll.cu), on the same stream after it.
 int launch_qk_roll(const Params& p, int K, bool bf16, cudaStream_t st);
@@ -59,12 +59,12 @@ int launch_tile_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c
 }
 
 template <typename Act, int K, int CW>
-int launch_ws_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
-  auto fn = kda_ws_kernel<Act, K, CW>;
+int launch_pipe_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
+  auto fn = kda_pipe_kernel<Act, K, CW>;
   static unsigned long long configured = 0;
   int rc = configure_once(fn, &configured);
   if (rc) return rc;
-  fn<<<cfg.grid, (CW + 1) * 32, cfg.smem, st>>>(tmap, p);
+  fn<<<cfg.grid, pipe_threads(CW), cfg.smem, st>>>(tmap, p);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -93,10 +93,10 @@ int launch_tile_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchC
 }
 
 template <typename Act>
-int launch_ws_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c, cudaStream_t st) {
+int launch_pipe_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c, cudaStream_t st) {
 #define KDA_CASE(KK, WW) \
-  if (c.K == KK && c.warps == WW) return launch_ws_one<Act, KK, WW>(tmap, p, c, st);
-#define KDA_CASES_K(KK) KDA_CASE(KK, 2) KDA_CASE(KK, 4) KDA_CASE(KK, 8)
+  if (c.K == KK && c.warps == WW) return launch_pipe_one<Act, KK, WW>(tmap, p, c, st);
+#define KDA_CASES_K(KK) KDA_CASE(KK, 4) KDA_CASE(KK, 8)
   KDA_CASES_K(32)
   KDA_CASES_K(64)
   KDA_CASES_K(128)

@@ -19,11 +19,13 @@ from . import _build
 GATE_SOFTPLUS = 0
 GATE_SAFE = 1
 VARIANT_AUTO = 0
-VARIANT_SMALL_BATCH = 1
-VARIANT_LARGE_BATCH = 2
-VARIANT_SMEM_STATE = 3
-VARIANTS = {"auto": VARIANT_AUTO, "small_batch": VARIANT_SMALL_BATCH,
-            "large_batch": VARIANT_LARGE_BATCH, "smem_state": VARIANT_SMEM_STATE}
+VARIANT_ONE_ITEM = 1
+VARIANT_PIPELINED = 2
+VARIANT_ONE_ITEM_SMEM = 3
+VARIANTS = {"auto": VARIANT_AUTO, "one_item": VARIANT_ONE_ITEM, "pipelined": VARIANT_PIPELINED,
+            "one_item_smem": VARIANT_ONE_ITEM_SMEM}
+# plan-string prefix of each variant ("item:128", "pipe:128", "smem:128")
+PLAN_PREFIX = {VARIANT_ONE_ITEM: "item", VARIANT_PIPELINED: "pipe", VARIANT_ONE_ITEM_SMEM: "smem"}
 F32 = 0
 BF16 = 1
 MAX_T = 16
@@ -185,14 +187,13 @@ QK_ROLL_AUTO, QK_ROLL_COUNTER, QK_ROLL_KERNEL = 0, 1, 2
 
 
 def parse_plan(spec: str) -> KdaPlan:
-    """'small:32' / 'large:64' / 'smem:128' / 'large:64:300' / 'small:128:0:-1' /
+    """'item:32' / 'pipe:128' / 'smem:128' / 'pipe:128:300' / 'item:128:0:-1' /
     'smem:128:0:0:kernel' (variant, v-tile width, grid, L2 prefetch distance: -1 off,
     0 default, q/k conv_state roll: 'counter' or 'kernel', default the dispatcher's)."""
     parts = spec.split(":")
     plan = KdaPlan()
-    plan.variant = {"small": VARIANT_SMALL_BATCH, "small_batch": VARIANT_SMALL_BATCH,
-                    "large": VARIANT_LARGE_BATCH, "large_batch": VARIANT_LARGE_BATCH,
-                    "smem": VARIANT_SMEM_STATE, "smem_state": VARIANT_SMEM_STATE}[parts[0]]
+    plan.variant = {"item": VARIANT_ONE_ITEM, "pipe": VARIANT_PIPELINED,
+                    "smem": VARIANT_ONE_ITEM_SMEM}[parts[0]]
     plan.bv = int(parts[1])
     plan.grid = int(parts[2]) if len(parts) > 2 else 0
     plan.prefetch = int(parts[3]) if len(parts) > 3 else 0
@@ -208,7 +209,7 @@ def conv_verify(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: s
 
     Tensors must be contiguous CUDA tensors in the layouts of the header;
     conv_state is updated in place; o / inter_ssm / conv_snapshots are
-    written.  `plan` (a KdaPlan or a 'small:32'-style string) overrides the
+    written.  `plan` (a KdaPlan or a 'item:32'-style string) overrides the
     dispatcher.  Raises KdaError on any non-zero return code."""
     if shape is None:
         shape = shape_of(mixed_qkv, a, S0)
@@ -348,3 +349,8 @@ def run(inputs: Dict[str, torch.Tensor], gate: str, variant: str = "auto",
                 out["o"], out["inter_ssm"], out["conv_snapshots"], ws, stream=stream,
                 variant=variant, shape=shape, plan=plan)
     return out
+
+
+def plan_label(plan: KdaPlan) -> str:
+    """'item:128' etc.: the plan-string prefix of the variant and the v-tile width."""
+    return f"{PLAN_PREFIX[plan.variant]}:{plan.bv}"

@@ -74,8 +74,8 @@ def to_device(inputs, device="cuda"):
 
 def run_kernel(inputs_cpu, gate, variant="auto"):
     """Copy inputs to the GPU, run one call, return (device outputs, rolled
-    conv_state on the device).  `variant` is auto / small_batch / large_batch
-    or an explicit plan such as 'small:64' or 'large:32'."""
+    conv_state on the device).  `variant` is auto / one_item / pipelined
+    or an explicit plan such as 'item:64' or 'pipe:64'."""
     from linear_attention_speculative_gb300 import kda
     dev = to_device(inputs_cpu)
     if ":" in variant:
@@ -143,19 +143,31 @@ def conv_window_properties(inputs_cpu, out, conv_state_dev):
     assert torch.equal(conv_state_dev, xext[:, :, T:T + 3]), "rolled conv_state"
 
 
-def plan_built(plan, K, V, decode=False) -> bool:
+def variant_built(variant, K, V, decode=False) -> bool:
+    """Whether a named variant runs for head dims K x V (the pipelined kernel
+    needs K <= 128, V >= 64 and no decode)."""
+    if variant == "pipelined":
+        return K <= 128 and V >= 64 and not decode
+    return True
+
+
+def plan_built(plan, K, V, decode=False, T=1, act="bf16") -> bool:
     """Whether an explicit plan string names a kernel the library builds for
     head dims K x V: one-item tiles are 1/2/4/8 warps of 16 columns (K <= 128;
     1 warp not for K = 256, whose warps hold 8 columns), the shared-memory
-    state 4 or 8 warps, the persistent kernel K <= 128 and no decode."""
+    state 4 or 8 warps, the pipelined kernel 4 or 8 consumer warps at
+    K <= 128 and no decode (T and act matter only for its shared memory)."""
     if plan in (None, "auto"):
         return True
     kind, bv = plan.split(":")[0], int(plan.split(":")[1])
     wc = 8 if K == 256 else 16
     if bv > V or V % bv:
         return False
-    if kind == "large":
-        return K <= 128 and not decode and bv in (32, 64, 128)
+    if kind == "pipe":
+        # its shared memory fits one CTA except 128-wide K = 128 tiles at
+        # T = 16 with fp32 activations
+        too_big = bv == 128 and K == 128 and T >= 16 and act == "f32"
+        return K <= 128 and not decode and bv in (64, 128) and not too_big
     if kind == "smem":
         return bv in (4 * wc, 8 * wc)
     return bv in (2 * wc, 4 * wc, 8 * wc) or (K <= 128 and bv == wc)

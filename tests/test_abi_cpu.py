@@ -62,21 +62,21 @@ def test_workspace_bytes(kda):
 def test_plan_auto_uses_one_item_per_cta(kda):
     # whole states per 8-warp CTA, one item per CTA
     p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
-    assert p.variant == kda.VARIANT_SMALL_BATCH
+    assert p.variant == kda.VARIANT_ONE_ITEM
     assert p.bv == 128 and p.warps == 8 and p.items == 256 * 32 and p.grid == p.items
     # single-token calls over many units: state kept in shared memory
     p2 = kda.make_plan(kda.make_shape(512, 1, 32, 64), 152)
-    assert p2.variant == kda.VARIANT_SMEM_STATE and p2.bv == 128 and p2.items == 512 * 64
+    assert p2.variant == kda.VARIANT_ONE_ITEM_SMEM and p2.bv == 128 and p2.items == 512 * 64
     assert p2.ctas_per_sm == 3
-    assert kda.make_plan(kda.make_shape(512, 2, 32, 64), 152).variant == kda.VARIANT_SMEM_STATE
-    assert kda.make_plan(kda.make_shape(32, 2, 32, 64), 152).variant == kda.VARIANT_SMEM_STATE
-    assert kda.make_plan(kda.make_shape(32, 2, 16, 32), 152).variant == kda.VARIANT_SMALL_BATCH
-    assert kda.make_plan(kda.make_shape(512, 3, 32, 64), 152).variant == kda.VARIANT_SMEM_STATE
-    assert kda.make_plan(kda.make_shape(128, 3, 16, 16), 152).variant == kda.VARIANT_SMALL_BATCH
+    assert kda.make_plan(kda.make_shape(512, 2, 32, 64), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
+    assert kda.make_plan(kda.make_shape(32, 2, 32, 64), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
+    assert kda.make_plan(kda.make_shape(32, 2, 16, 32), 152).variant == kda.VARIANT_ONE_ITEM
+    assert kda.make_plan(kda.make_shape(512, 3, 32, 64), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
+    assert kda.make_plan(kda.make_shape(128, 3, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     p3 = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152)
-    assert p3.variant == kda.VARIANT_SMALL_BATCH and p3.bv == 128
-    assert kda.make_plan(kda.make_shape(2, 1, 16, 16), 152).variant == kda.VARIANT_SMALL_BATCH
-    assert kda.make_plan(kda.make_shape(32, 1, 16, 32), 152).variant == kda.VARIANT_SMALL_BATCH
+    assert p3.variant == kda.VARIANT_ONE_ITEM and p3.bv == 128
+    assert kda.make_plan(kda.make_shape(2, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
+    assert kda.make_plan(kda.make_shape(32, 1, 16, 32), 152).variant == kda.VARIANT_ONE_ITEM
     # L2 prefetch 3/8 of a wave of resident CTAs ahead
     assert p.prefetch == 152 * p.ctas_per_sm * 3 // 8 > 0
 
@@ -91,8 +91,10 @@ def test_plan_picks_the_qk_roll(kda):
     # two readers, a fraction of a wave: the counter, one launch
     p = kda.make_plan(kda.make_shape(2, 1, 16, 32), 152)
     assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
-    # the persistent variant always counts
-    p = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152, "large_batch")
+    # the pipelined variant: the same choice by items per resident CTA
+    p = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152, "pipelined")
+    assert p.qk_roll == kda.QK_ROLL_KERNEL and p.launches == 2
+    p = kda.make_plan(kda.make_shape(2, 4, 16, 32), 152, "pipelined")
     assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
 
 
@@ -100,39 +102,44 @@ def test_resolve_plan_fills_derived_fields(kda):
     s = kda.make_shape(512, 1, 32, 64)
     p = kda.resolve_plan(s, 152, "smem:128:0:0:counter")
     assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1 and p.ctas_per_sm == 3
-    p = kda.resolve_plan(s, 152, "small:64")
+    p = kda.resolve_plan(s, 152, "item:64")
     assert p.qk_roll == kda.QK_ROLL_KERNEL and p.launches == 2 and p.items == 512 * 64 * 2
     with pytest.raises(kda.KdaError):
-        kda.resolve_plan(s, 152, "large:64", decode=True)
+        kda.resolve_plan(s, 152, "pipe:64", decode=True)
 
 
 def test_plan_strings_carry_the_qk_roll(kda):
-    assert kda.parse_plan("small:64").qk_roll == kda.QK_ROLL_AUTO
-    assert kda.parse_plan("small:64:0:0:kernel").qk_roll == kda.QK_ROLL_KERNEL
+    assert kda.parse_plan("item:64").qk_roll == kda.QK_ROLL_AUTO
+    assert kda.parse_plan("item:64:0:0:kernel").qk_roll == kda.QK_ROLL_KERNEL
     assert kda.parse_plan("smem:128:0:-1:counter").qk_roll == kda.QK_ROLL_COUNTER
     with pytest.raises(KeyError):
-        kda.parse_plan("small:64:0:0:sometimes")
+        kda.parse_plan("item:64:0:0:sometimes")
     # fewer units than SMs: whole states per CTA
     p1 = kda.make_plan(kda.make_shape(1, 4, 16, 16), 152)
-    assert p1.variant == kda.VARIANT_SMALL_BATCH and p1.bv == 128 and p1.warps == 8
+    assert p1.variant == kda.VARIANT_ONE_ITEM and p1.bv == 128 and p1.warps == 8
     assert p1.items == 16 and p1.grid == 16
 
 
-def test_plan_large_batch_is_persistent(kda):
-    p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152, "large_batch")
-    assert p.variant == kda.VARIANT_LARGE_BATCH
-    assert p.bv == 64 and p.warps == 4 and p.items == 256 * 32 * 2
-    assert 152 <= p.grid <= 152 * p.ctas_per_sm
-    tiny = kda.make_plan(kda.make_shape(1, 2, 1, 1), 152, "large_batch")
-    assert tiny.grid == tiny.items == 2  # never more CTAs than items
+def test_plan_pipelined_is_persistent(kda):
+    p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152, "pipelined")
+    assert p.variant == kda.VARIANT_PIPELINED and kda.plan_label(p) == "pipe:128"
+    assert p.bv == 128 and p.warps == 8 and p.items == 256 * 32
+    assert p.ctas_per_sm == 1 and p.grid == 152 and p.prefetch == 0  # inputs requested one item ahead
+    p64 = kda.resolve_plan(kda.make_shape(256, 4, 32, 32), 152, "pipe:64")
+    assert p64.warps == 4 and p64.ctas_per_sm == 2 and p64.grid == 304
+    tiny = kda.make_plan(kda.make_shape(1, 2, 1, 1), 152, "pipelined")
+    assert tiny.grid == tiny.items == 1  # never more CTAs than items
 
 
 def test_plan_small_heads(kda):
     s = kda.make_shape(8, 2, 2, 4, K=64, V=32)
-    big = kda.make_plan(s, 152, "large_batch")
-    assert big.variant == kda.VARIANT_LARGE_BATCH and big.bv == 32 and big.warps == 2
-    small = kda.make_plan(s, 152, "small_batch")
-    assert small.variant == kda.VARIANT_SMALL_BATCH and small.bv in (16, 32)
+    with pytest.raises(kda.KdaError) as e:  # the pipelined kernel needs V >= 64
+        kda.make_plan(s, 152, "pipelined")
+    assert e.value.code == -8
+    small = kda.make_plan(s, 152, "one_item")
+    assert small.variant == kda.VARIANT_ONE_ITEM and small.bv in (16, 32)
+    p = kda.make_plan(kda.make_shape(8, 2, 2, 4, K=64, V=64), 152, "pipelined")
+    assert p.variant == kda.VARIANT_PIPELINED and p.bv == 64 and p.warps == 4
 
 
 @pytest.mark.parametrize("bad", [dict(T=0), dict(T=17), dict(W=3), dict(K=96), dict(V=512),
@@ -169,7 +176,7 @@ def _call_plan(kda, shape, ptrs, plan, gate=0, ws_bytes=1 << 20):
 
 def test_rejects_invalid_plans(kda):
     s = kda.make_shape(2, 2, 2, 2, 32, 64)
-    for spec in ("small:8", "small:128", "small:48", "large:16", "large:128"):
+    for spec in ("item:8", "item:128", "item:48", "pipe:16", "pipe:32", "pipe:128"):
         assert _call_plan(kda, s, _fake_args(kda), kda.parse_plan(spec)) == -8, spec
     bad = kda.KdaPlan()
     bad.variant, bad.bv = 0, 32  # AUTO is not a concrete plan
@@ -304,25 +311,25 @@ def test_decode_rejects_bad_arguments(kda):
                                  ctypes.byref(plan) if plan is not None else None, None)
     assert call(S=None) == -1
     assert call(o=p["S0"] + 64) == -5                 # output inside the in/out state
-    assert call(plan=kda.parse_plan("large:32")) == -8
-    assert call(plan=kda.parse_plan("small:64")) == -8  # wider than V = 32
+    assert call(plan=kda.parse_plan("pipe:64")) == -8
+    assert call(plan=kda.parse_plan("item:64")) == -8  # wider than V = 32
 
 
 def test_plan_head_dim_256_layout(kda):
     # K = 256: 16 row groups x 2 column quads per warp, 8 columns per warp, so an
     # 8-warp tile is 64 columns wide
     p = kda.make_plan(kda.make_shape(64, 4, 8, 16, K=256, V=256), 152)
-    assert p.variant == kda.VARIANT_SMALL_BATCH and p.bv == 64 and p.warps == 8
+    assert p.variant == kda.VARIANT_ONE_ITEM and p.bv == 64 and p.warps == 8
     assert p.items == 64 * 16 * 4
     p1 = kda.make_plan(kda.make_shape(512, 1, 8, 16, K=256, V=256), 152)
-    assert p1.variant == kda.VARIANT_SMALL_BATCH and p1.bv == 64 and p1.warps == 8
+    assert p1.variant == kda.VARIANT_ONE_ITEM and p1.bv == 64 and p1.warps == 8
     q = kda.make_plan(kda.make_shape(64, 4, 8, 16, K=128, V=256), 152)
-    assert q.variant == kda.VARIANT_SMALL_BATCH and q.bv == 128 and q.items == 64 * 16 * 2
+    assert q.variant == kda.VARIANT_ONE_ITEM and q.bv == 128 and q.items == 64 * 16 * 2
     with pytest.raises(kda.KdaError) as e:
-        kda.make_plan(kda.make_shape(4, 2, 1, 1, K=256, V=128), 152, "large_batch")
+        kda.make_plan(kda.make_shape(4, 2, 1, 1, K=256, V=128), 152, "pipelined")
     assert e.value.code == -8
     s = kda.make_shape(2, 2, 1, 1, K=256, V=128)
-    assert kda.resolve_plan(s, 152, "small:32").warps == 4
+    assert kda.resolve_plan(s, 152, "item:32").warps == 4
     assert kda.resolve_plan(s, 152, "smem:32").warps == 4
-    for bad in ("small:128", "smem:128", "small:8", "large:64"):  # 16 warps / 1 warp / persistent: not built
+    for bad in ("item:128", "smem:128", "item:8", "pipe:64"):  # 16 warps / 1 warp / pipelined: not built
         assert _call_plan(kda, s, _fake_args(kda), kda.parse_plan(bad)) == -8, bad

@@ -34,9 +34,9 @@ def _decode(kda, inp, gate, plan=None, idx=None):
     return o
 
 
-@pytest.mark.parametrize("plan", [None, "small:128", "small:32", "small:16:0:-1", "smem:128", "smem:64",
-                                  "small:32:0:0:kernel", "smem:64:0:0:kernel", "smem:128:0:0:counter",
-                                  "small:64", "smem:32"])
+@pytest.mark.parametrize("plan", [None, "item:128", "item:32", "item:16:0:-1", "smem:128", "smem:64",
+                                  "item:32:0:0:kernel", "smem:64:0:0:kernel", "smem:128:0:0:counter",
+                                  "item:64", "smem:32"])
 @pytest.mark.parametrize("case", [(5, 4, 2, 4, 128, 128, "bf16", "softplus"),
                                   (3, 1, 2, 2, 128, 128, "bf16", "safe"),
                                   (4, 3, 1, 2, 64, 64, "f32", "softplus"),
@@ -128,5 +128,5 @@ def test_decode_rejects_persistent_plans():
     wl = wk.custom(2, 1, 2, 2, 128, 128, seed=97)
     inp = to_device(wk.make_inputs(wl))
     with pytest.raises(kda.KdaError) as e:
-        _decode(kda, inp, wl.gate, plan="large:64")
+        _decode(kda, inp, wl.gate, plan="pipe:64")
     assert e.value.code == -8

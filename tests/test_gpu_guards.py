@@ -74,14 +74,15 @@ def _verify_fenced(kda, wl, plan=None, pools=False):
 
 
 CASES = [
-    (wk.custom(5, 3, 2, 4, 128, 128, seed=401), ("small:128", "small:16", "smem:128", "large:64",
-                                                 "large:128:2", "small:128:0:0:kernel",
-                                                 "smem:128:0:0:kernel", "small:64:0:0:counter")),
-    (wk.custom(3, 2, 1, 2, 256, 256, seed=402), ("smem:64", "smem:32", "small:64", "small:16",
-                                                 "small:64:0:0:kernel")),
-    (wk.custom(4, 16, 2, 2, 32, 32, act="f32", seed=403), ("small:32", "small:16", "large:32")),
-    (wk.custom(6, 1, 3, 6, 64, 128, gate="safe", seed=404), ("small:64", "smem:64", "large:32",
-                                                              "small:64:0:0:kernel")),
+    (wk.custom(5, 3, 2, 4, 128, 128, seed=401), ("item:128", "item:16", "smem:128", "pipe:64",
+                                                 "pipe:128:2", "item:128:0:0:kernel",
+                                                 "smem:128:0:0:kernel", "item:64:0:0:counter")),
+    (wk.custom(3, 2, 1, 2, 256, 256, seed=402), ("smem:64", "smem:32", "item:64", "item:16",
+                                                 "item:64:0:0:kernel")),
+    (wk.custom(4, 16, 2, 2, 32, 32, act="f32", seed=403), ("item:32", "item:16")),
+    (wk.custom(4, 16, 2, 2, 32, 64, act="f32", seed=406), ("pipe:64", "pipe:64:1:0:counter")),
+    (wk.custom(6, 1, 3, 6, 64, 128, gate="safe", seed=404), ("item:64", "smem:64", "pipe:64",
+                                                              "item:64:0:0:kernel")),
 ]
 
 
@@ -109,7 +110,7 @@ def test_decode_and_commit_writes_stay_inside_their_buffers():
     assert S.intact() and cs.intact()
     # decode with a fenced in/out state and outputs
     inp = f["inp"]
-    for plan in ("small:128", "smem:128", "small:32"):
+    for plan in ("item:128", "smem:128", "item:32"):
         Sd = Fenced((s.N, s.HV, s.K, s.V), torch.float32, fill=inp["S0"])
         csd = Fenced((s.N, s.dim, 3), s.torch_act, fill=wk.make_inputs(wl)["conv_state"].cuda())
         o = Fenced((s.N, s.T, s.HV, s.V), s.torch_act)

@@ -17,16 +17,17 @@ import torch
 import oracle
 from linear_attention_speculative_gb300 import workloads as wk
 from parity_util import (TOL, assert_parity, conv_window_properties, max_rel_err, plan_built,
-                         rel_rmse, run_kernel, to_device)
+                         rel_rmse, run_kernel, to_device, variant_built)
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ("auto", "small_batch", "large_batch")
+VARIANTS = ("auto", "one_item", "pipelined")
 # every explicit plan of a V = 128 problem
-ALL_PLANS = ("small:16", "small:32", "small:64", "small:128", "small:128:0:-1", "small:64:0:7",
-             "large:32", "large:64", "large:128", "smem:64", "smem:128",
+ALL_PLANS = ("item:16", "item:32", "item:64", "item:128", "item:128:0:-1", "item:64:0:7",
+             "pipe:64", "pipe:128", "pipe:128:0:-1", "pipe:128:0:0:kernel", "pipe:64:0:0:counter",
+             "smem:64", "smem:128",
              # both ways of rolling a q/k conv_state that several items read
-             "small:64:0:0:counter", "small:64:0:0:kernel", "smem:128:0:0:counter",
+             "item:64:0:0:counter", "item:64:0:0:kernel", "smem:128:0:0:counter",
              "smem:128:0:0:kernel", "smem:64:0:0:kernel")
 
 
@@ -41,6 +42,8 @@ def _lib():
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("wl", [wk.TINY, wk.DECODE], ids=lambda w: w.name)
 def test_parity_full(wl, variant):
+    if not variant_built(variant, wl.shape.K, wl.shape.V):
+        pytest.skip("no such kernel for this shape")
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, wl.gate, threads=8)
     out, cs = run_kernel(inp, wl.gate, variant)
@@ -85,8 +88,8 @@ def test_large_workload_takes_the_softplus_overflow_branch():
     assert torch.isfinite(out["inter_ssm"][seqs]).all()
 
 
-def _valid_plans(V):
-    return [p for p in ALL_PLANS if int(p.split(":")[1]) <= V]
+def _valid_plans(s):
+    return [p for p in ALL_PLANS if plan_built(p, s.K, s.V, T=s.T, act=s.act)]
 
 
 @pytest.mark.parametrize("wl", [wk.DECODE, wk.GVA,
@@ -96,7 +99,7 @@ def _valid_plans(V):
                          ids=lambda w: w.name)
 def test_all_plans_bit_identical(wl):
     inp = wk.make_inputs(wl)
-    plans = _valid_plans(wl.shape.V)
+    plans = _valid_plans(wl.shape)
     ref = run_kernel(inp, wl.gate, plans[0])
     for plan in plans[1:]:
         out = run_kernel(inp, wl.gate, plan)
@@ -120,7 +123,7 @@ def test_persistent_grid_smaller_than_items():
     inp = wk.make_inputs(wl)
     seqs = [0, 17, 63]
     ref = oracle.verify(inp, wl.gate, seqs=seqs, threads=4)
-    for plan in ("large:64:3", "large:32:7", "large:128:1"):
+    for plan in ("pipe:64:3", "pipe:64:7", "pipe:128:1", "pipe:128:5:0:counter", "pipe:128:2:0:kernel"):
         out, cs = run_kernel(inp, wl.gate, plan)
         assert_parity(out, cs, ref, seqs=seqs)
         conv_window_properties(inp, out, cs)
@@ -131,7 +134,7 @@ def test_deterministic_across_repeats():
     wl = wk.GVA
     inp = wk.make_inputs(wl)
     first = None
-    for v in ("small:32", "small:128", "large:64"):
+    for v in ("item:32", "item:128", "pipe:64"):
         for _ in range(iters):
             out, cs = run_kernel(inp, wl.gate, v)
             cur = (out["o"], out["inter_ssm"], out["conv_snapshots"], cs)
@@ -142,7 +145,7 @@ def test_deterministic_across_repeats():
                     assert torch.equal(x, y)
 
 
-@pytest.mark.parametrize("variant", ("small_batch", "large_batch"))
+@pytest.mark.parametrize("variant", ("one_item", "pipelined"))
 @pytest.mark.parametrize("gate", ("softplus", "safe"))
 def test_chain_of_single_token_calls_is_bit_exact(variant, gate):
     from linear_attention_speculative_gb300 import kda
@@ -198,6 +201,8 @@ EDGE = [
 @pytest.mark.parametrize("case", EDGE, ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}".format(*c))
 def test_edge_shapes(case, variant):
     N, T, H, HV, K, V, act, gate = case
+    if not variant_built(variant, K, V):
+        pytest.skip("no such kernel for this shape")
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=N * 100 + T)
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, gate)
@@ -220,8 +225,8 @@ def test_workspace_is_left_zeroed():
     inp = to_device(wk.make_inputs(wl))
     shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
     ws = kda.alloc_workspace(shape, "cuda")
-    for v in ("small:16", "small:128", "large:32", "large:128", "small:128:0:0:counter",
-              "small:128:0:0:kernel"):
+    for v in ("item:16", "item:128", "pipe:64", "pipe:128", "item:128:0:0:counter",
+              "item:128:0:0:kernel"):
         kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate, plan=v, workspace=ws)
         torch.cuda.synchronize()
         assert int(ws.count_nonzero()) == 0
@@ -247,7 +252,7 @@ def test_side_streams_and_separate_workspaces():
         assert torch.equal(out["o"], ref["o"])
 
 
-@pytest.mark.parametrize("plan", [None, "small:128:0:0:counter", "small:128:0:0:kernel"])
+@pytest.mark.parametrize("plan", [None, "item:128:0:0:counter", "item:128:0:0:kernel"])
 def test_cuda_graph_replay(plan):
     # two v-heads per q/k head: the q/k conv_state roll runs by either protocol
     # (the roll kernel as a programmatic dependent launch inside the graph)
@@ -337,8 +342,8 @@ def test_head_dim_256(case):
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=300 + K + V + T)
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, gate)
-    plans = ["auto"] + [p for p in ("smem:32", "smem:64", "smem:128", "small:16", "small:32", "small:64",
-                                      "small:128", "large:64") if plan_built(p, K, V)]
+    plans = ["auto"] + [p for p in ("smem:32", "smem:64", "smem:128", "item:16", "item:32", "item:64",
+                                      "item:128", "pipe:64") if plan_built(p, K, V)]
     first = None
     for plan in plans:
         out, cs = run_kernel(inp, gate, plan)
@@ -362,8 +367,9 @@ def _random_cases(n=24, seed=2026):
         N = int(rng.integers(1, 7))
         act = str(rng.choice(["bf16", "f32"]))
         gate = str(rng.choice(["softplus", "safe"]))
-        plans = [p for p in ("small:16", "small:32", "small:64", "small:128", "large:32",
-                             "large:64", "smem:32", "smem:64", "smem:128") if plan_built(p, K, V)]
+        plans = [p for p in ("item:16", "item:32", "item:64", "item:128", "pipe:64",
+                             "pipe:128", "smem:32", "smem:64", "smem:128")
+                 if plan_built(p, K, V, T=T, act=act)]
         if not plans:
             continue
         plan = str(rng.choice(plans))
@@ -403,7 +409,7 @@ def test_qk_roll_kernel_and_counter_match_the_oracle(case):
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, gate)
     full = min(V, 64 if K == 256 else 128)
-    kinds = ("small", "smem") if plan_built(f"smem:{full}", K, V) else ("small",)
+    kinds = tuple(k for k in ("item", "smem", "pipe") if plan_built(f"{k}:{full}", K, V))
     outs = []
     for kind in kinds:
         bv = full
@@ -441,7 +447,7 @@ def test_extreme_activation_inputs(gate):
     b = inp["b"].float() * 50.0
     inp["b"] = b.to(inp["b"].dtype)
     ref = oracle.verify(inp, gate)
-    for plan in ("auto", "small:64", "smem:64", "small:32:0:0:kernel"):
+    for plan in ("auto", "item:64", "smem:64", "item:32:0:0:kernel"):
         out, cs = run_kernel(inp, gate, plan)
         for key in ("o", "inter_ssm"):
             assert torch.isfinite(out[key].float()).all(), (plan, key)

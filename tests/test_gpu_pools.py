@@ -64,8 +64,8 @@ def _run_indexed(kda, wl, inp, pl, plan=None):
                 idx=idx, slot=slot)
 
 
-@pytest.mark.parametrize("plan", [None, "small:128", "small:32", "large:64", "small:128:0:0:kernel",
-                                  "small:32:0:0:counter", "smem:64:0:0:kernel"])
+@pytest.mark.parametrize("plan", [None, "item:128", "item:32", "pipe:64", "item:128:0:0:kernel",
+                                  "item:32:0:0:counter", "smem:64:0:0:kernel"])
 def test_indexed_equals_dense_on_gathered_inputs(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(8, 3, 2, 4, 128, 128, seed=81)
@@ -112,7 +112,7 @@ def test_indexed_matches_the_oracle():
     assert_parity(out, cs, ref)
 
 
-@pytest.mark.parametrize("plan", [None, "small:128:0:0:counter", "small:128:0:0:kernel"])
+@pytest.mark.parametrize("plan", [None, "item:128:0:0:counter", "item:128:0:0:kernel"])
 def test_out_of_range_slot_skips_and_reports(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(4, 2, 2, 2, 128, 128, seed=83)  # two v-heads read each q/k head
