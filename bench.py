@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--sweep-out", default="")
     ap.add_argument("--sweep-filter", default="",
                     help="regular expression: only sweep points whose name matches")
+    ap.add_argument("--sweep-report", default="",
+                    help="read a --sweep-out file and print its markdown summary (no GPU)")
     ap.add_argument("--sweep-plans", default="auto,item:32,item:64,item:128,smem:128,pipe:64,pipe:128",
                     help="plans timed at every sweep point")
     return ap.parse_args()
@@ -110,9 +112,11 @@ def measured_hbm_peak():
 # kernel that each plan variant launches (ONE_ITEM, PIPELINED, ONE_ITEM_SMEM)
 KERNEL_OF_VARIANT = {1: "kda_tile_kernel", 2: "kda_pipe_kernel", 3: "kda_tile_kernel_sms"}
 
-# CUDA sources each profiled kernel is built from (the verify kernels: every
-# source but the commit kernel's own file)
+# device sources each profiled kernel is built from (host-only files such as
+# the dispatcher in kda_api.cu do not change the kernels' code)
 COMMIT_SOURCES = ("kda_commit.cu", "kda_device.cuh")
+VERIFY_SOURCES = ("kda_kernel.cuh", "kda_device.cuh", "kda_launch.cuh", "kda_inst_tile_bf16.cu",
+                  "kda_inst_tile_f32.cu", "kda_inst_pipe_bf16.cu", "kda_inst_pipe_f32.cu", "kda_roll.cu")
 
 
 def kernel_src_hash(kernel="verify"):
@@ -121,10 +125,7 @@ def kernel_src_hash(kernel="verify"):
     kernel's file, keeps the committed ncu summaries valid."""
     d = os.path.join(ROOT, "linear_attention_speculative_gb300", "csrc")
     names = sorted(os.listdir(d))
-    if kernel == "commit":
-        names = [f for f in names if f in COMMIT_SOURCES]
-    else:
-        names = [f for f in names if f != COMMIT_SOURCES[0]]
+    names = [f for f in names if f in (COMMIT_SOURCES if kernel == "commit" else VERIFY_SOURCES)]
     h = hashlib.sha256()
     for f in names:
         with open(os.path.join(d, f), encoding="utf-8") as fh:
@@ -589,6 +590,72 @@ def run_sweep(args):
                           "worst_point": worst["workload"]}))
 
 
+def sweep_report(path, peak_gbs, peak_src):
+    """Markdown summary of a --sweep-out file: per point the dispatcher's plan
+    and time, the fastest explicit plan, their ratio, the bandwidth fraction,
+    and which kernel wins where."""
+    rows = [json.loads(line) for line in open(path) if line.strip()]
+    plans = [k for k in rows[0]["us"] if k != "auto"]
+    out = []
+    out.append(f"Peak: {peak_gbs:.1f} GB/s ({peak_src}, MEASURED_PEAKS.json hbm_gbs).  Times are the median of "
+               "per-launch CUDA events with L2 flushed before each launch; GB/s = algorithmic bytes / time.")
+    out.append("")
+    out.append("| T | N | H | HV | gate | auto plan | auto us | best plan | best us | auto/best | "
+               "best GB/s | of peak | " + " | ".join(f"{p} us" for p in plans) + " |")
+    out.append("|" + "---|" * (12 + len(plans)))
+    for r in rows:
+        best = r["best"]
+        b_us = r["us"][best]
+        gbs = r["alg_bytes"] / (b_us / 1e6) / 1e9
+        out.append(f"| {r['T']} | {r['N']} | {r['H']} | {r['HV']} | {r['gate']} | {r['auto']} | "
+                   f"{r['us']['auto']:.1f} | {best} | {b_us:.1f} | {r['us']['auto'] / b_us:.3f} | "
+                   f"{gbs:.0f} | {gbs / peak_gbs:.3f} | "
+                   + " | ".join(f"{r['us'][p]:.1f}" for p in plans) + " |")
+    ratios = [r["us"]["auto"] / r["us"][r["best"]] for r in rows]
+    out.append("")
+    out.append(f"Points: {len(rows)}.  auto / best: mean {sum(ratios) / len(ratios):.4f}, "
+               f"max {max(ratios):.4f}.")
+    for lo, hi in ((1, 1), (8, 32), (128, 512)):
+        sub = [x for x, r in zip(ratios, rows) if lo <= r["N"] <= hi]
+        if sub:
+            out.append(f"- N in [{lo}, {hi}]: auto / best mean {sum(sub) / len(sub):.4f}, max {max(sub):.4f} "
+                       f"({len(sub)} points)")
+    # which kernel is fastest, by T and units (N * HV)
+    out.append("")
+    out.append("Fastest explicit plan's kernel by T (rows) and N * HV (columns); item = one item per CTA "
+               "(state in registers), smem = one item per CTA (state in shared memory), pipe = pipelined:")
+    units = sorted({r["N"] * r["HV"] for r in rows})
+    Ts = sorted({r["T"] for r in rows})
+    out.append("")
+    out.append("| T \\ N*HV | " + " | ".join(str(u) for u in units) + " |")
+    out.append("|" + "---|" * (1 + len(units)))
+    for T in Ts:
+        cells = []
+        for u in units:
+            kinds = sorted({r["best"].split(":")[0] for r in rows if r["T"] == T and r["N"] * r["HV"] == u})
+            cells.append("/".join(kinds) if kinds else "")
+        out.append(f"| {T} | " + " | ".join(cells) + " |")
+    if any(p.startswith("pipe") for p in plans):
+        pipe = [p for p in plans if p.startswith("pipe")]
+        out.append("")
+        out.append("Pipelined kernel against the dispatcher's plan (best pipe plan time / auto time; "
+                   "below 1 = pipelined faster):")
+        out.append("")
+        out.append("| T \\ N*HV | " + " | ".join(str(u) for u in units) + " |")
+        out.append("|" + "---|" * (1 + len(units)))
+        for T in Ts:
+            cells = []
+            for u in units:
+                rs = [r for r in rows if r["T"] == T and r["N"] * r["HV"] == u]
+                if not rs:
+                    cells.append("")
+                    continue
+                q = [min(r["us"][p] for p in pipe) / r["us"]["auto"] for r in rs]
+                cells.append(f"{min(q):.2f}-{max(q):.2f}" if len(q) > 1 else f"{q[0]:.2f}")
+            out.append(f"| {T} | " + " | ".join(cells) + " |")
+    return "\n".join(out)
+
+
 def run_commit(args, wl):
     """HBM bandwidth of kda_commit after one verify of the workload."""
     import torch
@@ -674,6 +741,10 @@ def run_decode(args, wl):
 
 def main():
     args = parse()
+    if args.sweep_report:
+        peak, src = measured_hbm_peak()
+        print(sweep_report(args.sweep_report, peak, src))
+        return
     if args.sweep:
         run_sweep(args)
         return

@@ -176,7 +176,12 @@ size_t kda_workspace_bytes(const kda_shape* s) {
   return (bytes + 255) / 256 * 256;
 }
 
-int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out) {
+}  // extern "C"
+
+namespace {
+
+// The dispatcher.  `decode`: plan for kda_conv_decode (one-item kernels only).
+int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool decode, kda_plan* out) {
   int rc = check_shape(s);
   if (rc) return rc;
   if (!out) return KDA_ERR_NULL;
@@ -213,9 +218,34 @@ int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan
     const long long sms_from = s->T == 1 ? 8 : (s->T == 2 ? 12 : (s->T == 3 ? 24 : 0));
     if (s->K <= 128 && full_bv == 128 && sms_from > 0 && units >= sms_from * num_sms)
       out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
+    // Small batches: the pipelined kernel, whose producer warps work from
+    // inputs staged by bulk copies, measured faster on the 150-point sweep
+    // with at most half a unit per SM (64-column items, -11..15 % at T >= 2)
+    // and with at most one unit per SM from T = 4 on (128-column items,
+    // -8..11 %); from about two units per SM on the one-item kernels win.
+    if (!decode && s->K <= 128 && s->V >= 128) {
+      kda_plan pipe;
+      std::memset(&pipe, 0, sizeof(pipe));
+      pipe.variant = KDA_VARIANT_PIPELINED;
+      pipe.bv = 0;
+      if (2 * units <= num_sms) pipe.bv = 4 * kda::warp_cols(s->K);
+      else if (s->T >= 4 && units <= num_sms) pipe.bv = 8 * kda::warp_cols(s->K);
+      if (pipe.bv && valid_plan(&pipe, s, false)) {
+        out->variant = KDA_VARIANT_PIPELINED;
+        out->bv = pipe.bv;
+      }
+    }
   }
   finish_plan(s, num_sms, out, 0, 0, KDA_QK_ROLL_AUTO);
   return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out) {
+  return make_plan_impl(s, num_sms, variant, false, out);
 }
 
 int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan) {
@@ -543,7 +573,7 @@ int kda_conv_decode(const kda_shape* s, const kda_state_indices* idx, const void
     p = *plan;
     finish_plan(s, num_sms, &p, plan->grid, plan->prefetch, plan->qk_roll);
   } else {
-    rc = kda_make_plan(s, num_sms, KDA_VARIANT_AUTO, &p);
+    rc = make_plan_impl(s, num_sms, KDA_VARIANT_AUTO, true, &p);
     if (rc) return rc;
   }
   return launch_plan(s, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S, gate_mode, o,

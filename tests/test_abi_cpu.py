@@ -75,8 +75,9 @@ def test_plan_auto_uses_one_item_per_cta(kda):
     assert kda.make_plan(kda.make_shape(128, 3, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     p3 = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152)
     assert p3.variant == kda.VARIANT_ONE_ITEM and p3.bv == 128
-    assert kda.make_plan(kda.make_shape(2, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
+    assert kda.make_plan(kda.make_shape(8, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     assert kda.make_plan(kda.make_shape(32, 1, 16, 32), 152).variant == kda.VARIANT_ONE_ITEM
+    assert kda.make_plan(kda.make_shape(16, 4, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     # L2 prefetch 3/8 of a wave of resident CTAs ahead
     assert p.prefetch == 152 * p.ctas_per_sm * 3 // 8 > 0
 
@@ -114,10 +115,27 @@ def test_plan_strings_carry_the_qk_roll(kda):
     assert kda.parse_plan("smem:128:0:-1:counter").qk_roll == kda.QK_ROLL_COUNTER
     with pytest.raises(KeyError):
         kda.parse_plan("item:64:0:0:sometimes")
-    # fewer units than SMs: whole states per CTA
-    p1 = kda.make_plan(kda.make_shape(1, 4, 16, 16), 152)
-    assert p1.variant == kda.VARIANT_ONE_ITEM and p1.bv == 128 and p1.warps == 8
-    assert p1.items == 16 and p1.grid == 16
+    # fewer units than SMs at K = 256 (no pipelined kernel): whole states per CTA
+    p1 = kda.make_plan(kda.make_shape(1, 4, 16, 16, K=256, V=256), 152)
+    assert p1.variant == kda.VARIANT_ONE_ITEM and p1.bv == 64 and p1.warps == 8
+    assert p1.items == 64 and p1.grid == 64
+
+
+def test_plan_small_batches_use_the_pipelined_kernel(kda):
+    # at most half a unit per SM: 64-column items of the pipelined kernel
+    for T in (1, 2, 4, 8):
+        p = kda.make_plan(kda.make_shape(1, T, 16, 16), 152)
+        assert kda.plan_label(p) == "pipe:64" and p.items == 32 and p.grid == 32
+    p = kda.make_plan(kda.make_shape(2, 4, 32, 32), 152)  # 64 units
+    assert kda.plan_label(p) == "pipe:64"
+    # at most one unit per SM from T = 4 on: 128-column items
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 4, 16, 16), 152)) == "pipe:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 8, 16, 16), 152)) == "pipe:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 2, 16, 16), 152)) == "item:128"
+    # more units, K = 256 or V = 64: one item per CTA
+    assert kda.plan_label(kda.make_plan(kda.make_shape(16, 4, 16, 16), 152)) == "item:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 4, 1, 2, K=256, V=256), 152)) == "item:64"
+    assert kda.make_plan(kda.make_shape(1, 4, 1, 2, K=64, V=64), 152).variant == kda.VARIANT_ONE_ITEM
 
 
 def test_plan_pipelined_is_persistent(kda):

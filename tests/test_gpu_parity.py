@@ -129,20 +129,44 @@ def test_persistent_grid_smaller_than_items():
         conv_window_properties(inp, out, cs)
 
 
-def test_deterministic_across_repeats():
-    iters = int(os.environ.get("KDA_DET_ITERS", "20"))
-    wl = wk.GVA
-    inp = wk.make_inputs(wl)
+# Repeated launches must give the same bits every time (no race between the
+# items that share a q/k group, in either roll protocol, nor between the
+# pipelined kernel's producer and consumer warps).  KDA_DET_ITERS sets the
+# repeats per case (default 300; the verify-decode page stress-tested 1e5).
+DET_CASES = [
+    (wk.LARGE, "auto"),                        # single reader per q/k group
+    (wk.GVA, "item:128:0:0:counter"),          # four readers, last-arrival counter
+    (wk.GVA, "item:128:0:0:kernel"),           # four readers, second roll kernel
+    (wk.GVA, "pipe:128:0:0:counter"),          # pipelined kernel, counter
+    (wk.DECODE, "item:32"),                    # four v-tiles per state read q/k
+]
+
+
+@pytest.mark.parametrize("wl,plan", DET_CASES, ids=lambda c: c if isinstance(c, str) else c.name)
+def test_deterministic_across_repeats(wl, plan):
+    from linear_attention_speculative_gb300 import kda
+    iters = int(os.environ.get("KDA_DET_ITERS", "300"))
+    inp = to_device(wk.make_inputs(wl))
+    shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
+    ws = kda.alloc_workspace(shape, "cuda")
+    cs0 = inp["conv_state"].clone()
+    out = {k: v.cuda() for k, v in wk.empty_outputs(wl).items()}
     first = None
-    for v in ("item:32", "item:128", "pipe:64"):
-        for _ in range(iters):
-            out, cs = run_kernel(inp, wl.gate, v)
-            cur = (out["o"], out["inter_ssm"], out["conv_snapshots"], cs)
-            if first is None:
-                first = cur
-            else:
-                for x, y in zip(first, cur):
-                    assert torch.equal(x, y)
+    for i in range(iters):
+        inp["conv_state"].copy_(cs0)
+        kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
+                        inp["dt_bias"], inp["a"], inp["b"], inp["S0"], wl.gate, out["o"],
+                        out["inter_ssm"], out["conv_snapshots"], ws, shape=shape,
+                        plan=None if plan == "auto" else plan)
+        cur = (out["o"], out["inter_ssm"], out["conv_snapshots"], inp["conv_state"])
+        if first is None:
+            first = tuple(t.clone() for t in cur)
+        else:
+            # compared on the device, every element, every repeat
+            for name, x, y in zip(("o", "inter_ssm", "conv_snapshots", "conv_state"), first, cur):
+                assert torch.equal(x, y), f"repeat {i}: {name} differs"
+    assert kda.read_status(shape, ws) == 0
+    assert int(ws.count_nonzero()) == 0
 
 
 @pytest.mark.parametrize("variant", ("one_item", "pipelined"))
