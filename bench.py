@@ -138,18 +138,20 @@ def kernel_src_hash(kernel="verify"):
 
 
 def ncu_traffic(wl_name, kernel_tag):
-    """DRAM bytes per launch from the committed ncu summary of this kernel
-    (profiles/ncu_<kernel_tag>_<workload>.md), or None when absent or taken on
-    other kernel sources."""
+    """DRAM bytes per launch (total, read, write) from the committed ncu summary
+    of this kernel (profiles/ncu_<kernel_tag>_<workload>.md), or Nones when
+    absent or taken on other kernel sources."""
+    none = (None, None, None)
     path = os.path.join(ROOT, "profiles", f"ncu_{kernel_tag}_{wl_name}.md")
     if not os.path.exists(path):
-        return None
+        return none
     text = open(path).read()
-    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"kernel_src_sha256:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_src_hash():
-        return None
-    return float(m.group(1))
+    if not h or h.group(1) != kernel_src_hash():
+        return none
+    get = lambda key: (lambda m: float(m.group(1)) if m else None)(
+        re.search(key + r":\s*([0-9.eE+]+)", text))
+    return get("dram_bytes_per_launch"), get("dram_bytes_read_per_launch"), get("dram_bytes_write_per_launch")
 
 
 class ClockSampler:
@@ -482,6 +484,7 @@ def run_ours(args, wl):
     if args.plan:
         plan = kda.resolve_plan(shape, torch.cuda.get_device_properties(dev).multi_processor_count,
                                 args.plan)
+    traffic = ncu_traffic(wl.name, KERNEL_OF_VARIANT[plan.variant])
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True,
@@ -497,7 +500,10 @@ def run_ours(args, wl):
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": ncu_traffic(wl.name, KERNEL_OF_VARIANT[plan.variant]),
+                     "traffic": traffic[0], "traffic_read": traffic[1], "traffic_write": traffic[2],
+                     "traffic_source": ("one-pass ncu capture of the same launch, steady state "
+                                        f"(profiles/ncu_{KERNEL_OF_VARIANT[plan.variant]}_{wl.name}.md)"
+                                        if traffic[0] is not None else "no current capture"),
                      "algorithmic_bytes_per_launch": alg_bytes,
                      "peak_source": f"{peak_src} (hbm_gbs, STREAM-style copy)",
                      "kernel": KERNEL_OF_VARIANT[plan.variant]},
