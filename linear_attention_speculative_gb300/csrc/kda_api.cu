@@ -220,10 +220,11 @@ int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool de
       out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
     // Small batches: the pipelined kernel, whose producer warps work from
     // inputs staged by bulk copies, measured faster on the 150-point sweep
-    // with at most half a unit per SM (64-column items, -11..15 % at T >= 2)
-    // and with at most one unit per SM from T = 4 on (128-column items,
-    // -8..11 %); from about two units per SM on the one-item kernels win.
-    if (!decode && s->K <= 128 && s->V >= 128) {
+    // with at most half a unit per SM from T = 2 on (64-column items, up to
+    // -15 %) and with at most one unit per SM from T = 4 on (128-column
+    // items, up to -8 %); single-token calls of a few units and batches from
+    // about two units per SM on run faster on the one-item kernels.
+    if (!decode && s->K <= 128 && s->V >= 128 && s->T >= 2) {
       kda_plan pipe;
       std::memset(&pipe, 0, sizeof(pipe));
       pipe.variant = KDA_VARIANT_PIPELINED;

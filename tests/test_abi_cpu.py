@@ -122,10 +122,11 @@ def test_plan_strings_carry_the_qk_roll(kda):
 
 
 def test_plan_small_batches_use_the_pipelined_kernel(kda):
-    # at most half a unit per SM: 64-column items of the pipelined kernel
-    for T in (1, 2, 4, 8):
+    # at most half a unit per SM from T = 2 on: 64-column items of the pipelined kernel
+    for T in (2, 4, 8):
         p = kda.make_plan(kda.make_shape(1, T, 16, 16), 152)
         assert kda.plan_label(p) == "pipe:64" and p.items == 32 and p.grid == 32
+    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)) == "item:128"
     p = kda.make_plan(kda.make_shape(2, 4, 32, 32), 152)  # 64 units
     assert kda.plan_label(p) == "pipe:64"
     # at most one unit per SM from T = 4 on: 128-column items
