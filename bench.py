@@ -577,6 +577,11 @@ def run_sweep(args):
                "us": {}}
         for spec in plans:
             plan = None if spec == "auto" else spec
+            if plan is not None:
+                try:  # a plan the library does not build for this point is left out
+                    kda.resolve_plan(shape, sms, plan)
+                except kda.KdaError:
+                    continue
 
             def step():
                 kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"],
@@ -623,7 +628,9 @@ def sweep_report(path, peak_gbs, peak_src):
     and time, the fastest explicit plan, their ratio, the bandwidth fraction,
     and which kernel wins where."""
     rows = [json.loads(line) for line in open(path) if line.strip()]
-    plans = [k for k in rows[0]["us"] if k != "auto"]
+    plans = []
+    for r in rows:
+        plans += [k for k in r["us"] if k != "auto" and k not in plans]
     out = []
     out.append(f"Peak: {peak_gbs:.1f} GB/s ({peak_src}, MEASURED_PEAKS.json hbm_gbs).  Times are the median of "
                "per-launch CUDA events with L2 flushed before each launch (258 MB written, then 258 MB read); "
@@ -639,7 +646,7 @@ def sweep_report(path, peak_gbs, peak_src):
         out.append(f"| {r['T']} | {r['N']} | {r['H']} | {r['HV']} | {r['gate']} | {r['auto']} | "
                    f"{r['us']['auto']:.1f} | {best} | {b_us:.1f} | {r['us']['auto'] / b_us:.3f} | "
                    f"{gbs:.0f} | {gbs / peak_gbs:.3f} | "
-                   + " | ".join(f"{r['us'][p]:.1f}" for p in plans) + " |")
+                   + " | ".join(f"{r['us'][p]:.1f}" if p in r["us"] else "—" for p in plans) + " |")
     ratios = [r["us"]["auto"] / r["us"][r["best"]] for r in rows]
     out.append("")
     out.append(f"Points: {len(rows)}.  auto / best: mean {sum(ratios) / len(ratios):.4f}, "
@@ -652,7 +659,8 @@ def sweep_report(path, peak_gbs, peak_src):
     # which kernel is fastest, by T and units (N * HV)
     out.append("")
     out.append("Fastest explicit plan's kernel by T (rows) and N * HV (columns); item = one item per CTA "
-               "(state in registers), smem = one item per CTA (state in shared memory), pipe = pipelined:")
+               "(state in registers), smem = one item per CTA (state in shared memory), pipe = pipelined, "
+               "split = prep kernel + recurrence kernel:")
     units = sorted({r["N"] * r["HV"] for r in rows})
     Ts = sorted({r["T"] for r in rows})
     out.append("")
@@ -664,22 +672,25 @@ def sweep_report(path, peak_gbs, peak_src):
             kinds = sorted({r["best"].split(":")[0] for r in rows if r["T"] == T and r["N"] * r["HV"] == u})
             cells.append("/".join(kinds) if kinds else "")
         out.append(f"| {T} | " + " | ".join(cells) + " |")
-    if any(p.startswith("pipe") for p in plans):
-        pipe = [p for p in plans if p.startswith("pipe")]
+    for kind, what in (("pipe", "Pipelined kernel"), ("split", "Split variant (prep kernel + recurrence kernel)")):
+        mine = [p for p in plans if p.startswith(kind + ":")]
+        if not mine:
+            continue
         out.append("")
-        out.append("Pipelined kernel against the dispatcher's plan (best pipe plan time / auto time; "
-                   "below 1 = pipelined faster):")
+        out.append(f"{what} against the dispatcher's plan (its best plan's time / auto time; "
+                   "below 1 = faster than the dispatcher's pick):")
         out.append("")
         out.append("| T \\ N*HV | " + " | ".join(str(u) for u in units) + " |")
         out.append("|" + "---|" * (1 + len(units)))
         for T in Ts:
             cells = []
             for u in units:
-                rs = [r for r in rows if r["T"] == T and r["N"] * r["HV"] == u]
+                rs = [r for r in rows if r["T"] == T and r["N"] * r["HV"] == u
+                      and any(p in r["us"] for p in mine)]
                 if not rs:
                     cells.append("")
                     continue
-                q = [min(r["us"][p] for p in pipe) / r["us"]["auto"] for r in rs]
+                q = [min(r["us"][p] for p in mine if p in r["us"]) / r["us"]["auto"] for r in rs]
                 cells.append(f"{min(q):.2f}-{max(q):.2f}" if len(q) > 1 else f"{q[0]:.2f}")
             out.append(f"| {T} | " + " | ".join(cells) + " |")
     return "\n".join(out)

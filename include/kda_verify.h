@@ -62,8 +62,16 @@ typedef enum {
                                     next item (conv, norms, gate) while consumer warps write the
                                     current item's snapshots; the next state tile arrives by TMA
                                     meanwhile.  4 or 8 consumer warps, K <= 128 */
-  KDA_VARIANT_ONE_ITEM_SMEM = 3  /* one item per CTA, the state kept in shared memory instead
+  KDA_VARIANT_ONE_ITEM_SMEM = 3, /* one item per CTA, the state kept in shared memory instead
                                     of registers (more CTAs per SM; 4 or 8 warps) */
+  KDA_VARIANT_SPLIT = 4          /* two kernels: a prep kernel runs the conv / norm / gate work
+                                    once per (sequence, q/k head) and rolls conv_state; the
+                                    recurrence kernel, its programmatic dependent, issues its
+                                    state-tile load first, then reads the item's staged q, k,
+                                    alpha, v, beta and writes the snapshots (one item per CTA,
+                                    2, 4 or 8 warps, K <= 128).  The stages travel through each
+                                    item's own inter_ssm slice of the last token, which the
+                                    recurrence overwrites: no workspace beyond the usual */
 } kda_variant;
 
 /* Problem shape.  Supported: T in [1, KDA_MAX_T] (N == 0 is a no-op),
@@ -91,7 +99,7 @@ typedef struct {
    * requests every input one item ahead itself and ignores it (0). */
   int prefetch;
   /* When G * (V / bv) > 1 items read the same q/k channels: who rolls their
-   * conv_state.  KDA_QK_ROLL_COUNTER: the last of those items to arrive on a
+   * conv_state (0 for SPLIT, whose first kernel rolls every channel).  KDA_QK_ROLL_COUNTER: the last of those items to arrive on a
    * counter in the workspace, inside the verify kernel (one launch).
    * KDA_QK_ROLL_KERNEL: a second, small kernel launched after the verify
    * kernel on the same stream (no atomics in the verify kernel; faster on
@@ -314,7 +322,9 @@ int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan
  * width, at most V and dividing V: 1, 2, 4 or 8 warps of 16 columns for
  * ONE_ITEM, 4 or 8 for ONE_ITEM_SMEM -- at K = 256 warps of 8 columns, and 2,
  * 4 or 8 of them for ONE_ITEM; 64 or 128 for PIPELINED, whose shared memory
- * must also fit one CTA: at T = 16 with fp32 activations only 64), for
+ * must also fit one CTA: at T = 16 with fp32 activations only 64; 32, 64 or
+ * 128 for SPLIT, as long as the item's stage fits its K x bv slice, e.g. at
+ * K = 128 and bv = 32 up to T = 7), for
  * PIPELINED grid (persistent CTAs; <= 0 picks one wave of resident CTAs),
  * prefetch and qk_roll (see kda_plan).  The other fields are recomputed.  An invalid plan
  * returns KDA_ERR_VARIANT.  Every plan produces bit-identical outputs. */

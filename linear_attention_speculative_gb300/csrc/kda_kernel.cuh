@@ -873,6 +873,47 @@ __device__ __forceinline__ void consume_smem(const Params& p, const Item& it, co
 }
 
 // ---------------------------------------------------------------------------
+// split variant: the stage of an item travels from the prep kernel to the
+// recurrence kernel inside the item's own snapshot of the last token
+// ---------------------------------------------------------------------------
+// The stage (q, k, alpha [T][KS], v [T][BV], beta [round4(T)], the layout the
+// consumer reads) is kept in the first rows of the K x BV slice that the item
+// later overwrites with its state after token T-1: stage float s at row
+// s / BV, column s % BV.  The item's CTA reads it all into shared memory
+// before a barrier and only then writes any snapshot.  The host checks that
+// stage_floats(T, K, BV) <= K * BV.
+template <int K, int BV>
+__device__ __forceinline__ float* stage_home(const Params& p, const Item& it) {
+  return p.inter_ssm + (((size_t)it.im_row * p.T + p.T - 1) * p.HV + it.hv) * (size_t)K * p.V +
+         (size_t)it.vt * BV;
+}
+
+// Copy the item's stage from its home into shared memory (16-byte pieces).
+template <int K, int BV>
+__device__ __forceinline__ void copy_stage_in(const Params& p, const Item& it, float* stage, int tid,
+                                              int nthr) {
+  const float* home = stage_home<K, BV>(p, it);
+  const int n4 = stage_floats(p.T, K, BV) / 4;
+  for (int i = tid; i < n4; i += nthr) {
+    const int sidx = 4 * i;
+    *reinterpret_cast<float4*>(stage + sidx) =
+        __ldcg(reinterpret_cast<const float4*>(home + (size_t)(sidx / BV) * p.V + (sidx % BV)));
+  }
+}
+
+// L2 prefetch of item `itm`'s state tile only (the recurrence kernel of the
+// split variant reads no raw inputs).
+template <int K, int BV>
+__device__ __forceinline__ void prefetch_tile_l2(const Params& p, const CUtensorMap* tmap, long long itm,
+                                                 int lane) {
+  constexpr int BOX = tile_box_cols(BV);
+  const Item it = decode_item(p, itm);
+  if (it.skip) return;
+  for (int bx = lane; bx < BV / BOX; bx += 32)
+    tma_prefetch_2d(tmap, it.vt * BV + bx * BOX, static_cast<int>(it.s_unit * K));
+}
+
+// ---------------------------------------------------------------------------
 // one item per CTA: every warp produces, then consumes
 // ---------------------------------------------------------------------------
 // SMS: keep S in the shared-memory tile (consume_smem) instead of registers;
@@ -881,7 +922,11 @@ __host__ __device__ constexpr int tile_min_blocks(int warps, bool sms) {
   return sms ? 24 / warps : 16 / warps;
 }
 
-template <typename Act, int K, int WARPS, bool DEC = false, bool SMS = false>
+// PRE: the recurrence kernel of the split variant -- the stage comes from the
+// prep kernel (through the item's home), which also wrote the conv snapshots
+// and rolled the conv_state; launched as its programmatic dependent, the CTA
+// issues its state-tile load before waiting for the prep kernel.
+template <typename Act, int K, int WARPS, bool DEC = false, bool SMS = false, bool PRE = false>
 __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     kda_tile_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
   constexpr int BV = WARPS * warp_cols(K);
@@ -910,7 +955,7 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   if (item >= p.num_items) return;
   const Item it = decode_item(p, item);
   if (it.skip) {  // padding sequence: nothing to read or write
-    if (it.bad && tid == 0 && it.hv == 0 && it.vt == 0) atomicOr(p.status, kStatusBadIndex);
+    if (!PRE && it.bad && tid == 0 && it.hv == 0 && it.vt == 0) atomicOr(p.status, kStatusBadIndex);
     return;
   }
 
@@ -921,19 +966,29 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     mbar_arrive_expect_tx(mbar, K * BV * sizeof(float));
     tma_load_tile<K, BV>(sbuf, &tmap_s0, it.vt, it.s_unit, mbar, l2_policy_evict_first());
   }
-  if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items)
-    prefetch_item_l2<Act, K, BV>(p, &tmap_s0, item + p.prefetch, lane);
-  const GlobalSrc<Act, K, BV> src{p, it};
-  produce_tasks<Act, K, BV, DEC, SMS>(src, p, it, sQ, sK, sA, sV, sB, sRoll, tid, NT);
-  __syncthreads();  // every conv_state read of this CTA is done, stage written
-  for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
+  if (warp == WARPS - 1 && p.prefetch > 0 && item + p.prefetch < p.num_items) {
+    if constexpr (PRE) prefetch_tile_l2<K, BV>(p, &tmap_s0, item + p.prefetch, lane);
+    else prefetch_item_l2<Act, K, BV>(p, &tmap_s0, item + p.prefetch, lane);
+  }
+  if constexpr (PRE) {
+    // the prep kernel has completed and its writes are visible
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    copy_stage_in<K, BV>(p, it, sQ, tid, NT);
+    __syncthreads();  // the stage is in shared memory before any snapshot overwrites its home
+  } else {
+    const GlobalSrc<Act, K, BV> src{p, it};
+    produce_tasks<Act, K, BV, DEC, SMS>(src, p, it, sQ, sK, sA, sV, sB, sRoll, tid, NT);
+    __syncthreads();  // every conv_state read of this CTA is done, stage written
+    for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
+  }
   // Arrival on the q/k group counter by lane 0 of the last warp, after its
   // own rows (none while 2T < WARPS).  The returned count is first used at
   // the end of the CTA, so nothing waits here for the atomic's round trip.
-  // With the separate roll kernel there is no arrival and no q/k roll here.
+  // With the separate roll kernel there is no arrival and no q/k roll here;
+  // in the split variant the prep kernel rolls.
   constexpr int kRollWarp = WARPS - 1;
   const int expected = p.G * p.nvt;
-  const bool counted = expected > 1 && !p.qk_roll_kernel;
+  const bool counted = !PRE && expected > 1 && !p.qk_roll_kernel;
   int* cnt = p.counters + (size_t)it.n * p.H + it.h;
   int arrival = 0;
   if (warp == kRollWarp && lane == 0 && counted) {
@@ -956,6 +1011,7 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     load_tile<K, BV>(sbuf, s, warp, lane);
     consume<Act, K, BV, DEC>(p, it, sQ, sK, sA, sV, sB, s, warp, lane);
   }
+  if constexpr (PRE) return;
   constexpr int NQV = 2 * K / ActT<Act>::VEC;  // q/k channel vectors
   constexpr int NCV = NQV + BV / ActT<Act>::VEC;
   roll_staged<Act, K, BV>(p, it, sRoll, NQV, NCV, tid, NT);  // v: owned by this item
@@ -970,6 +1026,162 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
       __syncwarp();
       roll_staged<Act, K, BV>(p, it, sRoll, 0, NQV, lane, 32);
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// split variant, first kernel: the producer arithmetic of one q/k group
+// ---------------------------------------------------------------------------
+// One CTA per (sequence n, q/k head h): the conv + SiLU of the group's q and k
+// channels and of the v channels of its G v-heads, their gates and betas, the
+// q/k norms -- once per group instead of once per item that reads them; the
+// conv snapshots and the rolled conv_state of all those channels (the group
+// owns them: no other CTA reads them); then every item's stage (G v-heads x
+// V / BV tiles), assembled from shared memory, written to its home.  The
+// recurrence kernel, a programmatic dependent of this one, reads the stages.
+constexpr int kPrepThreads = 256;
+
+// floats of the prep kernel's shared staging: q, k [2][T][KS], alpha
+// [G][T][KS], v [G][T][V], beta [G][round4(T)]; then the staged windows
+__host__ __device__ constexpr size_t prep_stage_floats(int T, int K, int V, int G) {
+  return (size_t)(2 + G) * T * stage_ks(K) + (size_t)G * T * V + (size_t)G * round4(T);
+}
+__host__ __device__ constexpr size_t prep_smem_bytes(int T, int K, int V, int G, int ab) {
+  return sizeof(float) * prep_stage_floats(T, K, V, G) + (size_t)(2 * K + G * V) * 3 * ab;
+}
+
+template <typename Act, int K, int BV>
+__global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(const Params p) {
+  using AT = ActT<Act>;
+  constexpr int VEC = AT::VEC;
+  constexpr int NQ = K / VEC;  // q (or k) channel vectors
+  constexpr int KS = stage_ks(K);
+  const int T = p.T, G = p.G, V = p.V;
+  const int NVV = V / VEC;     // v channel vectors of one v-head
+  const int NCV = 2 * NQ + G * NVV;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  // the recurrence kernel may be scheduled once every CTA here has started
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int n = blockIdx.x / p.H;
+  const int h = blockIdx.x - n * p.H;
+  if (n >= p.N) return;
+  // slots of sequence n from the group's first item
+  const Item base = decode_item(p, ((long long)n * p.HV + (long long)h * G) * p.nvt);
+  if (base.skip) {
+    if (base.bad && h == 0 && tid == 0) atomicOr(p.status, kStatusBadIndex);
+    return;
+  }
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* sQK = reinterpret_cast<float*>(smem);   // [2][T][KS]: q tokens, then k tokens
+  float* sA = sQK + 2 * T * KS;                  // [G][T][KS]
+  float* sV = sA + (size_t)G * T * KS;           // [G][T][V]
+  float* sB = sV + (size_t)G * T * V;            // [G][round4(T)]
+  uint4* stash = reinterpret_cast<uint4*>(sB + (size_t)G * round4(T));  // [NCV][3]
+
+  // one task per (channel vector, token), then one per (v-head, 8 gate
+  // channels, token); the gate tasks start on a warp boundary when the
+  // threads outnumber the tasks (as in produce_tasks)
+  const int n_conv = NCV * T;
+  const int n_gate = G * NQ * T;
+  const int gate0 = (n_conv + 31) & ~31;
+  const bool spread = gate0 + n_gate <= kPrepThreads;
+  const int n_slots = spread ? gate0 + n_gate : n_conv + n_gate;
+  for (int slot = tid; slot < n_slots; slot += kPrepThreads) {
+    int task = slot;
+    if (spread && slot >= n_conv) {
+      if (slot < gate0) continue;
+      task = n_conv + (slot - gate0);
+    }
+    if (task < n_conv) {
+      const int cv = task / T;
+      const int t = task - cv * T;
+      const int kind = cv < NQ ? 0 : (cv < 2 * NQ ? 1 : 2);
+      const int g = kind == 2 ? (cv - 2 * NQ) / NVV : 0;
+      const int e0 = kind == 2 ? (cv - 2 * NQ - g * NVV) * VEC : (cv - kind * NQ) * VEC;
+      Item itg = base;
+      itg.hv = h * G + g;
+      itg.vt = 0;
+      const GlobalSrc<Act, K, BV> src{p, itg};
+      const int c = block_channel<K, BV>(p, itg, kind) + e0;
+      float y[VEC];
+      conv_task_unpacked<Act>(src, p, itg, kind, e0, c, t, y, true, false,
+                              t == T - 1 ? stash + 3 * cv : nullptr);
+      if (kind == 2) {
+        float* dst = sV + ((size_t)g * T + t) * V + e0;
+#pragma unroll
+        for (int e = 0; e < VEC; e += 4)
+          *reinterpret_cast<float4*>(dst + e) = make_float4(y[e], y[e + 1], y[e + 2], y[e + 3]);
+      } else {
+        float* dst = sQK + ((size_t)kind * T + t) * KS;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) dst[stage_pos<K>(e0 + e)] = y[e];
+      }
+    } else {
+      const int gi = task - n_conv;        // (g, t, e0) with e0 fastest
+      const int g = gi / (NQ * T);
+      const int r = gi - g * NQ * T;
+      const int t = r / NQ;
+      const int e0 = (r - t * NQ) * VEC;
+      Item itg = base;
+      itg.hv = h * G + g;
+      itg.vt = 0;
+      const GlobalSrc<Act, K, BV> src{p, itg};
+      const float braw = e0 == 0 ? load_b<Act>(p, itg, t) : 0.0f;  // issued before the gate math
+      const float negA = p.gate_mode != 0 ? 0.0f : -expf(__ldg(p.A_log + itg.hv));
+      float al[VEC];
+      gate_task<Act>(src, p.gate_mode, negA, t, e0, al);
+      float* dst = sA + ((size_t)g * T + t) * KS;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) dst[stage_pos<K>(e0 + e)] = al[e];
+      if (e0 == 0) sB[(size_t)g * round4(T) + t] = sigmoid_f(braw);
+    }
+  }
+  __syncthreads();  // every conv_state read of the group is done; staging complete
+  for (int r = warp; r < 2 * T; r += kPrepThreads / 32) l2norm_warp<K>(sQK + (size_t)r * KS, r < T, lane);
+  // roll the group's conv_state to the staged windows
+  for (int cv = tid; cv < NCV; cv += kPrepThreads) {
+    const int kind = cv < NQ ? 0 : (cv < 2 * NQ ? 1 : 2);
+    const int g = kind == 2 ? (cv - 2 * NQ) / NVV : 0;
+    const int e0 = kind == 2 ? (cv - 2 * NQ - g * NVV) * VEC : (cv - kind * NQ) * VEC;
+    Item itg = base;
+    itg.hv = h * G + g;
+    itg.vt = 0;
+    const int c = block_channel<K, BV>(p, itg, kind) + e0;
+    char* cp = reinterpret_cast<char*>(static_cast<Act*>(p.conv_state) +
+                                       ((size_t)base.cs_row * p.dim + c) * (kConvW - 1));
+#pragma unroll
+    for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, stash[3 * cv + m]);
+  }
+  __syncthreads();  // norms done
+  // every item's stage, at its home: item (g, vt) of the group
+  const int SF4 = stage_floats(T, K, BV) / 4;
+  const int nitems = G * p.nvt;
+  const int qk4 = 2 * T * KS / 4, a4 = T * KS / 4, v4 = T * BV / 4;
+  for (int i = tid; i < nitems * SF4; i += kPrepThreads) {
+    const int j = i / SF4;
+    const int s4 = i - j * SF4;
+    const int g = j / p.nvt;
+    const int vt = j - g * p.nvt;
+    const float* src;
+    if (s4 < qk4) {
+      src = sQK + 4 * s4;
+    } else if (s4 < qk4 + a4) {
+      src = sA + (size_t)g * T * KS + 4 * (s4 - qk4);
+    } else if (s4 < qk4 + a4 + v4) {
+      const int idx = 4 * (s4 - qk4 - a4);
+      const int t = idx / BV;
+      src = sV + ((size_t)g * T + t) * V + vt * BV + (idx - t * BV);
+    } else {
+      src = sB + (size_t)g * round4(T) + 4 * (s4 - qk4 - a4 - v4);
+    }
+    Item itg = base;
+    itg.hv = h * G + g;
+    itg.vt = vt;
+    float* home = stage_home<K, BV>(p, itg);
+    const int sidx = 4 * s4;
+    *reinterpret_cast<float4*>(home + (size_t)(sidx / BV) * V + (sidx % BV)) =
+        *reinterpret_cast<const float4*>(src);
   }
 }
 

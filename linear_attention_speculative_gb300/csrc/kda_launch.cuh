@@ -16,6 +16,7 @@ struct LaunchCfg {
   bool pipe;    // persistent warp-specialised (pipelined) kernel
   bool decode;  // tile kernel without snapshots, final state written in place
   bool sms;     // tile kernel with the state kept in shared memory
+  bool split;   // split variant: prep kernel, then the tile kernel reading its stages
   int grid;     // CTAs
   size_t smem;  // dynamic shared memory bytes
 };
@@ -26,6 +27,12 @@ int launch_tile_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& 
 int launch_tile_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
 int launch_pipe_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
 int launch_pipe_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st);
+// The split variant: the prep kernel (grid N * H) and, as its programmatic
+// dependent, the recurrence kernel (grid cfg.grid) on the same stream.
+int launch_split_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, size_t prep_smem,
+                      cudaStream_t st);
+int launch_split_f32(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, size_t prep_smem,
+                     cudaStream_t st);
 // The q/k conv_state roll of a one-item-per-CTA launch run with
 // p.qk_roll_kernel set (kda_roll.cu), on the same stream after it.
 int launch_qk_roll(const Params& p, int K, bool bf16, cudaStream_t st);
@@ -88,6 +95,48 @@ int launch_tile_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchC
   KDA_CASE_SMS(256, 8)
 #undef KDA_CASES_K
 #undef KDA_CASE_SMS
+#undef KDA_CASE
+  return -1;
+}
+
+template <typename Act, int K, int WARPS>
+int launch_split_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, size_t prep_smem,
+                     cudaStream_t st) {
+  constexpr int BV = WARPS * warp_cols(K);
+  auto prep = kda_prep_kernel<Act, K, BV>;
+  auto rec = kda_tile_kernel<Act, K, WARPS, false, false, true>;
+  static unsigned long long configured_prep = 0, configured_rec = 0;
+  int rc = configure_once(prep, &configured_prep);
+  if (!rc) rc = configure_once(rec, &configured_rec);
+  if (rc) return rc;
+  prep<<<p.N * p.H, kPrepThreads, prep_smem, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return static_cast<int>(e);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cfg.grid);
+  lc.blockDim = dim3(WARPS * 32);
+  lc.dynamicSmemBytes = cfg.smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, rec, tmap, p);
+  if (e != cudaSuccess) return static_cast<int>(e);
+  return static_cast<int>(cudaGetLastError());
+}
+
+template <typename Act>
+int launch_split_dispatch(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c, size_t prep_smem,
+                          cudaStream_t st) {
+#define KDA_CASE(KK, WW) \
+  if (c.K == KK && c.warps == WW) return launch_split_one<Act, KK, WW>(tmap, p, c, prep_smem, st);
+#define KDA_CASES_K(KK) KDA_CASE(KK, 2) KDA_CASE(KK, 4) KDA_CASE(KK, 8)
+  KDA_CASES_K(32)
+  KDA_CASES_K(64)
+  KDA_CASES_K(128)
+#undef KDA_CASES_K
 #undef KDA_CASE
   return -1;
 }

@@ -22,10 +22,12 @@ VARIANT_AUTO = 0
 VARIANT_ONE_ITEM = 1
 VARIANT_PIPELINED = 2
 VARIANT_ONE_ITEM_SMEM = 3
+VARIANT_SPLIT = 4
 VARIANTS = {"auto": VARIANT_AUTO, "one_item": VARIANT_ONE_ITEM, "pipelined": VARIANT_PIPELINED,
-            "one_item_smem": VARIANT_ONE_ITEM_SMEM}
-# plan-string prefix of each variant ("item:128", "pipe:128", "smem:128")
-PLAN_PREFIX = {VARIANT_ONE_ITEM: "item", VARIANT_PIPELINED: "pipe", VARIANT_ONE_ITEM_SMEM: "smem"}
+            "one_item_smem": VARIANT_ONE_ITEM_SMEM, "split": VARIANT_SPLIT}
+# plan-string prefix of each variant ("item:128", "pipe:128", "smem:128", "split:128")
+PLAN_PREFIX = {VARIANT_ONE_ITEM: "item", VARIANT_PIPELINED: "pipe", VARIANT_ONE_ITEM_SMEM: "smem",
+               VARIANT_SPLIT: "split"}
 F32 = 0
 BF16 = 1
 MAX_T = 16
@@ -193,7 +195,7 @@ def parse_plan(spec: str) -> KdaPlan:
     parts = spec.split(":")
     plan = KdaPlan()
     plan.variant = {"item": VARIANT_ONE_ITEM, "pipe": VARIANT_PIPELINED,
-                    "smem": VARIANT_ONE_ITEM_SMEM}[parts[0]]
+                    "smem": VARIANT_ONE_ITEM_SMEM, "split": VARIANT_SPLIT}[parts[0]]
     plan.bv = int(parts[1])
     plan.grid = int(parts[2]) if len(parts) > 2 else 0
     plan.prefetch = int(parts[3]) if len(parts) > 3 else 0

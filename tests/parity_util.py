@@ -143,15 +143,34 @@ def conv_window_properties(inputs_cpu, out, conv_state_dev):
     assert torch.equal(conv_state_dev, xext[:, :, T:T + 3]), "rolled conv_state"
 
 
-def variant_built(variant, K, V, decode=False) -> bool:
+def _stage_floats(T, K, BV):
+    rows = K // 8 if K <= 128 else K // 16
+    rs = rows + (0 if (rows // 4) & 1 else 4)
+    ks = (8 if K <= 128 else 16) * rs
+    return 3 * T * ks + T * BV + (T + 3) // 4 * 4
+
+
+def split_fits(K, V, T, bv, G, act="bf16") -> bool:
+    """The split variant's limits: each item's stage within its K x bv slice
+    of the last token's snapshot, the prep kernel's staging within one CTA."""
+    ks = _stage_floats(1, K, 0) - 4  # 3 * KS
+    prep = 4 * ((2 + G) * T * ks // 3 + G * T * V + G * ((T + 3) // 4 * 4)) \
+        + (2 * K + G * V) * 3 * (4 if act == "f32" else 2)
+    return _stage_floats(T, K, bv) <= K * bv and prep <= 232448
+
+
+def variant_built(variant, K, V, decode=False, T=1, G=1, act="bf16") -> bool:
     """Whether a named variant runs for head dims K x V (the pipelined kernel
-    needs K <= 128, V >= 64 and no decode)."""
+    needs K <= 128, V >= 64 and no decode; the split variant K <= 128, no
+    decode and a stage that fits)."""
     if variant == "pipelined":
         return K <= 128 and V >= 64 and not decode
+    if variant == "split":
+        return K <= 128 and not decode and split_fits(K, V, T, min(V, 128), G, act)
     return True
 
 
-def plan_built(plan, K, V, decode=False, T=1, act="bf16") -> bool:
+def plan_built(plan, K, V, decode=False, T=1, act="bf16", G=1) -> bool:
     """Whether an explicit plan string names a kernel the library builds for
     head dims K x V: one-item tiles are 1/2/4/8 warps of 16 columns (K <= 128;
     1 warp not for K = 256, whose warps hold 8 columns), the shared-memory
@@ -163,6 +182,9 @@ def plan_built(plan, K, V, decode=False, T=1, act="bf16") -> bool:
     wc = 8 if K == 256 else 16
     if bv > V or V % bv:
         return False
+    if kind == "split":
+        return (K <= 128 and not decode and bv in (32, 64, 128)
+                and split_fits(K, V, T, bv, G, act))
     if kind == "pipe":
         # its shared memory fits one CTA except 128-wide K = 128 tiles at
         # T = 16 with fp32 activations

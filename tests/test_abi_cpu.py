@@ -76,7 +76,7 @@ def test_plan_auto_uses_one_item_per_cta(kda):
     p3 = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152)
     assert p3.variant == kda.VARIANT_ONE_ITEM and p3.bv == 128
     assert kda.make_plan(kda.make_shape(8, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
-    assert kda.make_plan(kda.make_shape(32, 1, 16, 32), 152).variant == kda.VARIANT_ONE_ITEM
+    assert kda.make_plan(kda.make_shape(32, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     assert kda.make_plan(kda.make_shape(16, 4, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     # L2 prefetch 3/8 of a wave of resident CTAs ahead
     assert p.prefetch == 152 * p.ctas_per_sm * 3 // 8 > 0
@@ -119,6 +119,36 @@ def test_plan_strings_carry_the_qk_roll(kda):
     p1 = kda.make_plan(kda.make_shape(1, 4, 16, 16, K=256, V=256), 152)
     assert p1.variant == kda.VARIANT_ONE_ITEM and p1.bv == 64 and p1.warps == 8
     assert p1.items == 64 and p1.grid == 64
+
+
+def test_plan_split_variant(kda):
+    # two launches (prep kernel + recurrence kernel), one item per CTA, the
+    # recurrence kernel with the one-item kernel's resources
+    s = kda.make_shape(64, 4, 8, 32)
+    p = kda.resolve_plan(s, 152, "split:128")
+    assert p.variant == kda.VARIANT_SPLIT and p.launches == 2 and p.qk_roll == 0
+    assert p.items == 64 * 32 and p.grid == p.items and p.ctas_per_sm == 2 and p.warps == 8
+    p32 = kda.resolve_plan(s, 152, "split:32")
+    assert p32.items == 64 * 32 * 4 and p32.warps == 2 and p32.ctas_per_sm == 8
+    assert kda.plan_label(kda.make_plan(s, 152, "split")) == "split:128"
+    # the stage must fit the item's slice of the last snapshot: at K = 128 a
+    # 32-column item holds up to T = 7
+    assert kda.resolve_plan(kda.make_shape(4, 7, 2, 2), 152, "split:32").launches == 2
+    for bad, shape in (("split:32", (4, 8, 2, 2)), ("split:16", (4, 2, 2, 2)),
+                       ("split:64", (4, 2, 2, 2, 256, 256))):
+        with pytest.raises(kda.KdaError) as e:
+            kda.resolve_plan(kda.make_shape(*shape), 152, bad)
+        assert e.value.code == -8, bad
+    with pytest.raises(kda.KdaError):  # no plain-decode form
+        kda.resolve_plan(s, 152, "split:128", decode=True)
+    # the dispatcher: single-token calls, two or more v-heads per q/k head,
+    # ~1.5 to 8 units per SM
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 1, 16, 32), 152)) == "split:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 1, 32, 64), 152)) == "split:64"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(32, 1, 16, 32), 152)) == "split:64"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(32, 1, 32, 64), 152)) == "smem:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 2, 16, 32), 152)) == "item:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(16, 1, 16, 16), 152)) == "item:128"
 
 
 def test_plan_small_batches_use_the_pipelined_kernel(kda):

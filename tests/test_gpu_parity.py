@@ -21,10 +21,11 @@ from parity_util import (TOL, assert_parity, conv_window_properties, max_rel_err
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = ("auto", "one_item", "pipelined")
+VARIANTS = ("auto", "one_item", "pipelined", "split")
 # every explicit plan of a V = 128 problem
 ALL_PLANS = ("item:16", "item:32", "item:64", "item:128", "item:128:0:-1", "item:64:0:7",
              "pipe:64", "pipe:128", "pipe:128:0:-1", "pipe:128:0:0:kernel", "pipe:64:0:0:counter",
+             "split:32", "split:64", "split:128", "split:128:0:-1",
              "smem:64", "smem:128",
              # both ways of rolling a q/k conv_state that several items read
              "item:64:0:0:counter", "item:64:0:0:kernel", "smem:128:0:0:counter",
@@ -42,7 +43,7 @@ def _lib():
 @pytest.mark.parametrize("variant", VARIANTS)
 @pytest.mark.parametrize("wl", [wk.TINY, wk.DECODE], ids=lambda w: w.name)
 def test_parity_full(wl, variant):
-    if not variant_built(variant, wl.shape.K, wl.shape.V):
+    if not variant_built(variant, wl.shape.K, wl.shape.V, T=wl.shape.T, G=wl.shape.G, act=wl.shape.act):
         pytest.skip("no such kernel for this shape")
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, wl.gate, threads=8)
@@ -89,7 +90,7 @@ def test_large_workload_takes_the_softplus_overflow_branch():
 
 
 def _valid_plans(s):
-    return [p for p in ALL_PLANS if plan_built(p, s.K, s.V, T=s.T, act=s.act)]
+    return [p for p in ALL_PLANS if plan_built(p, s.K, s.V, T=s.T, act=s.act, G=s.G)]
 
 
 @pytest.mark.parametrize("wl", [wk.DECODE, wk.GVA,
@@ -138,6 +139,7 @@ DET_CASES = [
     (wk.GVA, "item:128:0:0:counter"),          # four readers, last-arrival counter
     (wk.GVA, "item:128:0:0:kernel"),           # four readers, second roll kernel
     (wk.GVA, "pipe:128:0:0:counter"),          # pipelined kernel, counter
+    (wk.GVA, "split:64"),                      # prep kernel + dependent recurrence kernel
     (wk.DECODE, "item:32"),                    # four v-tiles per state read q/k
 ]
 
@@ -225,7 +227,7 @@ EDGE = [
 @pytest.mark.parametrize("case", EDGE, ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}".format(*c))
 def test_edge_shapes(case, variant):
     N, T, H, HV, K, V, act, gate = case
-    if not variant_built(variant, K, V):
+    if not variant_built(variant, K, V, T=T, G=HV // H, act=act):
         pytest.skip("no such kernel for this shape")
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=N * 100 + T)
     inp = wk.make_inputs(wl)
@@ -392,8 +394,9 @@ def _random_cases(n=24, seed=2026):
         act = str(rng.choice(["bf16", "f32"]))
         gate = str(rng.choice(["softplus", "safe"]))
         plans = [p for p in ("item:16", "item:32", "item:64", "item:128", "pipe:64",
-                             "pipe:128", "smem:32", "smem:64", "smem:128")
-                 if plan_built(p, K, V, T=T, act=act)]
+                             "pipe:128", "smem:32", "smem:64", "smem:128", "split:32",
+                             "split:64", "split:128")
+                 if plan_built(p, K, V, T=T, act=act, G=HV // H)]
         if not plans:
             continue
         plan = str(rng.choice(plans))
