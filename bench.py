@@ -131,8 +131,10 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-# kernel that each plan variant launches (ONE_ITEM, PIPELINED, ONE_ITEM_SMEM)
-KERNEL_OF_VARIANT = {1: "kda_tile_kernel", 2: "kda_pipe_kernel", 3: "kda_tile_kernel_sms"}
+# kernel that each plan variant launches (ONE_ITEM, PIPELINED, ONE_ITEM_SMEM, SPLIT)
+KERNEL_OF_VARIANT = {1: "kda_tile_kernel", 2: "kda_pipe_kernel", 3: "kda_tile_kernel_sms",
+                     4: "kda_split"}
+VARIANT_NAME = {1: "one_item", 2: "pipelined", 3: "one_item_smem", 4: "split"}
 
 # device sources each profiled kernel is built from (host-only files such as
 # the dispatcher in kda_api.cu do not change the kernels' code)
@@ -513,7 +515,7 @@ def run_ours(args, wl):
         "scaling": args.scaling, "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "K": s.K,
                    "V": s.V, "W": s.W, "act": s.act, "state": "f32", "gate": wl.gate,
-                   "variant": {1: "one_item", 2: "pipelined", 3: "one_item_smem"}[plan.variant],
+                   "variant": VARIANT_NAME[plan.variant],
                    "v_tile": plan.bv, "plan": args.plan or f"auto ({plan_label(plan)})",
                    "qk_roll": ("single reader" if (s.HV // s.H) * (s.V // plan.bv) == 1 else
                                {1: "counter", 2: "kernel"}.get(plan.qk_roll, "counter")),

@@ -239,8 +239,11 @@ int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool de
     // thread either way) measured faster on the register state at every T.
     out->variant = KDA_VARIANT_ONE_ITEM;
     out->bv = full_bv;
+    // The same holds at most one unit per SM (the 150-point sweep: 5..13 %
+    // at N*HV = 128, T <= 3).
     const long long sms_from = s->T == 1 ? 8 : (s->T == 2 ? 12 : (s->T == 3 ? 24 : 0));
-    if (s->K <= 128 && full_bv == 128 && sms_from > 0 && units >= sms_from * num_sms)
+    if (s->K <= 128 && full_bv == 128 && sms_from > 0 &&
+        (units >= sms_from * num_sms || units <= num_sms))
       out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
     // Small batches: the pipelined kernel, whose producer warps work from
     // inputs staged by bulk copies, measured faster on the 150-point sweep

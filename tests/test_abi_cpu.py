@@ -75,7 +75,8 @@ def test_plan_auto_uses_one_item_per_cta(kda):
     assert kda.make_plan(kda.make_shape(128, 3, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     p3 = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152)
     assert p3.variant == kda.VARIANT_ONE_ITEM and p3.bv == 128
-    assert kda.make_plan(kda.make_shape(8, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
+    assert kda.make_plan(kda.make_shape(8, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
+    assert kda.make_plan(kda.make_shape(16, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     assert kda.make_plan(kda.make_shape(32, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     assert kda.make_plan(kda.make_shape(16, 4, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
     # L2 prefetch 3/8 of a wave of resident CTAs ahead
@@ -156,13 +157,15 @@ def test_plan_small_batches_use_the_pipelined_kernel(kda):
     for T in (2, 4, 8):
         p = kda.make_plan(kda.make_shape(1, T, 16, 16), 152)
         assert kda.plan_label(p) == "pipe:64" and p.items == 32 and p.grid == 32
-    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)) == "item:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)) == "smem:128"
     p = kda.make_plan(kda.make_shape(2, 4, 32, 32), 152)  # 64 units
     assert kda.plan_label(p) == "pipe:64"
     # at most one unit per SM from T = 4 on: 128-column items
     assert kda.plan_label(kda.make_plan(kda.make_shape(8, 4, 16, 16), 152)) == "pipe:128"
     assert kda.plan_label(kda.make_plan(kda.make_shape(8, 8, 16, 16), 152)) == "pipe:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 2, 16, 16), 152)) == "item:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 2, 16, 16), 152)) == "smem:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)) == "smem:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(16, 2, 16, 16), 152)) == "item:128"
     # more units, K = 256 or V = 64: one item per CTA
     assert kda.plan_label(kda.make_plan(kda.make_shape(16, 4, 16, 16), 152)) == "item:128"
     assert kda.plan_label(kda.make_plan(kda.make_shape(1, 4, 1, 2, K=256, V=256), 152)) == "item:64"

@@ -31,3 +31,12 @@ def test_non_zero_rank_of_the_reference_arm_does_nothing():
                         "--workload", "tiny_fp32_n2_t2_h2", "--steps", "1", "--warmup", "0"],
                        capture_output=True, text=True, timeout=300, cwd=ROOT, env=env)
     assert r.returncode == 0 and not r.stdout.strip()
+
+
+def test_bench_names_every_variant():
+    # the bench line names the kernel of every variant the library can pick
+    import bench
+    from linear_attention_speculative_gb300 import kda
+    for v in kda.VARIANTS.values():
+        if v:
+            assert v in bench.KERNEL_OF_VARIANT and v in bench.VARIANT_NAME

@@ -171,7 +171,7 @@ def test_deterministic_across_repeats(wl, plan):
     assert int(ws.count_nonzero()) == 0
 
 
-@pytest.mark.parametrize("variant", ("one_item", "pipelined"))
+@pytest.mark.parametrize("variant", ("one_item", "pipelined", "split"))
 @pytest.mark.parametrize("gate", ("softplus", "safe"))
 def test_chain_of_single_token_calls_is_bit_exact(variant, gate):
     from linear_attention_speculative_gb300 import kda
@@ -259,7 +259,8 @@ def test_workspace_is_left_zeroed():
     assert kda.read_status(shape, ws) == 0
 
 
-def test_side_streams_and_separate_workspaces():
+@pytest.mark.parametrize("plan", [None, "pipe:128", "split:64"])
+def test_side_streams_and_separate_workspaces(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(8, 4, 2, 4, 128, 128, seed=21)
     inp_cpu = wk.make_inputs(wl)
@@ -270,7 +271,7 @@ def test_side_streams_and_separate_workspaces():
     for st in streams:
         with torch.cuda.stream(st):
             inp = to_device(inp_cpu)
-            results.append((kda.run(inp, wl.gate, stream=st), inp["conv_state"]))
+            results.append((kda.run(inp, wl.gate, stream=st, plan=plan), inp["conv_state"]))
     torch.cuda.synchronize()
     for out, cs in results:
         assert_parity(out, cs, orc)
@@ -278,7 +279,8 @@ def test_side_streams_and_separate_workspaces():
         assert torch.equal(out["o"], ref["o"])
 
 
-@pytest.mark.parametrize("plan", [None, "item:128:0:0:counter", "item:128:0:0:kernel"])
+@pytest.mark.parametrize("plan", [None, "item:128:0:0:counter", "item:128:0:0:kernel", "pipe:64",
+                                  "pipe:128:0:0:kernel", "split:64", "split:128"])
 def test_cuda_graph_replay(plan):
     # two v-heads per q/k head: the q/k conv_state roll runs by either protocol
     # (the roll kernel as a programmatic dependent launch inside the graph)
