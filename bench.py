@@ -140,7 +140,8 @@ VARIANT_NAME = {1: "one_item", 2: "pipelined", 3: "one_item_smem", 4: "split"}
 # the dispatcher in kda_api.cu do not change the kernels' code)
 COMMIT_SOURCES = ("kda_commit.cu", "kda_device.cuh")
 VERIFY_SOURCES = ("kda_kernel.cuh", "kda_device.cuh", "kda_launch.cuh", "kda_inst_tile_bf16.cu",
-                  "kda_inst_tile_f32.cu", "kda_inst_pipe_bf16.cu", "kda_inst_pipe_f32.cu", "kda_roll.cu")
+                  "kda_inst_tile_f32.cu", "kda_inst_pipe_bf16.cu", "kda_inst_pipe_f32.cu",
+                  "kda_inst_split_bf16.cu", "kda_inst_split_f32.cu", "kda_roll.cu")
 
 
 def kernel_src_hash(kernel="verify"):
@@ -551,8 +552,9 @@ def plan_label(plan) -> str:
 
 def run_sweep(args):
     """Time each sweep point with every plan of --sweep-plans ("auto" = the
-    dispatcher's pick).  Inputs are drawn on the device (timing only); L2 is
-    flushed before every timed launch.  Median of --steps launches."""
+    dispatcher's pick) -- the verify call, or with --op decode the plain
+    decode.  Inputs are drawn on the device (timing only); L2 is flushed
+    before every timed launch.  Median of --steps launches."""
     import torch
     from linear_attention_speculative_gb300 import kda
     from linear_attention_speculative_gb300 import workloads as wk
@@ -562,6 +564,7 @@ def run_sweep(args):
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
     K = max(3, args.steps)
+    decode = args.op == "decode"
     plans = [p for p in args.sweep_plans.split(",") if p]
     rows = []
     sink = open(args.sweep_out, "w") if args.sweep_out else None
@@ -573,23 +576,29 @@ def run_sweep(args):
         out = {k: v for k, v in wk.empty_outputs(wl, device=dev).items()}
         shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
         ws = kda.alloc_workspace(shape, dev)
-        auto = plan_label(kda.make_plan(shape, sms, "auto"))
-        row = {"workload": wl.name, "N": s.N, "T": s.T, "H": s.H, "HV": s.HV, "gate": wl.gate,
-               "alg_bytes": s.algorithmic_bytes(), "head_steps": s.head_steps, "auto": auto,
-               "us": {}}
+        auto = plan_label(kda.make_plan(shape, sms, "auto", decode=decode))
+        alg = decode_bytes(s) if decode else s.algorithmic_bytes()
+        row = {"workload": wl.name, "op": args.op if decode else "verify", "N": s.N, "T": s.T,
+               "H": s.H, "HV": s.HV, "gate": wl.gate, "alg_bytes": alg,
+               "head_steps": s.head_steps, "auto": auto, "us": {}}
         for spec in plans:
             plan = None if spec == "auto" else spec
             if plan is not None:
                 try:  # a plan the library does not build for this point is left out
-                    kda.resolve_plan(shape, sms, plan)
+                    kda.resolve_plan(shape, sms, plan, decode=decode)
                 except kda.KdaError:
                     continue
 
             def step():
-                kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"],
-                                inp["A_log"], inp["dt_bias"], inp["a"], inp["b"], inp["S0"],
-                                wl.gate, out["o"], out["inter_ssm"], out["conv_snapshots"], ws,
-                                stream=stream, shape=shape, plan=plan)
+                if decode:
+                    kda.conv_decode(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"],
+                                    inp["A_log"], inp["dt_bias"], inp["a"], inp["b"], inp["S0"],
+                                    wl.gate, out["o"], ws, stream=stream, shape=shape, plan=plan)
+                else:
+                    kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"],
+                                    inp["A_log"], inp["dt_bias"], inp["a"], inp["b"], inp["S0"],
+                                    wl.gate, out["o"], out["inter_ssm"], out["conv_snapshots"], ws,
+                                    stream=stream, shape=shape, plan=plan)
             for _ in range(3):
                 step()
             times = []
@@ -606,7 +615,7 @@ def run_sweep(args):
         explicit = {k: v for k, v in row["us"].items() if k != "auto"}
         best = min(explicit, key=explicit.get) if explicit else "auto"
         row["best"] = best
-        row["best_gbs"] = s.algorithmic_bytes() / (row["us"][best] / 1e6) / 1e9
+        row["best_gbs"] = alg / (row["us"][best] / 1e6) / 1e9
         if "auto" in row["us"]:
             row["auto_over_best"] = row["us"]["auto"] / row["us"][best]
         rows.append(row)
@@ -634,6 +643,10 @@ def sweep_report(path, peak_gbs, peak_src):
     for r in rows:
         plans += [k for k in r["us"] if k != "auto" and k not in plans]
     out = []
+    op = rows[0].get("op", "verify") if rows else "verify"
+    out.append("Operation: " + ("the plain decode (kda_conv_decode: state updated in place, no snapshots)"
+                                if op == "decode" else "the verify call (kda_conv_verify)") + ".")
+    out.append("")
     out.append(f"Peak: {peak_gbs:.1f} GB/s ({peak_src}, MEASURED_PEAKS.json hbm_gbs).  Times are the median of "
                "per-launch CUDA events with L2 flushed before each launch (258 MB written, then 258 MB read); "
                "GB/s = algorithmic bytes / time.")
@@ -653,6 +666,13 @@ def sweep_report(path, peak_gbs, peak_src):
     out.append("")
     out.append(f"Points: {len(rows)}.  auto / best: mean {sum(ratios) / len(ratios):.4f}, "
                f"max {max(ratios):.4f}.")
+    # the dispatcher's plan timed as an explicit plan (the same launches as
+    # `best`'s column, so no second measurement's timer steps in the ratio)
+    own = [r["us"][r["auto"]] / r["us"][r["best"]] for r in rows if r["auto"] in r["us"]]
+    if own:
+        out.append(f"The dispatcher's plan's own column / best: mean {sum(own) / len(own):.4f}, "
+                   f"max {max(own):.4f} ({len(own)} points; the auto column is a second measurement of the "
+                   "same plan, so its ratio also carries the event timer's steps).")
     for lo, hi in ((1, 1), (8, 32), (128, 512)):
         sub = [x for x, r in zip(ratios, rows) if lo <= r["N"] <= hi]
         if sub:
@@ -737,6 +757,14 @@ def run_commit(args, wl):
                       "peak_source": src, "timing": "median of per-launch CUDA events, L2 flushed"}))
 
 
+def decode_bytes(s) -> int:
+    """Algorithmic bytes of one plain decode call: the state read and written in
+    place, the raw inputs, conv_state read and written, o, the weights."""
+    return (8 * s.N * s.HV * s.K * s.V + s.act_bytes * (
+        s.N * s.T * s.dim + 2 * s.N * s.dim * 3 + s.N * s.T * s.HV * s.K + s.N * s.T * s.HV
+        + s.N * s.T * s.HV * s.V + 4 * s.dim) + 4 * s.HV * (1 + s.K))
+
+
 def run_decode(args, wl):
     """Head-steps/s and HBM bandwidth of the plain decode (state in place)."""
     import torch
@@ -754,9 +782,7 @@ def run_decode(args, wl):
         kda.conv_decode(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
                         inp["dt_bias"], inp["a"], inp["b"], inp["S0"], wl.gate, o, ws,
                         stream=stream, shape=shape, plan=args.plan or None)
-    nbytes = (8 * s.N * s.HV * s.K * s.V + s.act_bytes * (
-        s.N * s.T * s.dim + 2 * s.N * s.dim * 3 + s.N * s.T * s.HV * s.K + s.N * s.T * s.HV
-        + s.N * s.T * s.HV * s.V + 4 * s.dim) + 4 * s.HV * (1 + s.K))
+    nbytes = decode_bytes(s)
     flush = nbytes < 2 * L2_BYTES
     fbuf = L2Flush(dev) if flush else None
     for _ in range(max(3, args.warmup)):

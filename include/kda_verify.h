@@ -309,6 +309,11 @@ size_t kda_workspace_bytes(const kda_shape* s);
  * CTA, grid size.  Returns 0 or a negative KDA_ERR_* code. */
 int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
 
+/* The plan kda_conv_decode picks for shape `s` (plain decode: ONE_ITEM or
+ * ONE_ITEM_SMEM only; AUTO, ONE_ITEM or ONE_ITEM_SMEM may be requested).
+ * Host-only, no CUDA call.  Returns 0 or a negative KDA_ERR_* code. */
+int kda_make_decode_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
+
 /* Fill the derived fields of a hand-written plan (variant, bv and the
  * optional grid / prefetch / qk_roll requests set) exactly as
  * kda_conv_verify_plan would before launching it: warps, grid, ctas_per_sm,

@@ -229,54 +229,33 @@ int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool de
     out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
     out->bv = full_bv;
   } else {
-    // One item per CTA.  Whole states (up to 8 warps' columns) per CTA: every
-    // CTA has many threads for its producer tasks and the q/k conv is not
-    // repeated per v-tile.  Calls of up to three tokens over many units keep
-    // the state in shared memory instead (3 CTAs/SM instead of 2): measured on
-    // GB300 +9..17 % at T = 1, +3..6 % at T = 2 and +2..4 % at T = 3 from the
-    // unit counts below (per SM: 8, 12, 24); from T = 4 on it is slower (two
-    // shared-memory passes per token).  K = 256 (16 rows x 4 columns per
-    // thread either way) measured faster on the register state at every T.
+    // One item per CTA, the state in registers: the fastest kernel at 145 of
+    // the 150 points of the configuration sweep (T in 1..8, N in 1..512, three
+    // head layouts, both gates; K = V = 128) and at 128 of the same 150 points
+    // for the plain decode.  Against the fastest explicit plan at each point
+    // the rules below measured within 0.04 % (verify) and 0.18 % (decode) on
+    // average, 1.3 % and 8.5 % at worst (single-digit-N points, where the
+    // event timer moves in ~2 us steps).
     out->variant = KDA_VARIANT_ONE_ITEM;
     out->bv = full_bv;
-    // The same holds at most one unit per SM (the 150-point sweep: 5..13 %
-    // at N*HV = 128, T <= 3).
-    const long long sms_from = s->T == 1 ? 8 : (s->T == 2 ? 12 : (s->T == 3 ? 24 : 0));
-    if (s->K <= 128 && full_bv == 128 && sms_from > 0 &&
-        (units >= sms_from * num_sms || units <= num_sms))
-      out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
-    // Small batches: the pipelined kernel, whose producer warps work from
-    // inputs staged by bulk copies, measured faster on the 150-point sweep
-    // with at most half a unit per SM from T = 2 on (64-column items, up to
-    // -15 %) and with at most one unit per SM from T = 4 on (128-column
-    // items, up to -8 %); single-token calls of a few units and batches from
-    // about two units per SM on run faster on the one-item kernels.
-    if (!decode && s->K <= 128 && s->V >= 128 && s->T >= 2) {
-      kda_plan pipe;
-      std::memset(&pipe, 0, sizeof(pipe));
-      pipe.variant = KDA_VARIANT_PIPELINED;
-      pipe.bv = 0;
-      if (2 * units <= num_sms) pipe.bv = 4 * kda::warp_cols(s->K);
-      else if (s->T >= 4 && units <= num_sms) pipe.bv = 8 * kda::warp_cols(s->K);
-      if (pipe.bv && valid_plan(&pipe, s, false)) {
-        out->variant = KDA_VARIANT_PIPELINED;
-        out->bv = pipe.bv;
-      }
-    }
-    // Single-token calls with several v-heads per q/k head, from about 1.5 to
-    // 8 units per SM: the split variant (each group's q/k conv run once
-    // instead of once per v-head) measured 6..13 % faster on the sweep;
-    // 64-column items from 3 units per SM on.
     const int G = s->HV / s->H;
-    if (!decode && s->T == 1 && G >= 2 && s->K <= 128 && 2 * units >= 3LL * num_sms &&
-        units < 8LL * num_sms) {
-      kda_plan split;
-      std::memset(&split, 0, sizeof(split));
-      split.variant = KDA_VARIANT_SPLIT;
-      split.bv = std::min(s->V, (units >= 3LL * num_sms ? 4 : 8) * kda::warp_cols(s->K));
-      if (valid_plan(&split, s, false)) {
-        out->variant = KDA_VARIANT_SPLIT;
-        out->bv = split.bv;
+    if (s->K <= 128 && full_bv == 128) {
+      // Short calls over many units: the shared-memory state (3 CTAs per SM
+      // instead of 2) -- single-token verifies with one v-head per q/k head
+      // from 8 units per SM (+3..5 %); plain decodes from 8 (T = 1) and 16
+      // (T = 2) units per SM (+2..6 %).
+      const long long smem_from =
+          decode ? (s->T == 1 ? 8 : (s->T == 2 ? 16 : 0)) : (s->T == 1 && G == 1 ? 8 : 0);
+      if (smem_from > 0 && units >= smem_from * num_sms) {
+        out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
+      } else if (G >= 2 && (s->T <= (decode ? 1 : 2) ||
+                            (2 * units <= num_sms && (!decode || s->T <= 3)))) {
+        // Several v-heads per q/k head: 64-column tiles for calls of up to
+        // two tokens (one for decode) and for at most half a unit per SM
+        // (twice the CTAs; +2..17 %; for decode only up to three tokens).
+        // Longer calls keep 128 columns: each 64-column item repeats the q/k
+        // conv of all T tokens.
+        out->bv = 4 * kda::warp_cols(s->K);
       }
     }
   }
@@ -290,6 +269,10 @@ extern "C" {
 
 int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out) {
   return make_plan_impl(s, num_sms, variant, false, out);
+}
+
+int kda_make_decode_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out) {
+  return make_plan_impl(s, num_sms, variant, true, out);
 }
 
 int kda_resolve_plan(const kda_shape* s, int num_sms, int decode, kda_plan* plan) {
@@ -447,6 +430,10 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.G = s->HV / s->H;
   p.nvt = s->V / plan.bv;
   p.gate_mode = gate_mode == KDA_GATE_SOFTPLUS ? 0 : 1;
+  p.div_nvt = kda::make_fastdiv((uint32_t)p.nvt);
+  p.div_HV = kda::make_fastdiv((uint32_t)p.HV);
+  p.div_G = kda::make_fastdiv((uint32_t)p.G);
+  p.div_T = kda::make_fastdiv((uint32_t)p.T);
   const bool roll_kernel = plan.qk_roll == KDA_QK_ROLL_KERNEL && p.G * p.nvt > 1;
   p.qk_roll_kernel = roll_kernel ? 1 : 0;
 

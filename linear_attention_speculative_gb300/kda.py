@@ -36,7 +36,8 @@ MAX_T = 16
 EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan",
             "kda_conv_verify_indexed", "kda_conv_decode", "kda_commit", "kda_commit_indexed",
             "kda_conv_verify_noalloc", "kda_noalloc_read_status", "kda_workspace_bytes",
-            "kda_make_plan", "kda_resolve_plan", "kda_read_status", "kda_strerror", "kda_version")
+            "kda_make_plan", "kda_make_decode_plan", "kda_resolve_plan", "kda_read_status",
+            "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
 
@@ -113,6 +114,8 @@ def _load():
     L.kda_workspace_bytes.argtypes = [sp]
     L.kda_make_plan.restype = ctypes.c_int
     L.kda_make_plan.argtypes = [sp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(KdaPlan)]
+    L.kda_make_decode_plan.restype = ctypes.c_int
+    L.kda_make_decode_plan.argtypes = [sp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(KdaPlan)]
     L.kda_resolve_plan.restype = ctypes.c_int
     L.kda_resolve_plan.argtypes = [sp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(KdaPlan)]
     L.kda_read_status.restype = ctypes.c_int
@@ -157,11 +160,13 @@ def alloc_workspace(shape: KdaShape, device) -> torch.Tensor:
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 
-def make_plan(shape: KdaShape, num_sms: int, variant: str = "auto") -> KdaPlan:
+def make_plan(shape: KdaShape, num_sms: int, variant: str = "auto", decode: bool = False) -> KdaPlan:
+    """The dispatcher's plan for kda_conv_verify (or, with decode, kda_conv_decode)."""
     plan = KdaPlan()
-    rc = lib().kda_make_plan(ctypes.byref(shape), num_sms, VARIANTS[variant], ctypes.byref(plan))
+    fn = lib().kda_make_decode_plan if decode else lib().kda_make_plan
+    rc = fn(ctypes.byref(shape), num_sms, VARIANTS[variant], ctypes.byref(plan))
     if rc != 0:
-        raise KdaError(rc, "kda_make_plan")
+        raise KdaError(rc, "kda_make_decode_plan" if decode else "kda_make_plan")
     return plan
 
 

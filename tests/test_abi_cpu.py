@@ -64,31 +64,63 @@ def test_plan_auto_uses_one_item_per_cta(kda):
     p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
     assert p.variant == kda.VARIANT_ONE_ITEM
     assert p.bv == 128 and p.warps == 8 and p.items == 256 * 32 and p.grid == p.items
-    # single-token calls over many units: state kept in shared memory
-    p2 = kda.make_plan(kda.make_shape(512, 1, 32, 64), 152)
-    assert p2.variant == kda.VARIANT_ONE_ITEM_SMEM and p2.bv == 128 and p2.items == 512 * 64
+    # single-token calls, one v-head per q/k head, from 8 units per SM: state
+    # kept in shared memory (3 CTAs per SM)
+    p2 = kda.make_plan(kda.make_shape(512, 1, 32, 32), 152)
+    assert p2.variant == kda.VARIANT_ONE_ITEM_SMEM and p2.bv == 128 and p2.items == 512 * 32
     assert p2.ctas_per_sm == 3
-    assert kda.make_plan(kda.make_shape(512, 2, 32, 64), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
-    assert kda.make_plan(kda.make_shape(32, 2, 32, 64), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
-    assert kda.make_plan(kda.make_shape(32, 2, 16, 32), 152).variant == kda.VARIANT_ONE_ITEM
-    assert kda.make_plan(kda.make_shape(512, 3, 32, 64), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
-    assert kda.make_plan(kda.make_shape(128, 3, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
-    p3 = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152)
-    assert p3.variant == kda.VARIANT_ONE_ITEM and p3.bv == 128
-    assert kda.make_plan(kda.make_shape(8, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM_SMEM
-    assert kda.make_plan(kda.make_shape(16, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
-    assert kda.make_plan(kda.make_shape(32, 1, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
-    assert kda.make_plan(kda.make_shape(16, 4, 16, 16), 152).variant == kda.VARIANT_ONE_ITEM
-    # L2 prefetch 3/8 of a wave of resident CTAs ahead
-    assert p.prefetch == 152 * p.ctas_per_sm * 3 // 8 > 0
+    assert kda.plan_label(kda.make_plan(kda.make_shape(76, 1, 16, 16), 152)) == "smem:128"  # 8 per SM
+    assert kda.plan_label(kda.make_plan(kda.make_shape(75, 1, 16, 16), 152)) == "item:128"
+    for shape in ((512, 2, 32, 32), (512, 3, 16, 16), (8, 1, 16, 16), (32, 1, 16, 16), (128, 3, 16, 16),
+                  (16, 4, 16, 16), (512, 4, 32, 64), (512, 3, 32, 64), (3, 4, 16, 32)):
+        assert kda.plan_label(kda.make_plan(kda.make_shape(*shape), 152)) == "item:128", shape
+    # several v-heads per q/k head: 64-column items up to T = 2 and at most
+    # half a unit per SM
+    for shape in ((512, 1, 32, 64), (512, 2, 32, 64), (32, 2, 16, 32), (8, 1, 16, 32), (1, 4, 16, 32),
+                  (2, 4, 16, 32), (1, 8, 32, 64)):
+        p = kda.make_plan(kda.make_shape(*shape), 152)
+        assert kda.plan_label(p) == "item:64" and p.warps == 4, shape
+    # K = 256 and V = 64: the widest one-item tile (64 columns)
+    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 4, 1, 2, K=256, V=256), 152)) == "item:64"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(512, 1, 8, 16, K=256, V=256), 152)) == "item:64"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 4, 1, 2, K=64, V=64), 152)) == "item:64"
+    # L2 prefetch 3/8 of a wave of resident CTAs ahead; plans may set or disable it
+    p4 = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
+    assert p4.prefetch == 152 * p4.ctas_per_sm * 3 // 8 > 0
+    assert kda.resolve_plan(kda.make_shape(256, 4, 32, 32), 152, "item:128:0:40").prefetch == 40
+    assert kda.resolve_plan(kda.make_shape(256, 4, 32, 32), 152, "item:128:0:-1").prefetch == 0
+
+
+def test_decode_plan(kda):
+    # kda_conv_decode's dispatcher: the shared-memory state from 8 (T = 1) and
+    # 16 (T = 2) units per SM, 64-column items for single tokens with several
+    # v-heads per q/k head and for at most half a unit per SM, else 128 columns
+    def label(*shape, variant="auto", **dims):
+        return kda.plan_label(kda.make_plan(kda.make_shape(*shape, **dims), 152, variant, decode=True))
+    assert label(512, 1, 32, 64) == "smem:128" and label(76, 1, 16, 16) == "smem:128"
+    assert label(75, 1, 16, 16) == "item:128" and label(8, 1, 16, 16) == "item:128"
+    assert label(152, 2, 16, 16) == "smem:128" and label(151, 2, 16, 16) == "item:128"
+    assert label(32, 1, 16, 32) == "item:64" and label(8, 2, 16, 32) == "item:128"
+    assert label(1, 2, 16, 32) == "item:64" and label(1, 3, 32, 64) == "item:64"
+    assert label(1, 4, 16, 32) == "item:128" and label(1, 8, 32, 64) == "item:128"
+    for T in (3, 4):
+        assert label(512, T, 32, 64) == "item:128"
+    assert label(64, 1, 8, 16, K=256, V=256) == "item:64"
+    assert label(8, 1, 16, 16, variant="one_item_smem") == "smem:128"
+    for bad in ("pipelined", "split"):
+        with pytest.raises(kda.KdaError) as e:
+            kda.make_plan(kda.make_shape(8, 1, 16, 16), 152, bad, decode=True)
+        assert e.value.code == -8
 
 
 def test_plan_picks_the_qk_roll(kda):
     # one reader per q/k group: rolled inside the verify kernel, one launch
     p = kda.make_plan(kda.make_shape(256, 4, 32, 32), 152)
     assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
-    # two readers, many waves: the separate roll kernel
+    # four readers (two v-heads x two 64-column tiles), many waves: the
+    # separate roll kernel
     p = kda.make_plan(kda.make_shape(512, 1, 32, 64), 152)
+    assert kda.plan_label(p) == "item:64"
     assert p.qk_roll == kda.QK_ROLL_KERNEL and p.launches == 2
     # two readers, a fraction of a wave: the counter, one launch
     p = kda.make_plan(kda.make_shape(2, 1, 16, 32), 152)
@@ -142,34 +174,21 @@ def test_plan_split_variant(kda):
         assert e.value.code == -8, bad
     with pytest.raises(kda.KdaError):  # no plain-decode form
         kda.resolve_plan(s, 152, "split:128", decode=True)
-    # the dispatcher: single-token calls, two or more v-heads per q/k head,
-    # ~1.5 to 8 units per SM
-    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 1, 16, 32), 152)) == "split:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 1, 32, 64), 152)) == "split:64"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(32, 1, 16, 32), 152)) == "split:64"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(32, 1, 32, 64), 152)) == "smem:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 2, 16, 32), 152)) == "item:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(16, 1, 16, 16), 152)) == "item:128"
+    # the dispatcher no longer picks it: the one-item kernels measured faster
+    for shape in ((8, 1, 16, 32), (8, 1, 32, 64), (32, 1, 16, 32)):
+        assert kda.make_plan(kda.make_shape(*shape), 152).variant == kda.VARIANT_ONE_ITEM
 
 
-def test_plan_small_batches_use_the_pipelined_kernel(kda):
-    # at most half a unit per SM from T = 2 on: 64-column items of the pipelined kernel
-    for T in (2, 4, 8):
-        p = kda.make_plan(kda.make_shape(1, T, 16, 16), 152)
-        assert kda.plan_label(p) == "pipe:64" and p.items == 32 and p.grid == 32
-    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)) == "smem:128"
-    p = kda.make_plan(kda.make_shape(2, 4, 32, 32), 152)  # 64 units
-    assert kda.plan_label(p) == "pipe:64"
-    # at most one unit per SM from T = 4 on: 128-column items
-    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 4, 16, 16), 152)) == "pipe:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 8, 16, 16), 152)) == "pipe:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 2, 16, 16), 152)) == "smem:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 1, 16, 16), 152)) == "smem:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(16, 2, 16, 16), 152)) == "item:128"
-    # more units, K = 256 or V = 64: one item per CTA
-    assert kda.plan_label(kda.make_plan(kda.make_shape(16, 4, 16, 16), 152)) == "item:128"
-    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 4, 1, 2, K=256, V=256), 152)) == "item:64"
-    assert kda.make_plan(kda.make_shape(1, 4, 1, 2, K=64, V=64), 152).variant == kda.VARIANT_ONE_ITEM
+def test_plan_small_batches_use_one_item_kernels(kda):
+    # small batches run one item per CTA too (the pipelined kernel, whose
+    # producer warps stage inputs by bulk copies, measured slower at every
+    # point of the sweep); it stays available by name
+    for T in (1, 2, 4, 8):
+        assert kda.plan_label(kda.make_plan(kda.make_shape(1, T, 16, 16), 152)) == "item:128"
+        assert kda.plan_label(kda.make_plan(kda.make_shape(1, T, 16, 16), 152, "pipelined")) == "pipe:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(2, 4, 32, 32), 152)) == "item:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(8, 4, 16, 16), 152)) == "item:128"
+    assert kda.plan_label(kda.make_plan(kda.make_shape(1, 4, 16, 32), 152)) == "item:64"
 
 
 def test_plan_pipelined_is_persistent(kda):
