@@ -52,8 +52,11 @@ typedef enum { KDA_GATE_SOFTPLUS = 0, KDA_GATE_SAFE = 1 } kda_gate_mode;
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 
 /* Kernel variants, named after the kernel they run.  An item is one
- * (sequence, v-head, v-tile) slice of a state.  AUTO picks from N*HV, T and
- * the SM count. */
+ * (sequence, v-head, v-tile) slice of a state.  AUTO picks ONE_ITEM (128- or
+ * 64-column tiles) or ONE_ITEM_SMEM from N*HV, T, the v-heads per q/k head
+ * and the SM count (kda_make_plan, kda_make_decode_plan); PIPELINED and SPLIT
+ * measured slower at every point of the configuration sweep on GB300 and run
+ * only when requested. */
 typedef enum {
   KDA_VARIANT_AUTO = 0,
   KDA_VARIANT_ONE_ITEM = 1,      /* one CTA per item, the state in registers; every warp

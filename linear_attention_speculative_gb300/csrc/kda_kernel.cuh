@@ -21,17 +21,25 @@
 //             the S^T q partial sums and the 16-byte streaming store of the
 //             snapshot, a second butterfly, o.
 //
-// Two kernels run that same producer arithmetic and consumer code:
+// Kernels that run that same producer arithmetic and consumer code:
 //   kda_tile_kernel  one item per CTA; every warp produces, then consumes.
-//                    The hardware block scheduler keeps several CTAs in
-//                    different phases on every SM.
-//   kda_ws_kernel    persistent and warp-specialised: one producer warp
-//                    stages the NEXT item -- its raw inputs arrive by 1-D
-//                    bulk TMA copies, its state tile by a 2-D TMA load as soon
-//                    as the consumers have moved the current tile to
-//                    registers -- while the consumer warps stream the
-//                    recurrence of the current item.  Full/empty mbarriers
-//                    hand stages and tiles over; every wait is bounded.
+//                    Thread 0 issues the state-tile TMA load while its own
+//                    first producer loads are in flight.  The hardware block
+//                    scheduler keeps several CTAs in different phases on
+//                    every SM.  Instantiated with the state in registers or
+//                    in shared memory (SMS), as the plain decode (DEC: no
+//                    snapshots, the final state written in place) and as the
+//                    split variant's recurrence (PRE: the stage comes from
+//                    kda_prep_kernel).
+//   kda_pipe_kernel  persistent and warp-specialised: producer warps stage
+//                    the NEXT item -- its raw inputs arrive by 1-D bulk TMA
+//                    copies, its state tile by a 2-D TMA load as soon as the
+//                    consumers have moved the current tile to registers --
+//                    while the consumer warps stream the recurrence of the
+//                    current item.  Full/empty mbarriers hand stages and tiles
+//                    over; every wait is bounded.
+//   kda_prep_kernel  the split variant's first kernel: the producer work of
+//                    one q/k group, once, for all the items that read it.
 // Same floating-point operations in the same order => bit-identical outputs.
 //
 // Shared q/k conv_state write-back: the q/k channels of group (n, h) are read
@@ -39,12 +47,13 @@
 // either a separate kernel launched after this one rolls them (kda_roll.cu;
 // Params::qk_roll_kernel), or each item arrives on a per-group counter after
 // its reads and the last arrival rolls the group's q/k conv_state and resets
-// the counter to zero.  Nothing ever waits on another CTA.  v channels belong
-// to exactly one item, which rolls them itself.  In the one-item kernel, whose
-// threads read conv_state straight from global memory, the producer stages the
-// new windows in shared memory and every roll is stored after the barrier
-// that ends the CTA's conv_state reads; the warp-specialised kernel reads its
-// raw inputs from shared memory and rolls directly.
+// the counter to zero (in the split variant the prep kernel rolls every
+// channel of its group).  Nothing ever waits on another CTA.  v channels
+// belong to exactly one item, which rolls them itself.  In the one-item
+// kernel, whose threads read conv_state straight from global memory, the
+// producer stages the new windows in shared memory and every roll is stored
+// after the barrier that ends the CTA's conv_state reads; the pipelined kernel
+// reads its raw inputs from shared memory and rolls directly.
 #pragma once
 
 #include "kda_device.cuh"
