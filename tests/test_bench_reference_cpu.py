@@ -40,3 +40,30 @@ def test_bench_names_every_variant():
     for v in kda.VARIANTS.values():
         if v:
             assert v in bench.KERNEL_OF_VARIANT and v in bench.VARIANT_NAME
+
+
+def test_sweep_report_of_verify_and_decode_rows(tmp_path):
+    # the committed report generator: per point the dispatcher's plan, the best
+    # explicit plan, and the dispatcher plan's own column against the best
+    import bench
+    rows = [{"workload": "sweep_T1_N1_H16_HV16_softplus", "op": op, "N": 1, "T": 1, "H": 16, "HV": 16,
+             "gate": "softplus", "alg_bytes": 2_000_000, "head_steps": 16, "auto": "item:128",
+             "us": {"auto": 10.4, "item:64": 10.2, "item:128": 10.3}, "best": "item:64",
+             "best_gbs": 2e6 / 10.2e-6 / 1e9, "auto_over_best": 10.4 / 10.2}
+            for op in ("verify", "decode")]
+    for op, row in zip(("verify", "decode"), rows):
+        path = tmp_path / f"{op}.jsonl"
+        path.write_text(json.dumps(row) + "\n")
+        text = bench.sweep_report(str(path), 6791.0, "measured")
+        assert ("kda_conv_decode" in text) == (op == "decode")
+        assert "| 1 | 1 | 16 | 16 | softplus | item:128 | 10.4 | item:64 | 10.2 |" in text
+        assert "own column / best: mean 1.0098" in text
+
+
+def test_committed_ncu_summaries_match_the_kernel_sources():
+    # the bench line's DRAM traffic comes from these summaries and is dropped
+    # (null) once the kernel sources differ from the ones they were taken on
+    import bench
+    for wl in ("large_bf16_n256_t4_h32", "gva_bf16_n64_t4_h8_hv32_safe", "decode_bf16_n16_t4_h16"):
+        total, rd, wr = bench.ncu_traffic(wl, "kda_tile_kernel")
+        assert total is not None and total == rd + wr, wl
