@@ -55,6 +55,42 @@ MUTANTS = {
                              " sizeof(double) * (size_t)K * V);"),
     "commit_takes_first_token": ("memcpy(S_out, inter + (size_t)(acc - 1) * ns, sizeof(double) * ns);",
                                  "memcpy(S_out, inter, sizeof(double) * ns);"),
+    "commit_conv_from_first_token": ("memcpy(cs_out, snap + (size_t)(acc - 1) * nc, sizeof(double) * nc);",
+                                     "memcpy(cs_out, snap, sizeof(double) * nc);"),
+    "q_not_normalised": ("      orc_l2norm(K, qn, eps);\n", ""),
+    "conv_state_not_rolled": ("cs_new[(size_t)c * (W - 1) + j] = xext[T + j];",
+                              "cs_new[(size_t)c * (W - 1) + j] = xext[j];"),
+    "beta_from_qk_head": ("const double beta = orc_sigmoid(b[(size_t)t * HV + hv]);",
+                          "const double beta = orc_sigmoid(b[(size_t)t * HV + h]);"),
+    "gate_from_first_token": ("const double* at = a + ((size_t)t * HV + hv) * K;",
+                              "const double* at = a + (size_t)hv * K;"),
+    "decay_after_update": (
+        "  /* S <- diag(exp g) S */\n"
+        "  for (int r = 0; r < K; ++r) {\n"
+        "    double d = exp(g[r]);\n"
+        "    for (int c = 0; c < V; ++c) S[(size_t)r * V + c] *= d;\n"
+        "  }\n"
+        "  /* S <- S + beta k (v - S^T k)^T */\n"
+        "  double* u = (double*)malloc(sizeof(double) * (size_t)V);\n"
+        "  for (int c = 0; c < V; ++c) {\n"
+        "    double sk = 0.0;\n"
+        "    for (int r = 0; r < K; ++r) sk += S[(size_t)r * V + c] * k[r];\n"
+        "    u[c] = v[c] - sk;\n"
+        "  }\n"
+        "  for (int r = 0; r < K; ++r)\n"
+        "    for (int c = 0; c < V; ++c) S[(size_t)r * V + c] += beta * k[r] * u[c];\n",
+        "  double* u = (double*)malloc(sizeof(double) * (size_t)V);\n"
+        "  for (int c = 0; c < V; ++c) {\n"
+        "    double sk = 0.0;\n"
+        "    for (int r = 0; r < K; ++r) sk += S[(size_t)r * V + c] * k[r];\n"
+        "    u[c] = v[c] - sk;\n"
+        "  }\n"
+        "  for (int r = 0; r < K; ++r)\n"
+        "    for (int c = 0; c < V; ++c) S[(size_t)r * V + c] += beta * k[r] * u[c];\n"
+        "  for (int r = 0; r < K; ++r) {\n"
+        "    double d = exp(g[r]);\n"
+        "    for (int c = 0; c < V; ++c) S[(size_t)r * V + c] *= d;\n"
+        "  }\n"),
 }
 
 
