@@ -12,9 +12,13 @@ exact value everywhere.  The bound is therefore applied to the computation,
 and the final round-to-nearest into the output type is allowed on top of it:
 an element passes when |x - y| <= 2e-3 * max(|y|, rms(y)) + ulp(x) / 2.
 For fp32 outputs the extra term is ~6e-8 relative.  The relative RMS error
-of o (||x - y|| / ||y||) must also stay below 2e-3; bf16 rounding alone
-gives about 1.5e-3 there, the floor the verify-decode page reports for o
-against fp32.
+of o must also stay below 2e-3, measured against the oracle rounded into the
+output type (||x - round(y)|| / ||y||), as the verify-decode page measures its
+own o (its Tests & Accuracy section reports o's relative RMS error against a
+reference in the same dtype, <= 1.7e-4, apart from the 1.5e-3 - 1.7e-3 that
+bf16 rounding alone leaves against fp32).  Against the unrounded y that floor
+fluctuates with the sample: on a few hundred elements rounding alone can give
+2.1e-3.
 
 Conv snapshots and the rolled conv_state are copies and must match bit for
 bit.
@@ -60,11 +64,29 @@ def max_rel_err_rounded(x, y, dtype) -> float:
     return float(np.max(excess / den))
 
 
+def round_to(y, dtype) -> np.ndarray:
+    """y (float64) rounded once, to nearest even, to the significand of
+    `dtype` (torch.bfloat16: 8 bits, torch.float32: 24 bits)."""
+    y = np.asarray(y, dtype=np.float64)
+    bits = 8 if dtype == torch.bfloat16 else 24
+    m, e = np.frexp(y)  # y = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.rint(np.ldexp(m, bits)), e - bits)
+
+
 def rel_rmse(x, y) -> float:
     x = np.asarray(x, dtype=np.float64)
     y = np.asarray(y, dtype=np.float64)
     d = float(np.sqrt(np.mean((x - y) ** 2)))
     r = float(np.sqrt(np.mean(y * y)))
+    return d / r if r > 0 else d
+
+
+def rel_rmse_rounded(x, y, dtype) -> float:
+    """||x - round(y)|| / ||y||: the relative RMS error left once the exact
+    result is rounded into the output type."""
+    y = np.asarray(y, dtype=np.float64)
+    r = float(np.sqrt(np.mean(y * y))) if y.size else 0.0
+    d = float(np.sqrt(np.mean((np.asarray(x, dtype=np.float64) - round_to(y, dtype)) ** 2))) if y.size else 0.0
     return d / r if r > 0 else d
 
 
@@ -94,7 +116,7 @@ def assert_parity(out, conv_state_dev, ref, seqs=None, tol=TOL):
 
     o = pick(out["o"])
     e_o = max_rel_err_rounded(o, ref["o"], out["o"].dtype)
-    r_o = rel_rmse(o, ref["o"])
+    r_o = rel_rmse_rounded(o, ref["o"], out["o"].dtype)
     e_s = max_rel_err(pick(out["inter_ssm"]), ref["inter_ssm"])
     assert np.array_equal(pick(out["conv_snapshots"]), ref["conv_snapshots"]), "conv snapshots differ"
     assert np.array_equal(pick(conv_state_dev), ref["conv_state"]), "rolled conv_state differs"
@@ -119,7 +141,7 @@ def assert_decode_parity(o, S_final, conv_state_dev, ref, seqs=None, t=-1, tol=T
     y_o = ref["o"][:, toks]
     x_o = pick(o)
     e_o = max_rel_err_rounded(x_o, y_o, o.dtype)
-    r_o = rel_rmse(x_o, y_o)
+    r_o = rel_rmse_rounded(x_o, y_o, o.dtype)
     e_s = max_rel_err(pick(S_final), ref["inter_ssm"][:, t])
     assert e_o <= tol, f"o max rel err beyond output rounding {e_o:.3e} > {tol}"
     assert r_o <= tol, f"o rel rmse {r_o:.3e} > {tol}"

@@ -383,7 +383,9 @@ def test_head_dim_256(case):
                 assert torch.equal(first[0][key], out[key]), (plan, key)
 
 
-def _random_cases(n=24, seed=2026):
+def _random_cases(n=None, seed=2026):
+    # KDA_RANDOM_CASES sets how many (default 24); the first 24 are always the same
+    n = int(os.environ.get("KDA_RANDOM_CASES", "24")) if n is None else n
     rng = np.random.default_rng(seed)
     cases = []
     while len(cases) < n:

@@ -3,7 +3,7 @@ the 2e-3 bound, a real 3e-3 error is not."""
 import numpy as np
 import torch
 
-from parity_util import TOL, max_rel_err, max_rel_err_rounded, rel_rmse
+from parity_util import TOL, max_rel_err, max_rel_err_rounded, rel_rmse, rel_rmse_rounded, round_to
 
 
 def test_bf16_rounding_alone_passes():
@@ -14,7 +14,30 @@ def test_bf16_rounding_alone_passes():
     x = torch.tensor(y, dtype=torch.float32).to(torch.bfloat16).double().numpy()
     assert max_rel_err(x, y) > TOL          # plain relative error exceeds 2e-3 ...
     assert max_rel_err_rounded(x, y, torch.bfloat16) == 0.0  # ... only by rounding
-    assert 1.3e-3 < rel_rmse(x, y) < 1.8e-3  # the bf16 floor
+    assert 1.3e-3 < rel_rmse(x, y) < 1.8e-3  # the bf16 floor against the unrounded value
+    assert rel_rmse_rounded(x, y, torch.bfloat16) == 0.0  # nothing left once y is rounded too
+
+
+def test_round_to_matches_a_single_rounding():
+    rng = np.random.default_rng(3)
+    y = rng.standard_normal(100000).astype(np.float32).astype(np.float64)  # exact in fp32
+    ref = torch.tensor(y, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(round_to(y, torch.bfloat16), ref)
+    assert np.array_equal(round_to(y, torch.float32), y)
+    ties = np.array([1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, -(1.0 + 2.0 ** -8)])  # halfway: to even
+    assert np.array_equal(round_to(ties, torch.bfloat16), np.array([1.0, 1.0 + 2 * 2.0 ** -7, -1.0]))
+
+
+def test_small_outputs_pass_on_rounding_alone():
+    # on a few hundred elements bf16 rounding alone can exceed 2e-3 RMS against
+    # the unrounded value; the rounded reference removes it
+    worst = 0.0
+    for seed in range(200):
+        y = np.random.default_rng(seed).standard_normal(288).astype(np.float32).astype(np.float64)
+        x = torch.tensor(y, dtype=torch.float32).to(torch.bfloat16).double().numpy()
+        worst = max(worst, rel_rmse(x, y))
+        assert rel_rmse_rounded(x, y, torch.bfloat16) == 0.0
+    assert worst > 1.8e-3
 
 
 def test_real_errors_fail():
@@ -25,6 +48,8 @@ def test_real_errors_fail():
     assert max_rel_err_rounded(x, y, torch.bfloat16) > TOL * 0.4
     xf = torch.tensor(bad).float().double().numpy()
     assert max_rel_err_rounded(xf, y, torch.float32) > TOL
+    # a systematic 3e-3 error stays visible in the RMS after rounding
+    assert rel_rmse_rounded(x, y, torch.bfloat16) > TOL
 
 
 def test_rms_floor_for_cancelled_elements():
