@@ -130,3 +130,42 @@ def test_decode_rejects_persistent_plans():
     with pytest.raises(kda.KdaError) as e:
         _decode(kda, inp, wl.gate, plan="pipe:64")
     assert e.value.code == -8
+
+
+def _random_decode_cases(seed=2027):
+    # KDA_RANDOM_CASES sets how many (default 24); the first 24 are always the same
+    import os
+    import numpy as np
+    n = int(os.environ.get("KDA_RANDOM_CASES", "24"))
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        K = int(rng.choice([32, 64, 128, 256]))
+        V = int(rng.choice([32, 64, 128, 256]))
+        H = int(rng.integers(1, 4))
+        HV = H * int(rng.choice([1, 2, 3, 4]))
+        T = int(rng.integers(1, 9))
+        N = int(rng.integers(1, 7))
+        act = str(rng.choice(["bf16", "f32"]))
+        gate = str(rng.choice(["softplus", "safe"]))
+        plans = [None] + [p for p in ("item:16", "item:32", "item:64", "item:128", "smem:32", "smem:64",
+                                      "smem:128", "item:64:0:0:kernel", "item:32:0:0:counter")
+                          if plan_built(p, K, V, decode=True, T=T, act=act, G=HV // H)]
+        plan = plans[int(rng.integers(0, len(plans)))]
+        cases.append((N, T, H, HV, K, V, act, gate, plan, 3000 + len(cases)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_decode_cases(),
+                         ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}_{}".format(*c[:9]))
+def test_random_decode_shapes_and_plans(case):
+    # the decode of random shapes and plans against the oracle's verify of the
+    # same inputs (its state after the last token, o, the rolled conv_state)
+    from linear_attention_speculative_gb300 import kda
+    N, T, H, HV, K, V, act, gate, plan, seed = case
+    wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=seed)
+    inp_cpu = wk.make_inputs(wl)
+    orc = oracle.verify(inp_cpu, gate)
+    dec = to_device(inp_cpu)
+    o = _decode(kda, dec, gate, plan)
+    assert_decode_parity(o, dec["S0"], dec["conv_state"], orc)

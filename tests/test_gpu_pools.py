@@ -148,3 +148,50 @@ def test_commit_indexed_rolls_back_into_pool_slots():
     untouched = [sl for sl in range(pl["PS"]) if sl not in {int(ss[n]) for n in live}]
     assert torch.equal(got["S_pool"][untouched], S_before[untouched])
     assert int(status.item()) == 0
+
+
+def _random_pool_cases(seed=2028):
+    # KDA_RANDOM_CASES sets how many (default 24); the first 24 are always the same
+    import os
+    n = int(os.environ.get("KDA_RANDOM_CASES", "24"))
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        K = int(rng.choice([32, 64, 128]))
+        V = int(rng.choice([32, 64, 128]))
+        H = int(rng.integers(1, 3))
+        HV = H * int(rng.choice([1, 2, 4]))
+        T = int(rng.integers(1, 7))
+        N = int(rng.integers(2, 7))
+        gate = str(rng.choice(["softplus", "safe"]))
+        from parity_util import plan_built
+        plans = [None] + [p for p in ("item:32", "item:64", "item:128", "smem:64", "smem:128", "pipe:64",
+                                      "pipe:128", "split:32", "split:64", "split:128")
+                          if plan_built(p, K, V, T=T, G=HV // H)]
+        plan = plans[int(rng.integers(0, len(plans)))]
+        n_pad = int(rng.integers(0, N))  # padding sequences among the N
+        pad = tuple(sorted(rng.choice(N, size=n_pad, replace=False).tolist())) if n_pad else ()
+        cases.append((N, T, H, HV, K, V, gate, plan, pad, 5000 + len(cases)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_pool_cases(),
+                         ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}_pad{}".format(*c[:7], c[7], len(c[8])))
+def test_random_pools_match_the_oracle(case):
+    # random shapes, plans and slot maps (shuffled slots, padding sequences):
+    # the live sequences' outputs in their pool slots against the oracle
+    from linear_attention_speculative_gb300 import kda
+    N, T, H, HV, K, V, gate, plan, pad, seed = case
+    wl = wk.custom(N, T, H, HV, K, V, gate=gate, seed=seed)
+    inp, live, pl = _pools(wl, seed=seed, pad=pad)
+    got = _run_indexed(kda, wl, inp, pl, plan)
+    si = pl["slot_i"].long()
+    if live:
+        ref = oracle.verify(inp, wl.gate, seqs=live, threads=4)
+        out = {"o": got["o"][live], "inter_ssm": got["inter"][si[live]],
+               "conv_snapshots": got["snaps"][si[live]]}
+        assert_parity(out, got["cs_pool"][pl["slot_c"].long()[live]], ref)
+    for n in pad:
+        assert bool((got["o"][n] == 5.0).all())
+    assert torch.equal(got["S_pool"].cpu(), pl["S_pool"])  # the state pool is read only
+    assert kda.read_status(got["shape"], got["ws"]) == 0
