@@ -80,3 +80,44 @@ def test_commit_in_place_into_the_verified_state():
     for n, a in enumerate(acc.tolist()):
         assert torch.equal(inp["S0"][n], out["inter_ssm"][n, a - 1])
         assert torch.equal(inp["conv_state"][n], out["conv_snapshots"][n, a - 1])
+
+
+def _random_commit_cases(seed=2029):
+    # KDA_RANDOM_CASES sets how many (default 24); the first 24 are always the same
+    import os
+    n = int(os.environ.get("KDA_RANDOM_CASES", "24"))
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        K = int(rng.choice([32, 64, 128, 256]))
+        V = int(rng.choice([32, 64, 128, 256]))
+        H = int(rng.integers(1, 4))
+        HV = H * int(rng.choice([1, 2, 3, 4]))
+        T = int(rng.integers(1, 17))
+        N = int(rng.integers(1, 9))
+        act = str(rng.choice(["bf16", "f32"]))
+        acc = [int(rng.integers(1, T + 1)) for _ in range(N)]
+        cases.append((N, T, H, HV, K, V, act, tuple(acc), 7000 + i))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_commit_cases(),
+                         ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}".format(*c[:7]))
+def test_random_commit_matches_the_oracle(case):
+    # random shapes and accepted counts: the committed state and conv_state
+    # bit for bit against the oracle's commit of the same snapshots
+    from linear_attention_speculative_gb300 import kda
+    N, T, H, HV, K, V, act, acc_l, seed = case
+    wl = wk.custom(N, T, H, HV, K, V, act=act, seed=seed)
+    inp = to_device(wk.make_inputs(wl))
+    out = kda.run(dict(inp, conv_state=inp["conv_state"].clone()), wl.gate)
+    acc = torch.tensor(acc_l, dtype=torch.int32, device="cuda")
+    S = torch.full_like(inp["S0"], 7.0)
+    cs = torch.full_like(inp["conv_state"], 3.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.commit(acc, out["inter_ssm"], out["conv_snapshots"], S, cs, status=status)
+    torch.cuda.synchronize()
+    ref = oracle.commit(list(acc_l), out["inter_ssm"].cpu(), out["conv_snapshots"].cpu())
+    np.testing.assert_array_equal(S.double().cpu().numpy(), ref["S"])
+    np.testing.assert_array_equal(cs.double().cpu().numpy(), ref["conv_state"])
+    assert int(status.item()) == 0
