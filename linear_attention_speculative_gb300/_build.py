@@ -1,9 +1,9 @@
 """Build the CUDA library (sm_103a) in-tree with nvcc.
 
-Ten translation units are compiled in parallel (the C ABI, one unit per
+Eleven translation units are compiled in parallel (the C ABI, one unit per
 verify kernel family and activation type -- one item per CTA, pipelined,
-split -- the q/k conv_state roll kernel, the commit kernel, and the
-allocation-free entry point) and linked into
+split -- the q/k conv_state roll kernel, the commit kernel, the
+allocation-free entry point, and the bounded-wait self-test) and linked into
 ``_lib/libkda_gb300.so``.  The shared CUDA runtime is used so the library and
 PyTorch share one runtime instance.
 """
@@ -23,7 +23,7 @@ OBJ_DIR = os.path.join(LIB_DIR, "obj")
 LIB_PATH = os.path.join(LIB_DIR, "libkda_gb300.so")
 SOURCES = ("kda_api.cu", "kda_inst_tile_bf16.cu", "kda_inst_tile_f32.cu", "kda_inst_pipe_bf16.cu",
            "kda_inst_pipe_f32.cu", "kda_inst_split_bf16.cu", "kda_inst_split_f32.cu", "kda_roll.cu",
-           "kda_commit.cu", "kda_noalloc.cu")
+           "kda_commit.cu", "kda_noalloc.cu", "kda_selftest.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -37,7 +37,7 @@ EXPORTED = ("kda_conv_verify", "kda_conv_verify_variant", "kda_conv_verify_plan"
             "kda_conv_verify_indexed", "kda_conv_decode", "kda_commit", "kda_commit_indexed",
             "kda_conv_verify_noalloc", "kda_noalloc_read_status", "kda_workspace_bytes",
             "kda_make_plan", "kda_make_decode_plan", "kda_resolve_plan", "kda_read_status",
-            "kda_strerror", "kda_version")
+            "kda_selftest_bounded_wait", "kda_strerror", "kda_version")
 NOALLOC_MAX_SCRATCH_BYTES = 256 * 1024
 
 
@@ -120,6 +120,8 @@ def _load():
     L.kda_resolve_plan.argtypes = [sp, ctypes.c_int, ctypes.c_int, ctypes.POINTER(KdaPlan)]
     L.kda_read_status.restype = ctypes.c_int
     L.kda_read_status.argtypes = [sp, vp, ctypes.POINTER(ctypes.c_int), vp]
+    L.kda_selftest_bounded_wait.restype = ctypes.c_int
+    L.kda_selftest_bounded_wait.argtypes = [ctypes.c_int, ctypes.c_longlong, vp, vp]
     L.kda_strerror.restype = ctypes.c_char_p
     L.kda_strerror.argtypes = [ctypes.c_int]
     L.kda_version.restype = ctypes.c_int
@@ -356,6 +358,17 @@ def run(inputs: Dict[str, torch.Tensor], gate: str, variant: str = "auto",
                 out["o"], out["inter_ssm"], out["conv_snapshots"], ws, stream=stream,
                 variant=variant, shape=shape, plan=plan)
     return out
+
+
+def selftest_bounded_wait(mode: int, limit_ns: int = 0, stream=None):
+    """Run the kernels' bounded waits until they give up (no fault); returns
+    (status word, mask of the waits that gave up: 1 one-item, 2 pipelined)."""
+    out = torch.zeros(2, dtype=torch.int32, device="cuda")
+    rc = lib().kda_selftest_bounded_wait(int(mode), int(limit_ns), _ptr(out), _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_selftest_bounded_wait")
+    torch.cuda.synchronize()
+    return int(out[0]), int(out[1])
 
 
 def plan_label(plan: KdaPlan) -> str:

@@ -404,3 +404,13 @@ def test_plan_head_dim_256_layout(kda):
     assert kda.resolve_plan(s, 152, "smem:32").warps == 4
     for bad in ("item:128", "smem:128", "item:8", "pipe:64"):  # 16 warps / 1 warp / pipelined: not built
         assert _call_plan(kda, s, _fake_args(kda), kda.parse_plan(bad)) == -8, bad
+
+
+def test_selftest_rejects_bad_arguments_on_the_host(kda):
+    # checked before any CUDA call (no GPU here)
+    L = kda.lib()
+    st = ctypes.c_void_p(0x7f0000000000)
+    assert L.kda_selftest_bounded_wait(0, 1000, None, None) == -1
+    assert L.kda_selftest_bounded_wait(3, 1000, st, None) == -2
+    assert L.kda_selftest_bounded_wait(0, -1, st, None) == -2
+    assert L.kda_selftest_bounded_wait(0, 3_000_000_000, st, None) == -2
