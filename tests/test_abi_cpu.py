@@ -414,3 +414,34 @@ def test_selftest_rejects_bad_arguments_on_the_host(kda):
     assert L.kda_selftest_bounded_wait(3, 1000, st, None) == -2
     assert L.kda_selftest_bounded_wait(0, -1, st, None) == -2
     assert L.kda_selftest_bounded_wait(0, 3_000_000_000, st, None) == -2
+
+
+def test_dispatcher_invariants_over_random_shapes(kda):
+    # whatever the shape, the dispatcher's plans are well formed: the tile
+    # width divides V and matches the warps, one item per (sequence, v-head,
+    # tile), a grid that covers them, one or two launches, and the plan
+    # resolves to itself; the decode dispatcher never picks a variant without
+    # a decode form
+    import numpy as np
+    rng = np.random.default_rng(77)
+    wc = {32: 16, 64: 16, 128: 16, 256: 8}
+    for _ in range(3000):
+        K = int(rng.choice([32, 64, 128, 256]))
+        V = int(rng.choice([32, 64, 128, 256]))
+        H = int(rng.integers(1, 65))
+        HV = H * int(rng.choice([1, 2, 3, 4, 8]))
+        N = int(rng.integers(1, 2049))
+        T = int(rng.integers(1, 17))
+        act = str(rng.choice(["bf16", "f32"]))
+        s = kda.make_shape(N, T, H, HV, K, V, act)
+        for decode in (False, True):
+            p = kda.make_plan(s, 152, decode=decode)
+            assert V % p.bv == 0 and p.bv == p.warps * wc[K], (N, T, H, HV, K, V, decode)
+            assert p.items == N * HV * (V // p.bv)
+            assert 1 <= p.grid and (p.grid == p.items or p.variant == kda.VARIANT_PIPELINED)
+            assert p.launches in (1, 2) and p.ctas_per_sm >= 1
+            if decode:
+                assert p.variant in (kda.VARIANT_ONE_ITEM, kda.VARIANT_ONE_ITEM_SMEM)
+            label = kda.plan_label(p)
+            q = kda.resolve_plan(s, 152, label, decode=decode)
+            assert (q.variant, q.bv, q.warps, q.items, q.grid) == (p.variant, p.bv, p.warps, p.items, p.grid)
