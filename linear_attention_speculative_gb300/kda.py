@@ -186,6 +186,86 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
+# ---- argument checks of the Python entry points ------------------------------
+# The C ABI takes raw pointers and cannot know the size of a buffer; here each
+# tensor is checked against the shape the call implies (its layout in
+# include/kda_verify.h), so a wrong-sized, wrongly typed, strided or host
+# tensor raises ValueError instead of being read or written out of bounds.
+# validate=False skips the checks (to exercise the library's own rejections).
+
+def _act(shape: KdaShape):
+    return torch.bfloat16 if shape.act == BF16 else torch.float32
+
+
+def _expect(name, t, dims, dtype, rows=None, optional=False):
+    """t: a contiguous tensor of `dtype` and shape `dims`; rows, when given,
+    replaces the first dimension by a lower bound (state pools).  That every
+    tensor lives on the GPU is checked last (_on_cuda), once the shapes are."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name} is required")
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    got = tuple(t.shape)
+    want = tuple(int(d) for d in dims)
+    if rows is None:
+        ok = got == want
+    else:
+        ok = len(got) == len(want) and got[1:] == want[1:] and got[0] >= rows
+        want = (f">={rows}",) + want[1:]
+    if not ok:
+        raise ValueError(f"{name} must have shape {want}, got {got}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _on_cuda(**tensors):
+    for name, t in tensors.items():
+        if t is not None and t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
+
+
+def _check_inputs(shape: KdaShape, gate, mixed_qkv, conv_w, A_log, dt_bias, a, b):
+    N, T, H, HV, K, V = shape.N, shape.T, shape.H, shape.HV, shape.K, shape.V
+    dim, act = 2 * H * K + HV * V, _act(shape)
+    softplus = gate in ("softplus", GATE_SOFTPLUS)
+    _expect("mixed_qkv", mixed_qkv, (N, T, dim), act)
+    _expect("conv_w", conv_w, (dim, 4), act)
+    _expect("A_log", A_log, (HV,), torch.float32, optional=not softplus)
+    _expect("dt_bias", dt_bias, (HV, K), torch.float32, optional=not softplus)
+    _expect("a", a, (N, T, HV, K), act)
+    _expect("b", b, (N, T, HV), act)
+    return dim, act
+
+
+def _pool_rows(shape: KdaShape, idx: Optional["KdaStateIndices"]):
+    """Rows each state pool must hold: its pool size where the call gives
+    slots for it, else N."""
+    N = shape.N
+    if idx is None:
+        return N, N, N
+    return (idx.state_pool if idx.cache_indices else N,
+            idx.conv_pool if idx.conv_state_indices else N,
+            idx.inter_pool if idx.intermediate_state_indices else N)
+
+
+def _check_verify(shape, gate, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, o,
+                  inter_ssm, conv_snapshots, idx=None):
+    N, T, HV, K, V = shape.N, shape.T, shape.HV, shape.K, shape.V
+    dim, act = _check_inputs(shape, gate, mixed_qkv, conv_w, A_log, dt_bias, a, b)
+    rs, rc, ri = _pool_rows(shape, idx)
+    _expect("conv_state", conv_state, (rc, dim, 3), act, rows=rc)
+    _expect("S0", S0, (rs, HV, K, V), torch.float32, rows=rs)
+    _expect("o", o, (N, T, HV, V), act)
+    _expect("inter_ssm", inter_ssm, (ri, T, HV, K, V), torch.float32, rows=ri)
+    _expect("conv_snapshots", conv_snapshots, (ri, T, dim, 3), act, rows=ri)
+    _on_cuda(mixed_qkv=mixed_qkv, conv_w=conv_w, conv_state=conv_state, A_log=A_log, dt_bias=dt_bias,
+             a=a, b=b, S0=S0, o=o, inter_ssm=inter_ssm, conv_snapshots=conv_snapshots)
+
+
 def _stream_handle(stream) -> ctypes.c_void_p:
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -213,15 +293,19 @@ def parse_plan(spec: str) -> KdaPlan:
 
 def conv_verify(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: str,
                 o, inter_ssm, conv_snapshots, workspace, stream=None, variant: str = "auto",
-                shape: Optional[KdaShape] = None, plan=None) -> None:
+                shape: Optional[KdaShape] = None, plan=None, validate: bool = True) -> None:
     """Launch the fused verify decode on `stream` (default: current stream).
 
-    Tensors must be contiguous CUDA tensors in the layouts of the header;
-    conv_state is updated in place; o / inter_ssm / conv_snapshots are
-    written.  `plan` (a KdaPlan or a 'item:32'-style string) overrides the
-    dispatcher.  Raises KdaError on any non-zero return code."""
+    Tensors must be contiguous CUDA tensors in the layouts of the header
+    (checked unless validate=False; ValueError otherwise); conv_state is
+    updated in place; o / inter_ssm / conv_snapshots are written.  `plan` (a
+    KdaPlan or a 'item:32'-style string) overrides the dispatcher.  Raises
+    KdaError on any non-zero return code."""
     if shape is None:
         shape = shape_of(mixed_qkv, a, S0)
+    if validate:
+        _check_verify(shape, gate, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, o,
+                      inter_ssm, conv_snapshots)
     gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
     args = (ctypes.byref(shape), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_state), _ptr(A_log),
             _ptr(dt_bias), _ptr(a), _ptr(b), _ptr(S0), gm, _ptr(o), _ptr(inter_ssm),
@@ -238,11 +322,14 @@ def conv_verify(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: s
 
 def conv_verify_noalloc(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, gate: str,
                         o, inter_ssm, conv_snapshots, stream=None,
-                        shape: Optional[KdaShape] = None) -> None:
+                        shape: Optional[KdaShape] = None, validate: bool = True) -> None:
     """The allocation-free entry point: no workspace argument, the scratch is
     the library's built-in device array (calls must not overlap on the GPU)."""
     if shape is None:
         shape = shape_of(mixed_qkv, a, S0)
+    if validate:
+        _check_verify(shape, gate, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, o,
+                      inter_ssm, conv_snapshots)
     gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
     rc = lib().kda_conv_verify_noalloc(
         ctypes.byref(shape), _ptr(mixed_qkv), _ptr(conv_w), _ptr(conv_state), _ptr(A_log),
@@ -270,9 +357,12 @@ STATUS_BAD_INDEX = 4
 
 def conv_verify_indexed(shape: KdaShape, idx: KdaStateIndices, mixed_qkv, conv_w, conv_state,
                         A_log, dt_bias, a, b, S0, gate: str, o, inter_ssm, conv_snapshots,
-                        workspace, stream=None, plan=None) -> None:
+                        workspace, stream=None, plan=None, validate: bool = True) -> None:
     """The verify over state pools (conv_state, S0, inter_ssm, conv_snapshots
     are pools addressed through `idx`; see kda_state_indices)."""
+    if validate:
+        _check_verify(shape, gate, mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S0, o,
+                      inter_ssm, conv_snapshots, idx)
     gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
     if isinstance(plan, str):
         plan = parse_plan(plan)
@@ -287,11 +377,19 @@ def conv_verify_indexed(shape: KdaShape, idx: KdaStateIndices, mixed_qkv, conv_w
 
 def conv_decode(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S, gate: str, o, workspace,
                 stream=None, plan=None, idx: Optional[KdaStateIndices] = None,
-                shape: Optional[KdaShape] = None) -> None:
+                shape: Optional[KdaShape] = None, validate: bool = True) -> None:
     """Plain decode: S (f32, the state pool or [N,HV,K,V]) is updated in place,
     conv_state rolled, o written; no snapshots."""
     if shape is None:
         shape = shape_of(mixed_qkv, a, S if idx is None else S[: mixed_qkv.shape[0]])
+    if validate:
+        dim, act = _check_inputs(shape, gate, mixed_qkv, conv_w, A_log, dt_bias, a, b)
+        rs, rc, _ = _pool_rows(shape, idx)
+        _expect("conv_state", conv_state, (rc, dim, 3), act, rows=rc)
+        _expect("S", S, (rs, shape.HV, shape.K, shape.V), torch.float32, rows=rs)
+        _expect("o", o, (shape.N, shape.T, shape.HV, shape.V), act)
+        _on_cuda(mixed_qkv=mixed_qkv, conv_w=conv_w, conv_state=conv_state, A_log=A_log,
+                 dt_bias=dt_bias, a=a, b=b, S=S, o=o)
     gm = GATE_SOFTPLUS if gate in ("softplus", GATE_SOFTPLUS) else GATE_SAFE
     if isinstance(plan, str):
         plan = parse_plan(plan)
@@ -304,8 +402,25 @@ def conv_decode(mixed_qkv, conv_w, conv_state, A_log, dt_bias, a, b, S, gate: st
         raise KdaError(rc, "kda_conv_decode")
 
 
+def _check_commit(shape, accepted, inter_ssm, conv_snapshots, S, conv_state, status, idx=None):
+    N, T, HV, K, V = shape.N, shape.T, shape.HV, shape.K, shape.V
+    dim, act = 2 * shape.H * K + HV * V, _act(shape)
+    rs, rc, ri = _pool_rows(shape, idx)
+    _expect("accepted", accepted, (N,), torch.int32)
+    _expect("inter_ssm", inter_ssm, (ri, T, HV, K, V), torch.float32, rows=ri)
+    _expect("conv_snapshots", conv_snapshots, (ri, T, dim, 3), act, rows=ri)
+    _expect("S", S, (rs, HV, K, V), torch.float32, rows=rs)
+    _expect("conv_state", conv_state, (rc, dim, 3), act, rows=rc)
+    if status is not None:
+        _expect("status", status, (1,), torch.int32, rows=1)
+    _on_cuda(accepted=accepted, inter_ssm=inter_ssm, conv_snapshots=conv_snapshots, S=S,
+             conv_state=conv_state, status=status)
+
+
 def commit_indexed(shape: KdaShape, idx: KdaStateIndices, accepted, inter_ssm, conv_snapshots,
-                   S, conv_state, status=None, stream=None) -> None:
+                   S, conv_state, status=None, stream=None, validate: bool = True) -> None:
+    if validate:
+        _check_commit(shape, accepted, inter_ssm, conv_snapshots, S, conv_state, status, idx)
     rc = lib().kda_commit_indexed(ctypes.byref(shape), ctypes.byref(idx), _ptr(accepted),
                                   _ptr(inter_ssm), _ptr(conv_snapshots), _ptr(S),
                                   _ptr(conv_state), _ptr(status), _stream_handle(stream))
@@ -314,7 +429,7 @@ def commit_indexed(shape: KdaShape, idx: KdaStateIndices, accepted, inter_ssm, c
 
 
 def commit(accepted, inter_ssm, conv_snapshots, S, conv_state, status=None, stream=None,
-           shape: Optional[KdaShape] = None) -> None:
+           shape: Optional[KdaShape] = None, validate: bool = True) -> None:
     """Accept accepted[n] (int32, device) verified tokens of every sequence:
     S[n] <- inter_ssm[n, acc-1], conv_state[n] <- conv_snapshots[n, acc-1]."""
     if shape is None:
@@ -322,6 +437,8 @@ def commit(accepted, inter_ssm, conv_snapshots, S, conv_state, status=None, stre
         dim = conv_snapshots.shape[2]
         H = (dim - HV * V) // (2 * K)
         shape = make_shape(N, T, H, HV, K, V, conv_snapshots.dtype)
+    if validate:
+        _check_commit(shape, accepted, inter_ssm, conv_snapshots, S, conv_state, status)
     rc = lib().kda_commit(ctypes.byref(shape), _ptr(accepted), _ptr(inter_ssm),
                           _ptr(conv_snapshots), _ptr(S), _ptr(conv_state), _ptr(status),
                           _stream_handle(stream))

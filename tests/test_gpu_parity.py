@@ -327,16 +327,21 @@ def test_rejects_bad_args_on_device():
     o = torch.empty((2, 2, 2, 128), dtype=torch.bfloat16, device="cuda")
     st = torch.empty((2, 2, 2, 128, 128), device="cuda")
     sn = torch.empty((2, 2, shape.HV * 128 + 4 * 128, 3), dtype=torch.bfloat16, device="cuda")
+    # the library's own checks (the binding's tensor checks bypassed)
     with pytest.raises(kda.KdaError) as e:  # output aliases an input
         kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
                         inp["dt_bias"], inp["a"], inp["b"], inp["S0"], "softplus", o,
-                        inp["S0"], sn, ws, shape=shape)
+                        inp["S0"], sn, ws, shape=shape, validate=False)
     assert e.value.code == -5
     with pytest.raises(kda.KdaError) as e:  # misaligned state pointer
         kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
                         inp["dt_bias"], inp["a"], inp["b"], inp["S0"].view(-1)[1:], "softplus",
-                        o, st, sn, ws, shape=shape)
+                        o, st, sn, ws, shape=shape, validate=False)
     assert e.value.code == -4
+    with pytest.raises(ValueError, match="inter_ssm must have shape"):  # the binding's check
+        kda.conv_verify(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
+                        inp["dt_bias"], inp["a"], inp["b"], inp["S0"], "softplus", o,
+                        inp["S0"], sn, ws, shape=shape)
 
 
 def _sweep_sample():
