@@ -140,7 +140,9 @@ VARIANT_NAME = {1: "one_item", 2: "pipelined", 3: "one_item_smem", 4: "split"}
 # the dispatcher in kda_api.cu do not change the kernels' code)
 COMMIT_SOURCES = ("kda_commit.cu", "kda_device.cuh")
 VERIFY_SOURCES = ("kda_kernel.cuh", "kda_device.cuh", "kda_launch.cuh", "kda_inst_tile_bf16.cu",
-                  "kda_inst_tile_f32.cu", "kda_inst_pipe_bf16.cu", "kda_inst_pipe_f32.cu",
+                  "kda_inst_tile_f32.cu", "kda_inst_tile_cl_bf16.cu", "kda_inst_tile_cl_f32.cu",
+                  "kda_inst_tile_dec_bf16.cu", "kda_inst_tile_dec_f32.cu",
+                  "kda_inst_pipe_bf16.cu", "kda_inst_pipe_f32.cu",
                   "kda_inst_split_bf16.cu", "kda_inst_split_f32.cu", "kda_roll.cu")
 
 
@@ -363,8 +365,8 @@ def run_ours(args, wl):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
-    step(validate=True)
-    for _ in range(max(3, args.warmup)):
+    step(validate=True)  # the first warm-up step
+    for _ in range(max(3, args.warmup) - 1):
         step()
     barrier()
 
@@ -580,18 +582,34 @@ def run_sweep(args):
         out = {k: v for k, v in wk.empty_outputs(wl, device=dev).items()}
         shape = kda.shape_of(inp["mixed_qkv"], inp["a"], inp["S0"])
         ws = kda.alloc_workspace(shape, dev)
-        auto = plan_label(kda.make_plan(shape, sms, "auto", decode=decode))
+        auto_plan = kda.make_plan(shape, sms, "auto", decode=decode)
+        auto = plan_label(auto_plan)
+        # who rolls the q/k conv_state when several items read it
+        shared = (s.HV // s.H) * (s.V // auto_plan.bv) > 1 and auto_plan.variant != kda.VARIANT_SPLIT
+        roll_names = {v: k for k, v in kda.QK_ROLL_NAMES.items()}
         alg = decode_bytes(s) if decode else s.algorithmic_bytes()
         row = {"workload": wl.name, "op": args.op if decode else "verify", "N": s.N, "T": s.T,
                "H": s.H, "HV": s.HV, "gate": wl.gate, "alg_bytes": alg,
-               "head_steps": s.head_steps, "auto": auto, "us": {}}
+               "head_steps": s.head_steps, "auto": auto,
+               "auto_roll": roll_names[auto_plan.qk_roll] if shared else "", "us": {}}
+        launched = {}
         for spec in plans:
             plan = None if spec == "auto" else spec
             if plan is not None:
                 try:  # a plan the library does not build for this point is left out
-                    kda.resolve_plan(shape, sms, plan, decode=decode)
+                    rp = kda.resolve_plan(shape, sms, plan, decode=decode)
                 except kda.KdaError:
                     continue
+                # explicit plans that resolve to the same launch (e.g. "item:64" and
+                # "item:64:0:0:cluster" where the dispatcher rolls by the cluster)
+                # are timed once: the minimum over repeats of one launch would
+                # bias "best" low
+                key = (rp.variant, rp.bv, rp.grid, rp.prefetch, rp.qk_roll)
+                if key in launched:
+                    row["us"][spec] = row["us"][launched[key]]
+                    row.setdefault("same_launch", {})[spec] = launched[key]
+                    continue
+                launched[key] = spec
 
             def step(validate=False):
                 if decode:
@@ -604,8 +622,8 @@ def run_sweep(args):
                                     inp["A_log"], inp["dt_bias"], inp["a"], inp["b"], inp["S0"],
                                     wl.gate, out["o"], out["inter_ssm"], out["conv_snapshots"], ws,
                                     stream=stream, shape=shape, plan=plan, validate=validate)
-            step(validate=True)
-            for _ in range(3):
+            step(validate=True)  # three warm-up launches, the first one checked
+            for _ in range(2):
                 step()
             times = []
             for i in range(K):
@@ -655,7 +673,9 @@ def sweep_report(path, peak_gbs, peak_src):
     out.append("")
     out.append(f"Peak: {peak_gbs:.1f} GB/s ({peak_src}, MEASURED_PEAKS.json hbm_gbs).  Times are the median of "
                "per-launch CUDA events with L2 flushed before each launch (258 MB written, then 258 MB read); "
-               "GB/s = algorithmic bytes / time.")
+               "GB/s = algorithmic bytes / time.  An explicit plan that resolves to the same launch as an "
+               "earlier column (e.g. a q/k roll the dispatcher would pick anyway) is timed once and shares "
+               "that column's time.")
     out.append("")
     out.append("| T | N | H | HV | gate | auto plan | auto us | best plan | best us | auto/best | "
                "best GB/s | of peak | " + " | ".join(f"{p} us" for p in plans) + " |")
@@ -664,7 +684,8 @@ def sweep_report(path, peak_gbs, peak_src):
         best = r["best"]
         b_us = r["us"][best]
         gbs = r["alg_bytes"] / (b_us / 1e6) / 1e9
-        out.append(f"| {r['T']} | {r['N']} | {r['H']} | {r['HV']} | {r['gate']} | {r['auto']} | "
+        auto = r["auto"] + (f" ({r['auto_roll']})" if r.get("auto_roll") else "")
+        out.append(f"| {r['T']} | {r['N']} | {r['H']} | {r['HV']} | {r['gate']} | {auto} | "
                    f"{r['us']['auto']:.1f} | {best} | {b_us:.1f} | {r['us']['auto'] / b_us:.3f} | "
                    f"{gbs:.0f} | {gbs / peak_gbs:.3f} | "
                    + " | ".join(f"{r['us'][p]:.1f}" if p in r["us"] else "—" for p in plans) + " |")
@@ -700,8 +721,11 @@ def sweep_report(path, peak_gbs, peak_src):
             kinds = sorted({r["best"].split(":")[0] for r in rows if r["T"] == T and r["N"] * r["HV"] == u})
             cells.append("/".join(kinds) if kinds else "")
         out.append(f"| {T} | " + " | ".join(cells) + " |")
-    for kind, what in (("pipe", "Pipelined kernel"), ("split", "Split variant (prep kernel + recurrence kernel)")):
-        mine = [p for p in plans if p.startswith(kind + ":")]
+    for pick, what in ((lambda p: p.startswith("pipe:"), "Pipelined kernel"),
+                       (lambda p: p.startswith("split:"), "Split variant (prep kernel + recurrence kernel)"),
+                       (lambda p: p.endswith(":cluster"), "Cluster q/k roll (one-item kernel, a q/k group's "
+                        "items as one thread-block cluster)")):
+        mine = [p for p in plans if pick(p)]
         if not mine:
             continue
         out.append("")
@@ -743,8 +767,8 @@ def run_commit(args, wl):
     def step(validate=False):
         kda.commit(acc, out["inter_ssm"], out["conv_snapshots"], S, cs, stream=stream,
                    validate=validate)
-    step(validate=True)
-    for _ in range(max(3, args.warmup)):
+    step(validate=True)  # the first warm-up step
+    for _ in range(max(3, args.warmup) - 1):
         step()
     flush = L2Flush(dev)
     ev = []
@@ -793,8 +817,8 @@ def run_decode(args, wl):
     nbytes = decode_bytes(s)
     flush = nbytes < 2 * L2_BYTES
     fbuf = L2Flush(dev) if flush else None
-    step(validate=True)
-    for _ in range(max(3, args.warmup)):
+    step(validate=True)  # the first warm-up step
+    for _ in range(max(3, args.warmup) - 1):
         step()
     ev = []
     for i in range(args.steps):

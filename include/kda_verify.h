@@ -102,12 +102,18 @@ typedef struct {
    * requests every input one item ahead itself and ignores it (0). */
   int prefetch;
   /* When G * (V / bv) > 1 items read the same q/k channels: who rolls their
-   * conv_state (0 for SPLIT, whose first kernel rolls every channel).  KDA_QK_ROLL_COUNTER: the last of those items to arrive on a
-   * counter in the workspace, inside the verify kernel (one launch).
+   * conv_state (0 for SPLIT, whose first kernel rolls every channel).
+   * KDA_QK_ROLL_COUNTER: the last of those items to arrive on a counter in
+   * the workspace, inside the verify kernel (one launch).
    * KDA_QK_ROLL_KERNEL: a second, small kernel launched after the verify
    * kernel on the same stream (no atomics in the verify kernel; faster on
-   * large launches).  In a plan given to kda_conv_verify_plan,
-   * KDA_QK_ROLL_AUTO (0) lets the dispatcher choose. */
+   * large launches).  KDA_QK_ROLL_CLUSTER (ONE_ITEM with bv of 64 or 128
+   * columns, 32 or 64 at K = 256, and G * (V / bv) <= KDA_MAX_QK_CLUSTER):
+   * the items of a group run as one thread-block cluster whose first CTA
+   * rolls after a cluster barrier (one launch, no atomics; the dispatcher's
+   * pick below 4 waves of resident CTAs, where it is built).  In a plan
+   * given to kda_conv_verify_plan, KDA_QK_ROLL_AUTO (0) lets the dispatcher
+   * choose. */
   int qk_roll;
   /* Kernels one call with this plan launches (1 or 2). */
   int launches;
@@ -116,6 +122,8 @@ typedef struct {
 #define KDA_QK_ROLL_AUTO 0
 #define KDA_QK_ROLL_COUNTER 1
 #define KDA_QK_ROLL_KERNEL 2
+#define KDA_QK_ROLL_CLUSTER 3
+#define KDA_MAX_QK_CLUSTER 8  /* largest cluster of the cluster roll (portable size) */
 
 /* Error codes (negative: rejected on the host, nothing launched). */
 #define KDA_OK 0

@@ -21,7 +21,9 @@ CSRC = os.path.join(HERE, "csrc")
 LIB_DIR = os.path.join(HERE, "_lib")
 OBJ_DIR = os.path.join(LIB_DIR, "obj")
 LIB_PATH = os.path.join(LIB_DIR, "libkda_gb300.so")
-SOURCES = ("kda_api.cu", "kda_inst_tile_bf16.cu", "kda_inst_tile_f32.cu", "kda_inst_pipe_bf16.cu",
+SOURCES = ("kda_api.cu", "kda_inst_tile_bf16.cu", "kda_inst_tile_f32.cu", "kda_inst_tile_cl_bf16.cu",
+           "kda_inst_tile_cl_f32.cu", "kda_inst_tile_dec_bf16.cu", "kda_inst_tile_dec_f32.cu",
+           "kda_inst_pipe_bf16.cu",
            "kda_inst_pipe_f32.cu", "kda_inst_split_bf16.cu", "kda_inst_split_f32.cu", "kda_roll.cu",
            "kda_commit.cu", "kda_noalloc.cu", "kda_selftest.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -67,12 +67,23 @@ bool valid_sms_bv(int bv, int K, int V) {
   return (bv == 4 * wc || bv == 8 * wc) && fits_v(bv, V);
 }
 
+// The cluster q/k roll is built for the one-item kernel with the state in
+// registers at 4 or 8 warps, and for groups of at most KDA_MAX_QK_CLUSTER
+// items (a portable cluster size).
+bool cluster_roll_built(const kda_plan* plan, const kda_shape* s) {
+  const int wc = kda::warp_cols(s->K);
+  if (plan->variant != KDA_VARIANT_ONE_ITEM || (plan->bv != 4 * wc && plan->bv != 8 * wc)) return false;
+  if (!valid_tile_bv(plan->bv, s->K, s->V)) return false;
+  return (long long)(s->HV / s->H) * (s->V / plan->bv) <= KDA_MAX_QK_CLUSTER;
+}
+
 // A plan's tile width against its variant (decode: no pipelined variant;
 // the pipelined variant is built for K <= 128 and needs its shared memory --
 // two raw-input buffers and two stages besides the tile -- to fit one CTA).
 bool valid_plan(const kda_plan* plan, const kda_shape* s, bool decode) {
-  if (plan->qk_roll < KDA_QK_ROLL_AUTO || plan->qk_roll > KDA_QK_ROLL_KERNEL) return false;
+  if (plan->qk_roll < KDA_QK_ROLL_AUTO || plan->qk_roll > KDA_QK_ROLL_CLUSTER) return false;
   const int K = s->K, V = s->V;
+  if (plan->qk_roll == KDA_QK_ROLL_CLUSTER && !cluster_roll_built(plan, s)) return false;
   switch (plan->variant) {
     case KDA_VARIANT_ONE_ITEM: return valid_tile_bv(plan->bv, K, V);
     case KDA_VARIANT_PIPELINED:
@@ -120,7 +131,11 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
   // q/k conv_state roll when several items share a group's q/k channels: the
   // counter protocol costs the verify kernel a fence and an atomic round trip
   // per item (measured on GB300: 6-14 % on launches of many waves), the second
-  // kernel a launch (~2-3 us, which dominates small launches)
+  // kernel a launch (~2-3 us, which dominates small launches), the cluster
+  // launch slower CTA scheduling on many waves (up to 25 % at one token) but
+  // nothing per item: measured on GB300 over the sweep's 100 points with
+  // several items per group, below 4 waves it beats the counter by 4 % on
+  // average (verify and decode), above it loses to the second kernel
   const bool shared_qk = (long long)(s->HV / s->H) * (s->V / out->bv) > 1;
   if (out->variant == KDA_VARIANT_SPLIT) {
     // its first kernel rolls every channel of a group: no protocol needed
@@ -136,7 +151,7 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
   } else {
     out->qk_roll = out->items >= (long long)kQkRollKernelWaves * num_sms * out->ctas_per_sm
                        ? KDA_QK_ROLL_KERNEL
-                       : KDA_QK_ROLL_COUNTER;
+                       : (cluster_roll_built(out, s) ? KDA_QK_ROLL_CLUSTER : KDA_QK_ROLL_COUNTER);
   }
   out->launches = (shared_qk && out->qk_roll == KDA_QK_ROLL_KERNEL) ? 2 : 1;
   if (units == 0) out->grid = 0;
@@ -436,6 +451,8 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
   p.div_T = kda::make_fastdiv((uint32_t)p.T);
   const bool roll_kernel = plan.qk_roll == KDA_QK_ROLL_KERNEL && p.G * p.nvt > 1;
   p.qk_roll_kernel = roll_kernel ? 1 : 0;
+  // (valid_plan admits the cluster roll only where it is built)
+  p.qk_cluster = plan.qk_roll == KDA_QK_ROLL_CLUSTER && p.G * p.nvt > 1 ? p.G * p.nvt : 0;
 
   LaunchCfg cfg;
   cfg.K = s->K;
@@ -457,7 +474,16 @@ int launch_plan(const kda_shape* s, const void* mixed_qkv, const void* conv_w, v
                             : kda::launch_split_f32(tmap, p, cfg, prep_smem, st);
     return rc < 0 ? KDA_ERR_SHAPE : rc;
   }
-  if (s->act == KDA_BF16)
+  // decode launches whose q/k conv_state needs no counter run the
+  // counter-free decode kernels
+  const bool counter_free = cfg.decode && !cfg.pipe && (p.G * p.nvt == 1 || p.qk_roll_kernel);
+  if (p.qk_cluster > 1)
+    rc = s->act == KDA_BF16 ? kda::launch_tile_cluster_bf16(tmap, p, cfg, st)
+                            : kda::launch_tile_cluster_f32(tmap, p, cfg, st);
+  else if (counter_free)
+    rc = s->act == KDA_BF16 ? kda::launch_tile_decode_bf16(tmap, p, cfg, st)
+                            : kda::launch_tile_decode_f32(tmap, p, cfg, st);
+  else if (s->act == KDA_BF16)
     rc = cfg.pipe ? kda::launch_pipe_bf16(tmap, p, cfg, st) : kda::launch_tile_bf16(tmap, p, cfg, st);
   else
     rc = cfg.pipe ? kda::launch_pipe_f32(tmap, p, cfg, st) : kda::launch_tile_f32(tmap, p, cfg, st);

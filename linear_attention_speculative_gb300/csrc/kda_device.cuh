@@ -74,6 +74,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Thread-block cluster barrier, split in its two halves.  Every thread of
+// every CTA of the cluster arrives once (release: its earlier memory accesses
+// are ordered before the arrival) and later waits (acquire).  The wait ends
+// once all threads of the cluster have arrived; the hardware schedules the
+// CTAs of a cluster together, so a CTA that arrives before any wait of its
+// own never leaves another waiting forever.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

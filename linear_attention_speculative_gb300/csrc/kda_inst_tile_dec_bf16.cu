@@ -1,0 +1,9 @@
+// bf16-activation instantiations of the tile decode kernel without the arrival
+// counter.
+#include "kda_launch.cuh"
+
+namespace kda {
+int launch_tile_decode_bf16(const CUtensorMap& tmap, const Params& p, const LaunchCfg& cfg, cudaStream_t st) {
+  return launch_tile_decode_dispatch<__nv_bfloat16>(tmap, p, cfg, st);
+}
+}  // namespace kda

@@ -116,8 +116,12 @@ struct Params {
   int gate_mode;          // 0 softplus, 1 safe
   // one-item kernels with G * nvt > 1: 1 = the q/k conv_state is rolled by
   // the separate roll kernel (no arrival counters), 0 = by the last arrival
+  // or, with qk_cluster set, by the cluster
   int qk_roll_kernel;
   FastDiv div_nvt, div_HV, div_G, div_T;  // the divisors of the item and task decodes
+  // one-item kernels: > 1 = the launch is made of clusters of this many CTAs,
+  // the G * nvt items of one q/k group (the kernel's kRollCluster instantiation)
+  int qk_cluster;
 };
 
 constexpr int kConvW = 4;
@@ -1038,7 +1042,22 @@ __host__ __device__ constexpr int tile_min_blocks(int warps, bool sms) {
 // prep kernel (through the item's home), which also wrote the conv snapshots
 // and rolled the conv_state; launched as its programmatic dependent, the CTA
 // issues its state-tile load before waiting for the prep kernel.
-template <typename Act, int K, int WARPS, bool DEC = false, bool SMS = false, bool PRE = false>
+// RM, who rolls a q/k conv_state that several items read:
+//   kRollCounter  the last arrival on the group's counter, or the separate
+//                 roll kernel (Params::qk_roll_kernel), chosen at launch;
+//   kRollCluster  launched as clusters of the G * nvt items of one q/k group:
+//                 every CTA arrives on the cluster barrier once its
+//                 conv_state reads are done, and the cluster's first CTA rolls
+//                 the group's q/k conv_state after the wait;
+//   kRollNone     no counter in the kernel: one reader per group (which rolls
+//                 itself) or the separate roll kernel.  The decode kernels use
+//                 it where they can: without the counter's pointer and count
+//                 held across the recurrence they keep every value in
+//                 registers (3-5 % faster from three tokens on, measured).
+constexpr int kRollCounter = 0, kRollCluster = 1, kRollNone = 2;
+
+template <typename Act, int K, int WARPS, bool DEC = false, bool SMS = false, bool PRE = false,
+          int RM = kRollCounter>
 __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     kda_tile_kernel(const __grid_constant__ CUtensorMap tmap_s0, const Params p) {
   constexpr int BV = WARPS * warp_cols(K);
@@ -1104,16 +1123,20 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
       produce_tasks<Act, K, BV, DEC, SMS>(src, p, it, sQ, sK, sA, sV, sB, sRoll, tid, NT, nullptr, nullptr,
                                           issue);
     __syncthreads();  // every conv_state read of this CTA is done, stage written
+    // cluster protocol: this CTA's reads are done (their values are in shared
+    // memory); the matching wait comes before the q/k roll at the end
+    if constexpr (RM == kRollCluster) cluster_arrive_release();
     for (int r = warp; r < 2 * T; r += WARPS) l2norm_warp<K>(r < T ? sQ + r * KS : sK + (r - T) * KS, r < T, lane);
   }
   // Arrival on the q/k group counter by lane 0 of the last warp, after its
   // own rows (none while 2T < WARPS).  The returned count is first used at
   // the end of the CTA, so nothing waits here for the atomic's round trip.
-  // With the separate roll kernel there is no arrival and no q/k roll here;
-  // in the split variant the prep kernel rolls.
+  // With the separate roll kernel or the cluster there is no counter; in the
+  // split variant the prep kernel rolls.
   constexpr int kRollWarp = WARPS - 1;
   const int expected = p.G * p.nvt;
-  const bool counted = !PRE && expected > 1 && !p.qk_roll_kernel;
+  constexpr bool CL = RM == kRollCluster;
+  const bool counted = !PRE && RM == kRollCounter && expected > 1 && !p.qk_roll_kernel;
   int* cnt = p.counters + (size_t)it.n * p.H + it.h;
   int arrival = 0;
   if (warp == kRollWarp && lane == 0 && counted) {
@@ -1127,6 +1150,7 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
     if (tid == 0) atomicOr(p.status, kStatusTmaTimeout);
     if (warp == kRollWarp && lane == 0 && counted && arrival == expected - 1) atomicExch(cnt, 0);
     mbar_wait_bounded(mbar, 0, kWaitLimitNs);
+    if constexpr (CL) cluster_wait_acquire();  // every thread arrived before its own waits
     return;
   }
   if constexpr (SMS) {
@@ -1140,9 +1164,13 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   constexpr int NQV = 2 * K / ActT<Act>::VEC;  // q/k channel vectors
   constexpr int NCV = NQV + BV / ActT<Act>::VEC;
   roll_staged<Act, K, BV>(p, it, sRoll, NQV, NCV, tid, NT);  // v: owned by this item
+  // cluster: every CTA of the group has read its q/k conv_state once the wait
+  // ends; rank 0 rolls
+  if constexpr (CL) cluster_wait_acquire();
   if (warp == kRollWarp) {
     // q/k: the group's last arrival resets the counter and rolls
-    const int last = __shfl_sync(0xffffffffu, expected == 1 || (counted && arrival == expected - 1) ? 1 : 0, 0);
+    const int last = __shfl_sync(0xffffffffu, expected == 1 || (counted && arrival == expected - 1) ||
+                                                  (CL && cluster_cta_rank() == 0) ? 1 : 0, 0);
     if (last) {
       if (lane == 0 && counted) {
         atomicExch(cnt, 0);

@@ -272,13 +272,16 @@ def _stream_handle(stream) -> ctypes.c_void_p:
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-QK_ROLL_AUTO, QK_ROLL_COUNTER, QK_ROLL_KERNEL = 0, 1, 2
+QK_ROLL_AUTO, QK_ROLL_COUNTER, QK_ROLL_KERNEL, QK_ROLL_CLUSTER = 0, 1, 2, 3
+QK_ROLL_NAMES = {"auto": QK_ROLL_AUTO, "counter": QK_ROLL_COUNTER, "kernel": QK_ROLL_KERNEL,
+                 "cluster": QK_ROLL_CLUSTER}
 
 
 def parse_plan(spec: str) -> KdaPlan:
     """'item:32' / 'pipe:128' / 'smem:128' / 'pipe:128:300' / 'item:128:0:-1' /
     'smem:128:0:0:kernel' (variant, v-tile width, grid, L2 prefetch distance: -1 off,
-    0 default, q/k conv_state roll: 'counter' or 'kernel', default the dispatcher's)."""
+    0 default, q/k conv_state roll: 'counter', 'kernel' or 'cluster', default the
+    dispatcher's)."""
     parts = spec.split(":")
     plan = KdaPlan()
     plan.variant = {"item": VARIANT_ONE_ITEM, "pipe": VARIANT_PIPELINED,
@@ -286,8 +289,7 @@ def parse_plan(spec: str) -> KdaPlan:
     plan.bv = int(parts[1])
     plan.grid = int(parts[2]) if len(parts) > 2 else 0
     plan.prefetch = int(parts[3]) if len(parts) > 3 else 0
-    plan.qk_roll = {"auto": QK_ROLL_AUTO, "counter": QK_ROLL_COUNTER,
-                    "kernel": QK_ROLL_KERNEL}[parts[4]] if len(parts) > 4 else QK_ROLL_AUTO
+    plan.qk_roll = QK_ROLL_NAMES[parts[4]] if len(parts) > 4 else QK_ROLL_AUTO
     return plan
 
 

@@ -204,6 +204,11 @@ def plan_built(plan, K, V, decode=False, T=1, act="bf16", G=1) -> bool:
     wc = 8 if K == 256 else 16
     if bv > V or V % bv:
         return False
+    if plan.split(":")[4:5] == ["cluster"]:
+        # the cluster roll: the one-item kernel with the state in registers at
+        # 4 or 8 warps, a group of at most 8 items
+        if kind != "item" or bv not in (4 * wc, 8 * wc) or G * (V // bv) > 8:
+            return False
     if kind == "split":
         return (K <= 128 and not decode and bv in (32, 64, 128)
                 and split_fits(K, V, T, bv, G, act))

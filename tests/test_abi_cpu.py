@@ -122,8 +122,18 @@ def test_plan_picks_the_qk_roll(kda):
     p = kda.make_plan(kda.make_shape(512, 1, 32, 64), 152)
     assert kda.plan_label(p) == "item:64"
     assert p.qk_roll == kda.QK_ROLL_KERNEL and p.launches == 2
-    # two readers, a fraction of a wave: the counter, one launch
+    # four readers (two v-heads x two 64-column tiles), a fraction of a wave:
+    # one cluster per group, one launch
     p = kda.make_plan(kda.make_shape(2, 1, 16, 32), 152)
+    assert kda.plan_label(p) == "item:64"
+    assert p.qk_roll == kda.QK_ROLL_CLUSTER and p.launches == 1
+    # the same below 4 waves for the plain decode; a group of more than 8
+    # items (G = 16) cannot be one portable cluster: the counter
+    p = kda.make_plan(kda.make_shape(8, 1, 8, 32), 152, decode=True)  # 4 v-heads x 2 tiles
+    assert kda.plan_label(p) == "item:64" and p.qk_roll == kda.QK_ROLL_CLUSTER
+    p = kda.make_plan(kda.make_shape(8, 1, 4, 32), 152, decode=True)  # 8 v-heads x 2 tiles
+    assert p.qk_roll == kda.QK_ROLL_COUNTER
+    p = kda.make_plan(kda.make_shape(2, 4, 2, 32), 152)
     assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
     # the pipelined variant: the same choice by items per resident CTA
     p = kda.make_plan(kda.make_shape(512, 4, 32, 64), 152, "pipelined")
@@ -142,9 +152,38 @@ def test_resolve_plan_fills_derived_fields(kda):
         kda.resolve_plan(s, 152, "pipe:64", decode=True)
 
 
+def test_cluster_roll_plans(kda):
+    # the items of a q/k group as one cluster: one launch, one-item kernels only,
+    # at most 8 items per group
+    s = kda.make_shape(64, 4, 8, 32)  # G = 4
+    p = kda.resolve_plan(s, 152, "item:128:0:0:cluster")
+    assert p.qk_roll == kda.QK_ROLL_CLUSTER and p.launches == 1 and p.grid == 64 * 32
+    p = kda.resolve_plan(s, 152, "item:64:0:0:cluster")  # 4 v-heads x 2 tiles = 8
+    assert p.qk_roll == kda.QK_ROLL_CLUSTER and p.launches == 1
+    p = kda.resolve_plan(s, 152, "item:128:0:0:cluster", decode=True)
+    assert p.qk_roll == kda.QK_ROLL_CLUSTER and p.launches == 1
+    # built for the register-state kernel at 4 or 8 warps, groups of <= 8 items
+    for bad in ("item:32:0:0:cluster",   # 2 warps (and 16 items per group)
+                "smem:128:0:0:cluster", "pipe:128:0:0:cluster", "split:128:0:0:cluster"):
+        with pytest.raises(kda.KdaError):
+            kda.resolve_plan(s, 152, bad)
+    s2 = kda.make_shape(4, 2, 2, 4, K=256, V=256)  # 4 warps = 32 columns at K = 256
+    assert kda.resolve_plan(s2, 152, "item:64:0:0:cluster").qk_roll == kda.QK_ROLL_CLUSTER  # 2 x 4
+    with pytest.raises(kda.KdaError):
+        kda.resolve_plan(s2, 152, "item:32:0:0:cluster")  # 2 x 8 items
+    # one item per group: nothing is shared, the request is moot
+    p = kda.resolve_plan(kda.make_shape(4, 4, 8, 8), 152, "item:128:0:0:cluster")
+    assert p.qk_roll == kda.QK_ROLL_COUNTER and p.launches == 1
+    # the grid is a whole number of clusters
+    for N, H, HV, bv in ((3, 2, 6, 64), (5, 1, 4, 128), (1, 3, 3, 64), (7, 2, 8, 128)):
+        p = kda.resolve_plan(kda.make_shape(N, 2, H, HV), 152, f"item:{bv}:0:0:cluster")
+        assert p.grid % ((HV // H) * (128 // bv)) == 0
+
+
 def test_plan_strings_carry_the_qk_roll(kda):
     assert kda.parse_plan("item:64").qk_roll == kda.QK_ROLL_AUTO
     assert kda.parse_plan("item:64:0:0:kernel").qk_roll == kda.QK_ROLL_KERNEL
+    assert kda.parse_plan("item:64:0:0:cluster").qk_roll == kda.QK_ROLL_CLUSTER
     assert kda.parse_plan("smem:128:0:-1:counter").qk_roll == kda.QK_ROLL_COUNTER
     with pytest.raises(KeyError):
         kda.parse_plan("item:64:0:0:sometimes")

@@ -58,6 +58,18 @@ def test_sweep_report_of_verify_and_decode_rows(tmp_path):
         assert ("kda_conv_decode" in text) == (op == "decode")
         assert "| 1 | 1 | 16 | 16 | softplus | item:128 | 10.4 | item:64 | 10.2 |" in text
         assert "own column / best: mean 1.0098" in text
+    # a grouped point: the dispatcher's q/k roll beside its plan, and the
+    # cluster plans' table against the dispatcher
+    row = {"workload": "sweep_T2_N8_H32_HV64_softplus", "op": "verify", "N": 8, "T": 2, "H": 32, "HV": 64,
+           "gate": "softplus", "alg_bytes": 100_000_000, "head_steps": 1024, "auto": "item:64",
+           "auto_roll": "cluster",
+           "us": {"auto": 24.8, "item:64": 24.6, "item:64:0:0:counter": 26.6, "item:64:0:0:cluster": 24.6},
+           "best": "item:64", "best_gbs": 1e8 / 24.6e-6 / 1e9, "auto_over_best": 24.8 / 24.6}
+    path = tmp_path / "grouped.jsonl"
+    path.write_text(json.dumps(row) + "\n")
+    text = bench.sweep_report(str(path), 6791.0, "measured")
+    assert "| 2 | 8 | 32 | 64 | softplus | item:64 (cluster) | 24.8 | item:64 | 24.6 |" in text
+    assert "Cluster q/k roll" in text and "| 2 | 0.99 |" in text
 
 
 def test_committed_ncu_summaries_match_the_kernel_sources():

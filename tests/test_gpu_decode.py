@@ -36,7 +36,8 @@ def _decode(kda, inp, gate, plan=None, idx=None):
 
 @pytest.mark.parametrize("plan", [None, "item:128", "item:32", "item:16:0:-1", "smem:128", "smem:64",
                                   "item:32:0:0:kernel", "smem:64:0:0:kernel", "smem:128:0:0:counter",
-                                  "item:64", "smem:32"])
+                                  "item:64", "smem:32", "item:128:0:0:cluster", "item:32:0:0:cluster",
+                                  "item:64:0:0:cluster"])
 @pytest.mark.parametrize("case", [(5, 4, 2, 4, 128, 128, "bf16", "softplus"),
                                   (3, 1, 2, 2, 128, 128, "bf16", "safe"),
                                   (4, 3, 1, 2, 64, 64, "f32", "softplus"),
@@ -45,7 +46,7 @@ def _decode(kda, inp, gate, plan=None, idx=None):
 def test_decode_equals_last_verify_snapshot(case, plan):
     from linear_attention_speculative_gb300 import kda
     N, T, H, HV, K, V, act, gate = case
-    if not plan_built(plan, K, V, decode=True):
+    if not plan_built(plan, K, V, decode=True, G=HV // H):
         pytest.skip("no such kernel for this shape")
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=91 + T)
     inp_cpu = wk.make_inputs(wl)

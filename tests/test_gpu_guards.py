@@ -76,9 +76,10 @@ def _verify_fenced(kda, wl, plan=None, pools=False):
 CASES = [
     (wk.custom(5, 3, 2, 4, 128, 128, seed=401), ("item:128", "item:16", "smem:128", "pipe:64",
                                                  "pipe:128:2", "split:32", "split:128", "item:128:0:0:kernel",
-                                                 "smem:128:0:0:kernel", "item:64:0:0:counter")),
+                                                 "smem:128:0:0:kernel", "item:64:0:0:counter",
+                                                 "item:128:0:0:cluster", "item:64:0:0:cluster")),
     (wk.custom(3, 2, 1, 2, 256, 256, seed=402), ("smem:64", "smem:32", "item:64", "item:16",
-                                                 "item:64:0:0:kernel")),
+                                                 "item:64:0:0:kernel", "item:64:0:0:cluster")),
     (wk.custom(4, 16, 2, 2, 32, 32, act="f32", seed=403), ("item:32", "item:16")),
     (wk.custom(4, 16, 2, 2, 32, 64, act="f32", seed=406), ("pipe:64", "pipe:64:1:0:counter")),
     (wk.custom(6, 1, 3, 6, 64, 128, gate="safe", seed=404), ("item:64", "smem:64", "pipe:64", "split:64",

@@ -29,7 +29,9 @@ ALL_PLANS = ("item:16", "item:32", "item:64", "item:128", "item:128:0:-1", "item
              "smem:64", "smem:128",
              # both ways of rolling a q/k conv_state that several items read
              "item:64:0:0:counter", "item:64:0:0:kernel", "smem:128:0:0:counter",
-             "smem:128:0:0:kernel", "smem:64:0:0:kernel")
+             "smem:128:0:0:kernel", "smem:64:0:0:kernel",
+             # ... and a group's items as one thread-block cluster
+             "item:128:0:0:cluster", "item:64:0:0:cluster", "item:128:0:-1:cluster")
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -112,6 +114,8 @@ def test_all_plans_bit_identical(wl):
 @pytest.mark.parametrize("plan", ALL_PLANS)
 def test_parity_every_plan_decode(plan):
     wl = wk.DECODE
+    if not plan_built(plan, wl.shape.K, wl.shape.V, T=wl.shape.T, act=wl.shape.act, G=wl.shape.G):
+        pytest.skip("no such kernel for this shape")
     inp = wk.make_inputs(wl)
     ref = oracle.verify(inp, wl.gate, threads=8)
     out, cs = run_kernel(inp, wl.gate, plan)
@@ -138,6 +142,8 @@ DET_CASES = [
     (wk.LARGE, "auto"),                        # single reader per q/k group
     (wk.GVA, "item:128:0:0:counter"),          # four readers, last-arrival counter
     (wk.GVA, "item:128:0:0:kernel"),           # four readers, second roll kernel
+    (wk.GVA, "item:128:0:0:cluster"),          # four readers, one cluster per group
+    (wk.GVA, "item:64:0:0:cluster"),           # eight readers (two v-tiles each), cluster of 8
     (wk.GVA, "pipe:128:0:0:counter"),          # pipelined kernel, counter
     (wk.GVA, "split:64"),                      # prep kernel + dependent recurrence kernel
     (wk.DECODE, "item:32"),                    # four v-tiles per state read q/k
@@ -415,6 +421,11 @@ def _random_cases(n=None, seed=2026):
 
 @pytest.mark.parametrize("case", _random_cases(), ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}_{}".format(*c[:9]))
 def test_random_shapes_and_plans(case):
+    _check_random_case(case)
+
+
+def _check_random_case(case):
+    # the plan against the oracle, and bit-identical to the dispatcher's plan
     N, T, H, HV, K, V, act, gate, plan, seed = case
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=seed)
     inp = wk.make_inputs(wl)
@@ -425,6 +436,37 @@ def test_random_shapes_and_plans(case):
     for key in ("o", "inter_ssm", "conv_snapshots"):
         assert torch.equal(out[key], auto[key]), key
     assert torch.equal(cs, auto_cs)
+
+
+def _random_cluster_cases(n=None, seed=2027):
+    # random shapes whose q/k groups span several items, each with a cluster
+    # roll plan (KDA_RANDOM_CASES sets how many, default 24)
+    n = int(os.environ.get("KDA_RANDOM_CASES", "24")) if n is None else n
+    rng = np.random.default_rng(seed)
+    cases = []
+    while len(cases) < n:
+        K = int(rng.choice([32, 64, 128, 256]))
+        V = int(rng.choice([32, 64, 128, 256]))
+        H = int(rng.integers(1, 4))
+        G = int(rng.choice([1, 2, 3, 4]))
+        T = int(rng.integers(1, 17))
+        N = int(rng.integers(1, 7))
+        act = str(rng.choice(["bf16", "f32"]))
+        gate = str(rng.choice(["softplus", "safe"]))
+        plans = [f"{p}:0:0:cluster" for p in ("item:32", "item:64", "item:128")
+                 if plan_built(f"{p}:0:0:cluster", K, V, T=T, act=act, G=G)
+                 and G * (V // int(p.split(":")[1])) > 1]
+        if not plans:
+            continue
+        plan = str(rng.choice(plans))
+        cases.append((N, T, H, H * G, K, V, act, gate, plan, 5000 + len(cases)))
+    return cases
+
+
+@pytest.mark.parametrize("case", _random_cluster_cases(),
+                         ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}_{}".format(*c[:9]))
+def test_random_cluster_roll_plans(case):
+    _check_random_case(case)
 
 
 ROLL_CASES = [
@@ -439,7 +481,7 @@ ROLL_CASES = [
 
 
 @pytest.mark.parametrize("case", ROLL_CASES, ids=lambda c: "N{}_T{}_H{}_HV{}_K{}_V{}_{}_{}".format(*c))
-def test_qk_roll_kernel_and_counter_match_the_oracle(case):
+def test_qk_roll_protocols_match_the_oracle(case):
     N, T, H, HV, K, V, act, gate = case
     wl = wk.custom(N, T, H, HV, K, V, act=act, gate=gate, seed=700 + T + K)
     inp = wk.make_inputs(wl)
@@ -449,8 +491,10 @@ def test_qk_roll_kernel_and_counter_match_the_oracle(case):
     outs = []
     for kind in kinds:
         bv = full
-        for roll in ("counter", "kernel"):
+        for roll in ("counter", "kernel", "cluster"):
             plan = f"{kind}:{bv}:0:0:{roll}"
+            if not plan_built(plan, K, V, T=T, act=act, G=HV // H):
+                continue
             out, cs = run_kernel(inp, gate, plan)
             assert_parity(out, cs, ref)
             outs.append((plan, out, cs))

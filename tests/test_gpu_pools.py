@@ -66,7 +66,8 @@ def _run_indexed(kda, wl, inp, pl, plan=None):
 
 @pytest.mark.parametrize("plan", [None, "item:128", "item:32", "pipe:64", "pipe:128:0:0:counter",
                                   "pipe:128:0:0:kernel", "split:32", "split:128",
-                                  "item:128:0:0:kernel", "item:32:0:0:counter", "smem:64:0:0:kernel"])
+                                  "item:128:0:0:kernel", "item:32:0:0:counter", "smem:64:0:0:kernel",
+                                  "item:128:0:0:cluster", "item:64:0:0:cluster"])
 def test_indexed_equals_dense_on_gathered_inputs(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(8, 3, 2, 4, 128, 128, seed=81)
@@ -100,7 +101,7 @@ def test_indexed_equals_dense_on_gathered_inputs(plan):
     assert kda.read_status(got["shape"], got["ws"]) == 0
 
 
-@pytest.mark.parametrize("plan", [None, "pipe:64", "split:64"])
+@pytest.mark.parametrize("plan", [None, "pipe:64", "split:64", "item:64:0:0:cluster"])
 def test_indexed_matches_the_oracle(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(6, 4, 2, 2, 128, 128, gate="safe", seed=82)
@@ -115,7 +116,7 @@ def test_indexed_matches_the_oracle(plan):
 
 
 @pytest.mark.parametrize("plan", [None, "item:128:0:0:counter", "item:128:0:0:kernel", "pipe:128",
-                                  "split:128"])
+                                  "split:128", "item:128:0:0:cluster"])
 def test_out_of_range_slot_skips_and_reports(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(4, 2, 2, 2, 128, 128, seed=83)  # two v-heads read each q/k head
