@@ -244,32 +244,30 @@ int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool de
     out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
     out->bv = full_bv;
   } else {
-    // One item per CTA, the state in registers: the fastest kernel at 145 of
+    // One item per CTA, the state in registers: the fastest kernel at 137 of
     // the 150 points of the configuration sweep (T in 1..8, N in 1..512, three
-    // head layouts, both gates; K = V = 128) and at 128 of the same 150 points
-    // for the plain decode.  Against the fastest explicit plan at each point
-    // the rules below measured within 0.04 % (verify) and 0.18 % (decode) on
-    // average, 1.3 % and 8.5 % at worst (single-digit-N points, where the
-    // event timer moves in ~2 us steps).
+    // head layouts, both gates; K = V = 128) and at 140 of the same 150 points
+    // for the plain decode.
     out->variant = KDA_VARIANT_ONE_ITEM;
     out->bv = full_bv;
     const int G = s->HV / s->H;
     if (s->K <= 128 && full_bv == 128) {
-      // Short calls over many units: the shared-memory state (3 CTAs per SM
-      // instead of 2) -- single-token verifies with one v-head per q/k head
-      // from 8 units per SM (+3..5 %); plain decodes from 8 (T = 1) and 16
-      // (T = 2) units per SM (+2..6 %).
-      const long long smem_from =
-          decode ? (s->T == 1 ? 8 : (s->T == 2 ? 16 : 0)) : (s->T == 1 && G == 1 ? 8 : 0);
+      // Single tokens over many units: the shared-memory state (3 CTAs per SM
+      // instead of 2) from 8 units per SM -- verifies with one v-head per q/k
+      // head (+3..5 %) and plain decodes (+2..5 %).  From two tokens on the
+      // register-state decode kernels are faster.
+      const long long smem_from = (s->T == 1 && (decode || G == 1)) ? 8 : 0;
+      const bool wide = decode ? (s->T == 1 || (s->T == 2 && (units >= 8LL * num_sms || 2 * units <= num_sms)))
+                               : (s->T <= 2 || 2 * units <= num_sms);
       if (smem_from > 0 && units >= smem_from * num_sms) {
         out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
-      } else if (G >= 2 && (s->T <= (decode ? 1 : 2) ||
-                            (2 * units <= num_sms && (!decode || s->T <= 3)))) {
-        // Several v-heads per q/k head: 64-column tiles for calls of up to
-        // two tokens (one for decode) and for at most half a unit per SM
-        // (twice the CTAs; +2..17 %; for decode only up to three tokens).
-        // Longer calls keep 128 columns: each 64-column item repeats the q/k
-        // conv of all T tokens.
+      } else if (G >= 2 && wide) {
+        // Several v-heads per q/k head: 64-column tiles (twice the CTAs) for
+        // verifies of up to two tokens and for at most half a unit per SM
+        // (+2..17 %); for plain decodes of one token, and of two tokens from
+        // 8 units per SM or at most half a unit per SM (+1..7 %).  Longer
+        // calls keep 128 columns: each 64-column item repeats the q/k conv
+        // of all T tokens.
         out->bv = 4 * kda::warp_cols(s->K);
       }
     }
