@@ -462,7 +462,11 @@ def test_dispatcher_invariants_over_random_shapes(kda):
     # width divides V and matches the warps, one item per (sequence, v-head,
     # tile), a grid that covers them, one or two launches, and the plan
     # resolves to itself; the decode dispatcher never picks a variant without
-    # a decode form
+    # a decode form.  A cluster q/k roll groups the items of one q/k head:
+    # at most 8 of them (a portable cluster), the register-state kernel at 4
+    # or 8 warps, a grid of whole clusters, and clusters that never span two
+    # sequences (a sequence's items are a whole number of groups), so a
+    # padding sequence skips whole clusters and every cluster barrier ends
     import numpy as np
     rng = np.random.default_rng(77)
     wc = {32: 16, 64: 16, 128: 16, 256: 8}
@@ -486,3 +490,12 @@ def test_dispatcher_invariants_over_random_shapes(kda):
             label = kda.plan_label(p)
             q = kda.resolve_plan(s, 152, label, decode=decode)
             assert (q.variant, q.bv, q.warps, q.items, q.grid) == (p.variant, p.bv, p.warps, p.items, p.grid)
+            group = (HV // H) * (V // p.bv)
+            if p.qk_roll == kda.QK_ROLL_CLUSTER:
+                assert 2 <= group <= 8 and p.variant == kda.VARIANT_ONE_ITEM and p.warps in (4, 8)
+                assert p.grid % group == 0 and (HV * (V // p.bv)) % group == 0
+                assert p.launches == 1
+                # below 4 waves of resident CTAs only; the roll kernel from there
+                assert p.items < 4 * 152 * p.ctas_per_sm
+            elif group > 1 and p.variant != kda.VARIANT_SPLIT:
+                assert p.qk_roll in (kda.QK_ROLL_COUNTER, kda.QK_ROLL_KERNEL)

@@ -265,7 +265,7 @@ def test_workspace_is_left_zeroed():
     assert kda.read_status(shape, ws) == 0
 
 
-@pytest.mark.parametrize("plan", [None, "pipe:128", "split:64"])
+@pytest.mark.parametrize("plan", [None, "pipe:128", "split:64", "item:128:0:0:cluster"])
 def test_side_streams_and_separate_workspaces(plan):
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(8, 4, 2, 4, 128, 128, seed=21)
@@ -285,11 +285,13 @@ def test_side_streams_and_separate_workspaces(plan):
         assert torch.equal(out["o"], ref["o"])
 
 
-@pytest.mark.parametrize("plan", [None, "item:128:0:0:counter", "item:128:0:0:kernel", "pipe:64",
+@pytest.mark.parametrize("plan", [None, "item:128:0:0:counter", "item:128:0:0:kernel",
+                                  "item:128:0:0:cluster", "item:64:0:0:cluster", "pipe:64",
                                   "pipe:128:0:0:kernel", "split:64", "split:128"])
 def test_cuda_graph_replay(plan):
-    # two v-heads per q/k head: the q/k conv_state roll runs by either protocol
-    # (the roll kernel as a programmatic dependent launch inside the graph)
+    # two v-heads per q/k head: the q/k conv_state roll runs by each protocol
+    # (the roll kernel as a programmatic dependent launch inside the graph, the
+    # cluster roll as a cluster launch captured in the graph)
     from linear_attention_speculative_gb300 import kda
     wl = wk.custom(4, 3, 2, 4, 128, 128, seed=23)
     inp_cpu = wk.make_inputs(wl)
