@@ -12,9 +12,12 @@
 // mixed_qkv[n, :, c]] as the verify kernel saw it.  Stream order is the only
 // synchronisation; the verify kernel needs no arrival counters for it.  The
 // launch is a programmatic dependent of the verify kernel: its CTAs may be
-// scheduled once every verify CTA has started, and each one first waits
-// (griddepcontrol.wait, a hardware dependency wait) until the verify grid has
-// completed and its writes are visible -- only the launch latency overlaps.
+// scheduled once every verify CTA has started.  A thread first loads what it
+// needs -- the new tokens, and for T < 3 the old q/k window, none of which the
+// verify kernel writes -- and only then waits (griddepcontrol.wait, a hardware
+// dependency wait) until the verify grid has completed, every read of the old
+// window included, before it stores: the launch and the loads overlap the
+// verify kernel's last wave.
 //
 // One thread per 16-byte vector of channels (8 bf16 / 4 fp32): it reads the
 // vector's 3 old values per channel when T < 3 and the last min(T, 3) token
@@ -30,7 +33,6 @@ constexpr int kRollThreads = 256;
 
 template <typename Act>
 __global__ void __launch_bounds__(kRollThreads) kda_qk_roll_kernel(const Params p, int K) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");  // the verify grid has completed
   using AT = ActT<Act>;
   using Raw = typename AT::Raw;
   constexpr int VEC = AT::VEC;
@@ -63,6 +65,8 @@ __global__ void __launch_bounds__(kRollThreads) kda_qk_roll_kernel(const Params 
 #pragma unroll
     for (int e = 0; e < VEC; ++e) r[e * (kConvW - 1) + j] = xv[e];
   }
+  // the verify grid has completed (its reads of the old window too)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 #pragma unroll
   for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
 }
