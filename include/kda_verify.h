@@ -111,7 +111,7 @@ typedef struct {
    * columns, 32 or 64 at K = 256, and G * (V / bv) <= KDA_MAX_QK_CLUSTER):
    * the items of a group run as one thread-block cluster whose first CTA
    * rolls after a cluster barrier (one launch, no atomics; the dispatcher's
-   * pick below 4 waves of resident CTAs, where it is built).  In a plan
+   * pick below 2 waves of resident CTAs, where it is built).  In a plan
    * given to kda_conv_verify_plan, KDA_QK_ROLL_AUTO (0) lets the dispatcher
    * choose. */
   int qk_roll;

@@ -44,8 +44,8 @@ int ctas_per_sm_for(int regs_limit, size_t smem) {
 }
 
 // Launches of at least this many waves of resident CTAs roll the shared q/k
-// conv_state with the second kernel instead of the counter.
-constexpr int kQkRollKernelWaves = 4;
+// conv_state with the second kernel instead of the cluster (or the counter).
+constexpr int kQkRollKernelWaves = 2;
 
 // v-tile widths of the one-item kernels: 1, 2, 4 or 8 warps of warp_cols(K)
 // columns each (16 columns for K <= 128, 8 for K = 256); the shared-memory
@@ -131,11 +131,12 @@ void finish_plan(const kda_shape* s, int num_sms, kda_plan* out, int requested_g
   // q/k conv_state roll when several items share a group's q/k channels: the
   // counter protocol costs the verify kernel a fence and an atomic round trip
   // per item (measured on GB300: 6-14 % on launches of many waves), the second
-  // kernel a launch (~2-3 us, which dominates small launches), the cluster
-  // launch slower CTA scheduling on many waves (up to 25 % at one token) but
-  // nothing per item: measured on GB300 over the sweep's 100 points with
-  // several items per group, below 4 waves it beats the counter by 4 % on
-  // average (verify and decode), above it loses to the second kernel
+  // kernel a launch and a dependency wait (its loads overlap the verify's
+  // last wave), the cluster launch slower CTA scheduling on many waves (up to
+  // 25 % at one token) but nothing per item.  Measured on GB300 over the
+  // sweep's 100 points with several items per group: below 2 waves the
+  // cluster is the fastest (2-6 % ahead of the second kernel, 4-8 % of the
+  // counter), from about 3 waves on the second kernel (4 % at 3.4 waves)
   const bool shared_qk = (long long)(s->HV / s->H) * (s->V / out->bv) > 1;
   if (out->variant == KDA_VARIANT_SPLIT) {
     // its first kernel rolls every channel of a group: no protocol needed

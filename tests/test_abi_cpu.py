@@ -495,7 +495,7 @@ def test_dispatcher_invariants_over_random_shapes(kda):
                 assert 2 <= group <= 8 and p.variant == kda.VARIANT_ONE_ITEM and p.warps in (4, 8)
                 assert p.grid % group == 0 and (HV * (V // p.bv)) % group == 0
                 assert p.launches == 1
-                # below 4 waves of resident CTAs only; the roll kernel from there
-                assert p.items < 4 * 152 * p.ctas_per_sm
+                # below 2 waves of resident CTAs only; the roll kernel from there
+                assert p.items < 2 * 152 * p.ctas_per_sm
             elif group > 1 and p.variant != kda.VARIANT_SPLIT:
                 assert p.qk_roll in (kda.QK_ROLL_COUNTER, kda.QK_ROLL_KERNEL)
