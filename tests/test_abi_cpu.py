@@ -94,15 +94,15 @@ def test_plan_auto_uses_one_item_per_cta(kda):
 def test_decode_plan(kda):
     # kda_conv_decode's dispatcher: the shared-memory state for single tokens
     # from 8 units per SM; with several v-heads per q/k head 64-column items
-    # for single tokens, and for two tokens from 8 units per SM or at most half
-    # a unit per SM; else 128 columns
+    # for one or two tokens; else 128 columns
     def label(*shape, variant="auto", **dims):
         return kda.plan_label(kda.make_plan(kda.make_shape(*shape, **dims), 152, variant, decode=True))
     assert label(512, 1, 32, 64) == "smem:128" and label(76, 1, 16, 16) == "smem:128"
     assert label(75, 1, 16, 16) == "item:128" and label(8, 1, 16, 16) == "item:128"
     assert label(152, 2, 16, 16) == "item:128" and label(512, 2, 16, 16) == "item:128"
-    assert label(38, 2, 16, 32) == "item:64" and label(37, 2, 16, 32) == "item:128"
-    assert label(32, 1, 16, 32) == "item:64" and label(8, 2, 16, 32) == "item:128"
+    assert label(38, 2, 16, 32) == "item:64" and label(37, 2, 16, 32) == "item:64"
+    assert label(32, 1, 16, 32) == "item:64" and label(8, 2, 16, 32) == "item:64"
+    assert label(8, 3, 16, 32) == "item:128" and label(512, 2, 32, 64) == "item:64"
     assert label(1, 2, 16, 32) == "item:64" and label(1, 3, 32, 64) == "item:128"
     assert label(1, 4, 16, 32) == "item:128" and label(1, 8, 32, 64) == "item:128"
     for T in (3, 4):
