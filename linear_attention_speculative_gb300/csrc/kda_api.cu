@@ -258,15 +258,16 @@ int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool de
       // head (+3..5 %) and plain decodes (+2..5 %).  From two tokens on the
       // register-state decode kernels are faster.
       const long long smem_from = (s->T == 1 && (decode || G == 1)) ? 8 : 0;
-      const bool wide = s->T <= 2 || (!decode && 2 * units <= num_sms);
+      const bool few = !decode && 2 * units <= num_sms;
       if (smem_from > 0 && units >= smem_from * num_sms) {
         out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
-      } else if (G >= 2 && wide) {
-        // Several v-heads per q/k head: 64-column tiles (twice the CTAs) for
-        // calls of up to two tokens (+2..17 %) and verifies of at most half a
-        // unit per SM.  Longer calls keep 128 columns: each 64-column item
-        // repeats the q/k conv of all T tokens (up to 20 % slower for plain
-        // decodes of three tokens).
+      } else if ((G >= 2 && s->T <= 2) || few) {
+        // 64-column tiles (twice the CTAs): with several v-heads per q/k head
+        // for calls of up to two tokens (+2..17 %), and for verifies of at
+        // most half a unit per SM, where the idle SMs absorb the repeated
+        // q/k work (+5..10 % at one token, even at other T).  Longer calls
+        // keep 128 columns: each 64-column item repeats the q/k conv of all T
+        // tokens (up to 20 % slower for plain decodes of three tokens).
         out->bv = 4 * kda::warp_cols(s->K);
       }
     }
