@@ -44,11 +44,15 @@
 //
 // Shared q/k conv_state write-back: the q/k channels of group (n, h) are read
 // by G * (V / BV) items.  With one reader it rolls them itself.  Otherwise
-// either a separate kernel launched after this one rolls them (kda_roll.cu;
-// Params::qk_roll_kernel), or each item arrives on a per-group counter after
-// its reads and the last arrival rolls the group's q/k conv_state and resets
-// the counter to zero (in the split variant the prep kernel rolls every
-// channel of its group).  Nothing ever waits on another CTA.  v channels
+// a separate kernel launched after this one rolls them (kda_roll.cu;
+// Params::qk_roll_kernel), or the items of the group run as one thread-block
+// cluster whose first CTA rolls after the cluster barrier (the one-item
+// kernel's kRollCluster instantiations), or each item arrives on a per-group
+// counter after its reads and the last arrival rolls the group's q/k
+// conv_state and resets the counter to zero (in the split variant the prep
+// kernel rolls every channel of its group).  No CTA spins on another; the
+// cluster barrier is a hardware barrier every CTA of the cluster reaches
+// before any wait of its own.  v channels
 // belong to exactly one item, which rolls them itself.  In the one-item
 // kernel, whose threads read conv_state straight from global memory, the
 // producer stages the new windows in shared memory and every roll is stored
