@@ -466,39 +466,61 @@ def run_ours(args, wl):
                               kda.alloc_workspace(shape, dev)))
         d2h = sum(v.numel() * v.element_size() for v in lanes[0]["host_out"].values())
 
-        def e2e_step(lane):
+        # the inputs a serving step receives anew (the new tokens' projections and
+        # gate inputs) and the output it returns; the other tensors are state
+        STEP_IN, STEP_OUT = ("mixed_qkv", "a", "b"), ("o",)
+
+        def e2e_step(lane, resident=False):
             st, x, y, ho = lane["stream"], lane["inp"], lane["out"], lane["host_out"]
             with torch.cuda.stream(st):
                 for k, v in host_in.items():
-                    if v is not None:
+                    if v is not None and (not resident or k in STEP_IN):
                         x[k].copy_(v, non_blocking=True)
                 kda.conv_verify(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"],
                                 x["dt_bias"], x["a"], x["b"], x["S0"], wl.gate, y["o"],
                                 y["inter_ssm"], y["conv_snapshots"], lane["ws"], stream=st,
                                 variant=args.variant, shape=shape, plan=args.plan or None)
-                for k in ("o", "inter_ssm", "conv_snapshots"):
+                for k in (STEP_OUT if resident else ("o", "inter_ssm", "conv_snapshots")):
                     ho[k].copy_(y[k], non_blocking=True)
-                ho["conv_state"].copy_(x["conv_state"], non_blocking=True)
+                if not resident:
+                    ho["conv_state"].copy_(x["conv_state"], non_blocking=True)
+
+        def e2e_time(steps, resident=False):
+            barrier()
+            f0 = torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            lanes[1]["stream"].wait_event(f0)
+            for i in range(steps):
+                e2e_step(lanes[i % 2], resident)
+            ends = []
+            for lane in lanes:
+                ev = torch.cuda.Event(enable_timing=True)
+                ev.record(lane["stream"])
+                ends.append(ev)
+            barrier()
+            return max_over_ranks(max(f0.elapsed_time(ev) for ev in ends), dev)
 
         for r in range(2):
-            e2e_step(lanes[r])
-        barrier()
-        f0 = torch.cuda.Event(enable_timing=True)
-        f0.record(stream)
-        lanes[1]["stream"].wait_event(f0)
-        for i in range(E):
-            e2e_step(lanes[i % 2])
-        ends = []
-        for lane in lanes:
-            ev = torch.cuda.Event(enable_timing=True)
-            ev.record(lane["stream"])
-            ends.append(ev)
-        barrier()
-        e2e_ms = max_over_ranks(max(f0.elapsed_time(ev) for ev in ends), dev)
+            e2e_step(lanes[r])  # also fills both lanes' state buffers
+        e2e_ms = e2e_time(E)
         e2e_value = global_head_steps * E / (e2e_ms / 1e3)
         e2e_line = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": E,
                     "note": "pinned host buffers; two streams alternate steps so copies overlap"}
+        # the same call with the state resident on the device, as a serving loop
+        # keeps it: per step the new inputs in and o out
+        ER = max(2, min(K, 50))
+        for r in range(2):
+            e2e_step(lanes[r], resident=True)
+        er_ms = e2e_time(ER, resident=True)
+        e2e_line["state_resident"] = {
+            "value": global_head_steps * ER / (er_ms / 1e3), "unit": UNIT,
+            "h2d_bytes_per_step": sum(host_in[k].numel() * host_in[k].element_size() for k in STEP_IN),
+            "d2h_bytes_per_step": sum(lanes[0]["host_out"][k].numel() * lanes[0]["host_out"][k].element_size()
+                                      for k in STEP_OUT),
+            "steps": ER,
+            "note": ("S0, conv_state, the weights and the snapshots stay on the device; per step "
+                     "mixed_qkv, a and b in from pinned host memory and o back")}
 
     if rank == 0:
         clocks.stop()
@@ -525,7 +547,8 @@ def run_ours(args, wl):
                    "variant": VARIANT_NAME[plan.variant],
                    "v_tile": plan.bv, "plan": args.plan or f"auto ({plan_label(plan)})",
                    "qk_roll": ("single reader" if (s.HV // s.H) * (s.V // plan.bv) == 1 else
-                               {1: "counter", 2: "kernel"}.get(plan.qk_roll, "counter")),
+                               "prep kernel" if plan.variant == kda.VARIANT_SPLIT else
+                               {v: k for k, v in kda.QK_ROLL_NAMES.items()}[plan.qk_roll]),
                    "l2": (L2_FLUSH_NOTE if flush_l2 else
                           f"inputs larger than L2: {alg_bytes / 1e9:.2f} GB moved per step"),
                    "parallelism": f"replicas x{world}" if world > 1 else "1 GPU"},
