@@ -245,7 +245,7 @@ int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool de
     out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
     out->bv = full_bv;
   } else {
-    // One item per CTA, the state in registers: the fastest kernel at 137 of
+    // One item per CTA, the state in registers: the fastest kernel at 143 of
     // the 150 points of the configuration sweep (T in 1..8, N in 1..512, three
     // head layouts, both gates; K = V = 128) and at 140 of the same 150 points
     // for the plain decode.
