@@ -356,15 +356,18 @@ int kda_read_status(const kda_shape* s, void* workspace, int* status, kda_stream
 
 /* Diagnostic: run the kernels' bounded device waits against an mbarrier that
  * nothing arrives at, so that they give up on purpose, without a fault; the
- * context stays usable.  One CTA on `stream`:
- *   mode 0  the one-item kernels' wait, limit_ns (0 .. 2e9) on the clock;
+ * context stays usable.  On `stream`:
+ *   mode 0  one CTA: the one-item kernels' wait, limit_ns (0 .. 2e9) on the clock;
  *   mode 1  the same, then it raises the pipelined kernel's abort flag, which
  *           ends a second warp's pipelined-kernel wait early;
- *   mode 2  the pipelined kernel's wait alone, until its own 2 s limit.
+ *   mode 2  the pipelined kernel's wait alone, until its own 2 s limit;
+ *   mode 3  a cluster of 4 CTAs: the one-item kernels' time-out path under the
+ *           cluster q/k roll (arrive on the cluster barrier, the wait gives up
+ *           at limit_ns, report, wait on the cluster barrier, return).
  * `status` is a device int[2], OR-ed into: status[0] gets KDA_STATUS_TMA_TIMEOUT
- * when a wait gave up, status[1] bit 1 (the one-item wait gave up) and bit 2
- * (the pipelined wait did).  Returns 0, KDA_ERR_NULL, KDA_ERR_SHAPE (mode or
- * limit out of range) or a cudaError_t. */
+ * when a wait gave up, status[1] 1 (the one-item wait gave up), 2 (the
+ * pipelined wait did), 4 (the cluster path's wait did).  Returns 0,
+ * KDA_ERR_NULL, KDA_ERR_SHAPE (mode or limit out of range) or a cudaError_t. */
 int kda_selftest_bounded_wait(int mode, long long limit_ns, int* status, kda_stream_t stream);
 
 /* Human-readable text for a return code (negative KDA_ERR_* or positive

@@ -481,7 +481,8 @@ def run(inputs: Dict[str, torch.Tensor], gate: str, variant: str = "auto",
 
 def selftest_bounded_wait(mode: int, limit_ns: int = 0, stream=None):
     """Run the kernels' bounded waits until they give up (no fault); returns
-    (status word, mask of the waits that gave up: 1 one-item, 2 pipelined)."""
+    (status word, mask of the waits that gave up: 1 one-item, 2 pipelined,
+    4 the one-item wait inside a cluster, mode 3)."""
     out = torch.zeros(2, dtype=torch.int32, device="cuda")
     rc = lib().kda_selftest_bounded_wait(int(mode), int(limit_ns), _ptr(out), _stream_handle(stream))
     if rc != 0:

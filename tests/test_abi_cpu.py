@@ -456,7 +456,8 @@ def test_selftest_rejects_bad_arguments_on_the_host(kda):
     L = kda.lib()
     st = ctypes.c_void_p(0x7f0000000000)
     assert L.kda_selftest_bounded_wait(0, 1000, None, None) == -1
-    assert L.kda_selftest_bounded_wait(3, 1000, st, None) == -2
+    assert L.kda_selftest_bounded_wait(4, 1000, st, None) == -2
+    assert L.kda_selftest_bounded_wait(-1, 1000, st, None) == -2
     assert L.kda_selftest_bounded_wait(0, -1, st, None) == -2
     assert L.kda_selftest_bounded_wait(0, 3_000_000_000, st, None) == -2
 

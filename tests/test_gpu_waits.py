@@ -57,6 +57,15 @@ def test_pipelined_wait_gives_up_at_its_own_limit():
     assert 1.9 < dt < 4.0, dt
 
 
+def test_cluster_roll_time_out_path_ends():
+    # every CTA of the cluster arrives on the cluster barrier before its own
+    # wait, so the wait on the cluster barrier after giving up ends at once
+    from linear_attention_speculative_gb300 import kda
+    status, mask, dt = _timed(3, 20_000_000)
+    assert status == kda.STATUS_TMA_TIMEOUT and mask == 4
+    assert 0.015 < dt < 1.5, dt
+
+
 def test_context_still_runs_a_verify_afterwards():
     _timed(0, 1_000_000)
     wl = wk.custom(3, 4, 2, 4, 128, 128, seed=61)
