@@ -75,10 +75,13 @@ def test_status_reader_rejects_bad_arguments_on_the_host():
                                      ctypes.byref(st), None) == -10
 
 
-# Four v-heads per q/k head in both.  The small launch rolls the shared q/k
-# conv_state with the arrival counters kept in the scratch array; the large one
-# uses the separate roll kernel, and the scratch holds only the status word.
-NOALLOC_CASES = [wk.custom(8, 4, 2, 8, 128, 128, gate="safe", seed=901), wk.GVA]
+# Several v-heads per q/k head in each.  The first small launch rolls the
+# shared q/k conv_state in a thread-block cluster of a group's items, the second
+# (groups of 16 items, too many for one cluster) with the arrival counters kept
+# in the scratch array; the large one uses the separate roll kernel.  The
+# scratch always holds the status word.
+NOALLOC_CASES = [wk.custom(8, 4, 2, 8, 128, 128, gate="safe", seed=901),
+                 wk.custom(4, 4, 2, 16, 128, 128, seed=902), wk.GVA]
 
 
 @pytest.mark.gpu
