@@ -144,6 +144,8 @@ DET_CASES = [
     (wk.GVA, "item:128:0:0:kernel"),           # four readers, second roll kernel
     (wk.GVA, "item:128:0:0:cluster"),          # four readers, one cluster per group
     (wk.GVA, "item:64:0:0:cluster"),           # eight readers (two v-tiles each), cluster of 8
+    # two tokens: the roll kernel reads the old q/k windows before its dependency wait
+    (wk.custom(64, 2, 8, 32, 128, 128, gate="safe", seed=77), "item:128:0:0:kernel"),
     (wk.GVA, "pipe:128:0:0:counter"),          # pipelined kernel, counter
     (wk.GVA, "split:64"),                      # prep kernel + dependent recurrence kernel
     (wk.DECODE, "item:32"),                    # four v-tiles per state read q/k
