@@ -317,7 +317,10 @@ size_t kda_workspace_bytes(const kda_shape* s);
  *   num_sms   streaming multiprocessors of the device
  *   variant   requested variant (AUTO lets the dispatcher decide)
  * Out: chosen variant, v-tile width bv (columns of V per CTA), warps per
- * CTA, grid size.  Returns 0 or a negative KDA_ERR_* code. */
+ * CTA, grid size, CTAs per SM, L2 prefetch distance, the q/k conv_state roll
+ * when several items read one q/k head (the cluster below 2 waves of resident
+ * CTAs where it is built, else the counter; the second kernel from 2 waves)
+ * and the number of launches.  Returns 0 or a negative KDA_ERR_* code. */
 int kda_make_plan(const kda_shape* s, int num_sms, kda_variant variant, kda_plan* out);
 
 /* The plan kda_conv_decode picks for shape `s` (plain decode: ONE_ITEM or
