@@ -730,9 +730,9 @@ def sweep_report(path, peak_gbs, peak_src):
                        f"({len(sub)} points)")
     # which kernel is fastest, by T and units (N * HV)
     out.append("")
-    out.append("Fastest explicit plan's kernel by T (rows) and N * HV (columns); item = one item per CTA "
-               "(state in registers), smem = one item per CTA (state in shared memory), pipe = pipelined, "
-               "split = prep kernel + recurrence kernel:")
+    out.append("Fastest explicit plan by T (rows) and N * HV (columns), as kernel:v-tile columns (the "
+               "dispatch crossovers); item = one item per CTA (state in registers), smem = one item per CTA "
+               "(state in shared memory), pipe = pipelined, split = prep kernel + recurrence kernel:")
     units = sorted({r["N"] * r["HV"] for r in rows})
     Ts = sorted({r["T"] for r in rows})
     out.append("")
@@ -741,7 +741,8 @@ def sweep_report(path, peak_gbs, peak_src):
     for T in Ts:
         cells = []
         for u in units:
-            kinds = sorted({r["best"].split(":")[0] for r in rows if r["T"] == T and r["N"] * r["HV"] == u})
+            kinds = sorted({":".join(r["best"].split(":")[:2]) for r in rows
+                            if r["T"] == T and r["N"] * r["HV"] == u})
             cells.append("/".join(kinds) if kinds else "")
         out.append(f"| {T} | " + " | ".join(cells) + " |")
     for pick, what in ((lambda p: p.startswith("pipe:"), "Pipelined kernel"),
