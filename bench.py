@@ -49,7 +49,8 @@ def parse():
     ap.add_argument("--workload", default="large_bf16_n256_t4_h32")
     ap.add_argument("--variant", default="auto")
     ap.add_argument("--plan", default="",
-                    help="explicit launch plan, e.g. item:32 or pipe:64 (overrides --variant)")
+                    help="explicit launch plan variant:columns[:grid[:prefetch[:qk_roll]]], e.g. item:32, "
+                         "pipe:64 or item:64:0:0:cluster (overrides --variant)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-only", action="store_true",
