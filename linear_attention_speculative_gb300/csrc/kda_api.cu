@@ -270,6 +270,11 @@ int make_plan_impl(const kda_shape* s, int num_sms, kda_variant variant, bool de
         // tokens (up to 20 % slower for plain decodes of three tokens).
         out->bv = 4 * kda::warp_cols(s->K);
       }
+    } else if (decode && s->T == 1 && units >= 8LL * num_sms && valid_sms_bv(full_bv, s->K, s->V)) {
+      // The other head dims' plain decode of one token over many units: the
+      // shared-memory state too (K = V = 64: +3.5 %, K = V = 256: +4 %); their
+      // verifies keep the register state (1-2 % faster there).
+      out->variant = KDA_VARIANT_ONE_ITEM_SMEM;
     }
   }
   finish_plan(s, num_sms, out, 0, 0, KDA_QK_ROLL_AUTO);

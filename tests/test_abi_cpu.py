@@ -107,7 +107,13 @@ def test_decode_plan(kda):
     assert label(1, 4, 16, 32) == "item:128" and label(1, 8, 32, 64) == "item:128"
     for T in (3, 4):
         assert label(512, T, 32, 64) == "item:128"
-    assert label(64, 1, 8, 16, K=256, V=256) == "item:64"
+    assert label(64, 1, 8, 16, K=256, V=256) == "item:64"  # fewer than 8 units per SM
+    # the other head dims: the shared-memory state for single tokens from 8
+    # units per SM where it is built (not at K = V = 32)
+    assert label(128, 1, 16, 16, K=256, V=256) == "smem:64"
+    assert label(512, 1, 16, 32, K=64, V=64) == "smem:64"
+    assert label(512, 1, 16, 32, K=32, V=32) == "item:32"
+    assert label(512, 2, 16, 32, K=64, V=64) == "item:64"
     assert label(8, 1, 16, 16, variant="one_item_smem") == "smem:128"
     for bad in ("pipelined", "split"):
         with pytest.raises(kda.KdaError) as e:
