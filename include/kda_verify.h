@@ -29,7 +29,11 @@
  * Ownership: the caller allocates every buffer (device memory) and keeps
  * ownership; the library allocates nothing and keeps no pointer after a call
  * returns.  Calls are asynchronous on `stream` (NULL = legacy default
- * stream); no call synchronises except kda_read_status.
+ * stream); no call synchronises except kda_read_status.  Stream order holds
+ * as for any launch: the one-item verify and decode kernels are launched as
+ * programmatic dependents of the stream's previous kernel, so their CTAs may
+ * become resident while it finishes, but no thread of theirs touches global
+ * memory before that kernel has completed and its writes are visible.
  *
  * Errors: 0 on success; a negative KDA_ERR_* code when the arguments are
  * rejected on the host (nothing is launched, no buffer is touched); a

@@ -58,6 +58,14 @@
 // producer stages the new windows in shared memory and every roll is stored
 // after the barrier that ends the CTA's conv_state reads; the pipelined kernel
 // reads its raw inputs from shared memory and rolls directly.
+//
+// Launch overlap: the one-item kernel is launched as a programmatic dependent
+// of whatever kernel precedes it on the stream.  Its first instruction waits
+// for that kernel (griddepcontrol.wait: completed, writes visible) and only
+// then triggers its own dependents, so its launch and CTA start overlap the
+// previous kernel's last wave while no access of its own, nor of the q/k roll
+// kernel that loads ahead of its own wait, can run before the previous
+// kernel's writes.
 #pragma once
 
 #include "kda_device.cuh"
@@ -1084,8 +1092,15 @@ __global__ void __launch_bounds__(WARPS * 32, tile_min_blocks(WARPS, SMS))
   const int warp = tid >> 5;
   const int lane = tid & 31;
   const long long item = blockIdx.x;
-  // a programmatic dependent launched after this grid (the q/k roll kernel)
-  // may be scheduled once every CTA has started; it waits for completion
+  // This grid is itself launched as a programmatic dependent of the stream's
+  // previous kernel, so its CTAs may be resident before that kernel has
+  // ended: every global access, reads of the slot indices included, comes
+  // after this wait (a no-op when nothing is in flight).  The split
+  // recurrence's dependency is the prep kernel, waited for below.
+  if constexpr (!PRE) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // A programmatic dependent launched after this grid (the q/k roll kernel,
+  // or the next call) may be scheduled once every CTA has got here, by which
+  // time the previous kernel has completed; it waits for this one's end.
   asm volatile("griddepcontrol.launch_dependents;");
   if (item >= p.num_items) return;
   const Item it = decode_item(p, item);

@@ -46,6 +46,14 @@ int launch_tile_cluster_f32(const CUtensorMap& tmap, const Params& p, const Laun
 // p.qk_roll_kernel set (kda_roll.cu), on the same stream after it.
 int launch_qk_roll(const Params& p, int K, bool bf16, cudaStream_t st);
 
+// Launch as a programmatic dependent of the stream's previous kernel: the
+// grid may be scheduled while that kernel's last CTAs run, and waits for it
+// (griddepcontrol.wait) before its first global access.
+inline void set_programmatic(cudaLaunchAttribute& a) {
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+}
+
 // Opt a kernel in to large dynamic shared memory once per device.
 template <typename Fn>
 int configure_once(Fn fn, unsigned long long* configured) {
@@ -70,7 +78,17 @@ int launch_tile_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c
   static unsigned long long configured = 0;  // bit per device ordinal (< 64)
   int rc = configure_once(fn, &configured);
   if (rc) return rc;
-  fn<<<cfg.grid, WARPS * 32, cfg.smem, st>>>(tmap, p);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cfg.grid);
+  lc.blockDim = dim3(WARPS * 32);
+  lc.dynamicSmemBytes = cfg.smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  set_programmatic(attr[0]);
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, fn, tmap, p);
+  if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -88,13 +106,14 @@ int launch_tile_cluster_one(const CUtensorMap& tmap, const Params& p, const Laun
   lc.blockDim = dim3(WARPS * 32);
   lc.dynamicSmemBytes = cfg.smem;
   lc.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)p.qk_cluster;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  set_programmatic(attr[1]);
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&lc, fn, tmap, p);
   if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());

@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(kRollThreads) kda_qk_roll_kernel(const Params 
   }
   // the verify grid has completed (its reads of the old window too)
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next call's verify kernel may be scheduled as this one ends
+  asm volatile("griddepcontrol.launch_dependents;");
 #pragma unroll
   for (int m = 0; m < 3; ++m) st_16(cp + 16 * m, AT::pack(r + m * VEC));
 }

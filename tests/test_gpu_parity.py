@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from linear_attention_speculative_gb300 import workloads as wk
-from parity_util import (TOL, assert_parity, conv_window_properties, max_rel_err, plan_built,
+from parity_util import (TOL, assert_decode_parity, assert_parity, conv_window_properties, max_rel_err, plan_built,
                          rel_rmse, run_kernel, to_device, variant_built)
 
 pytestmark = pytest.mark.gpu
@@ -214,6 +214,66 @@ def test_chain_of_single_token_calls_is_bit_exact(variant, gate):
         S = out["inter_ssm"][:, 0].contiguous()
     torch.cuda.synchronize()
     assert torch.equal(cs, full_cs)
+
+
+@pytest.mark.parametrize("op", ("verify", "decode"))
+@pytest.mark.parametrize("plan", [None, "item:128:0:0:kernel", "item:128:0:0:counter", "item:64:0:0:cluster",
+                                  "smem:128", "pipe:128", "split:64"])
+def test_neighbouring_kernels_without_a_sync(plan, op):
+    """Calls queued between ordinary kernels on one stream, with no
+    synchronisation: before each call a kernel writes its inputs and another
+    reads the previous call's o, which the call then overwrites; after it
+    kernels copy its outputs away.  The one-item kernels are launched as
+    programmatic dependents of the kernel before them, so this checks that no
+    access of theirs runs ahead of that kernel: each call matches the oracle
+    on its own inputs, and the read before call i + 1 sees call i's o."""
+    from linear_attention_speculative_gb300 import kda
+    N, T, H, HV = 24, 3, 4, 8
+    if not plan_built(plan, 128, 128, decode=op == "decode", G=HV // H):
+        pytest.skip("no such kernel for this shape")
+    steps = 4
+    cpu = [wk.make_inputs(wk.custom(N, T, H, HV, 128, 128, seed=23 + i)) for i in range(steps)]
+    src = [to_device(c) for c in cpu]
+    x = {k: (torch.empty_like(v) if v is not None else None) for k, v in src[0].items()}
+    shape = kda.shape_of(x["mixed_qkv"], x["a"], x["S0"])
+    ws = kda.alloc_workspace(shape, "cuda")
+    dim = x["mixed_qkv"].shape[2]
+    out = {"o": torch.zeros((N, T, HV, 128), dtype=torch.bfloat16, device="cuda"),
+           "inter_ssm": torch.empty((N, T, HV, 128, 128), dtype=torch.float32, device="cuda"),
+           "conv_snapshots": torch.empty((N, T, dim, 3), dtype=torch.bfloat16, device="cuda")}
+    saved = [torch.empty_like(out["o"]) for _ in range(steps)]
+    keep = [{"o": torch.empty_like(out["o"]), "S": torch.empty_like(x["S0"]),
+             "inter_ssm": torch.empty_like(out["inter_ssm"]),
+             "conv_snapshots": torch.empty_like(out["conv_snapshots"]),
+             "conv_state": torch.empty_like(x["conv_state"])} for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        for k, v in src[i].items():  # element-wise kernels (x * 1 is exact)
+            if v is not None:
+                torch.mul(v, 1, out=x[k])
+        torch.mul(out["o"], 1, out=saved[i])
+        if op == "verify":
+            kda.conv_verify(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"], x["dt_bias"], x["a"],
+                            x["b"], x["S0"], "softplus", out["o"], out["inter_ssm"], out["conv_snapshots"], ws,
+                            shape=shape, plan=plan, validate=False)
+            torch.mul(out["inter_ssm"], 1, out=keep[i]["inter_ssm"])
+            torch.mul(out["conv_snapshots"], 1, out=keep[i]["conv_snapshots"])
+        else:
+            kda.conv_decode(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"], x["dt_bias"], x["a"],
+                            x["b"], x["S0"], "softplus", out["o"], ws, shape=shape, plan=plan, validate=False)
+            torch.mul(x["S0"], 1, out=keep[i]["S"])
+        torch.mul(out["o"], 1, out=keep[i]["o"])
+        torch.mul(x["conv_state"], 1, out=keep[i]["conv_state"])
+    torch.cuda.synchronize()
+    assert not saved[0].any()
+    for i in range(steps):
+        orc = oracle.verify(cpu[i], "softplus")
+        if op == "verify":
+            assert_parity(keep[i], keep[i]["conv_state"], orc)
+        else:
+            assert_decode_parity(keep[i]["o"], keep[i]["S"], keep[i]["conv_state"], orc)
+        if i + 1 < steps:
+            assert torch.equal(saved[i + 1], keep[i]["o"])
 
 
 EDGE = [
