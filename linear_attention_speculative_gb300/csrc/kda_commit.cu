@@ -11,7 +11,9 @@
 // and chunk come from the block index, so no per-element division), every
 // thread issuing all four of its streaming loads before its four stores so
 // that 64 bytes per thread are in flight.  Sequences whose count is out of
-// range are left untouched and reported in the status word.
+// range are left untouched and reported in the status word.  The launch is a
+// programmatic dependent of the stream's previous kernel: its CTAs may start
+// while that kernel ends and wait for it before any global access.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -45,6 +47,10 @@ struct CommitParams {
 constexpr int kCommitChunk = kCommitThreads * kCommitUnroll;  // vectors per CTA
 
 __global__ void __launch_bounds__(kCommitThreads) kda_commit_kernel(const CommitParams p) {
+  // launched as a programmatic dependent of the stream's previous kernel (the
+  // verify, as a rule): nothing global is touched before it has completed
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   const long long n = blockIdx.x / p.chunks;
   const long long r0 = (long long)(blockIdx.x - n * p.chunks) * kCommitChunk + threadIdx.x;
   const long long ss = p.idx_state ? __ldg(p.idx_state + n) : n;
@@ -150,7 +156,18 @@ extern "C" int kda_commit_indexed(const kda_shape* s, const kda_state_indices* i
   const long long blocks = (long long)N * chunks;
   if (chunks > 0x7fffffffLL || blocks > 0x7fffffffLL) return KDA_ERR_SHAPE;
   p.chunks = (int)chunks;
-  kda_commit_kernel<<<(unsigned)blocks, kCommitThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(p);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)blocks);
+  lc.blockDim = dim3(kCommitThreads);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&lc, kda_commit_kernel, p);
+  if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());
 }
 

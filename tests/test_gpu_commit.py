@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from linear_attention_speculative_gb300 import workloads as wk
-from parity_util import to_device
+from parity_util import assert_parity, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -121,3 +121,51 @@ def test_random_commit_matches_the_oracle(case):
     np.testing.assert_array_equal(S.double().cpu().numpy(), ref["S"])
     np.testing.assert_array_equal(cs.double().cpu().numpy(), ref["conv_state"])
     assert int(status.item()) == 0
+
+
+@pytest.mark.parametrize("plan", [None, "item:64:0:0:cluster", "item:128:0:0:kernel", "smem:128"])
+def test_verify_commit_loop_without_a_sync(plan):
+    """A serving loop: verify, commit, verify, commit ... queued back to back
+    on one stream with nothing between them and no synchronisation.  Both
+    kernels are launched as programmatic dependents of the kernel before
+    them, so each commit must see its verify's snapshots and each verify the
+    state and conv_state the commit before it wrote: every verify is checked
+    against the oracle run on the state that commit left (taken from the
+    previous verify's own snapshots), and the final state bit for bit."""
+    from linear_attention_speculative_gb300 import kda
+    N, T, H, HV, steps = 24, 3, 4, 8, 4
+    cpu = [wk.make_inputs(wk.custom(N, T, H, HV, 128, 128, seed=130 + i)) for i in range(steps)]
+    dev = [to_device(c) for c in cpu]
+    S = dev[0]["S0"].clone()
+    cs = dev[0]["conv_state"].clone()
+    rng = np.random.default_rng(5)
+    accs = [torch.tensor(rng.integers(1, T + 1, N), dtype=torch.int32, device="cuda") for _ in range(steps)]
+    shape = kda.shape_of(dev[0]["mixed_qkv"], dev[0]["a"], S)
+    ws = kda.alloc_workspace(shape, "cuda")
+    outs = [{k: v.cuda() for k, v in wk.empty_outputs(wk.custom(N, T, H, HV, 128, 128)).items()}
+            for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        x, o = dev[i], outs[i]
+        kda.conv_verify(x["mixed_qkv"], x["conv_w"], cs, x["A_log"], x["dt_bias"], x["a"], x["b"], S,
+                        "softplus", o["o"], o["inter_ssm"], o["conv_snapshots"], ws, shape=shape, plan=plan,
+                        validate=False)
+        kda.commit(accs[i], o["inter_ssm"], o["conv_snapshots"], S, cs, shape=shape, validate=False)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        inp = dict(cpu[i])
+        if i > 0:  # the state the previous commit left: the previous verify's accepted snapshot
+            a = accs[i - 1].long().cpu()
+            prev = outs[i - 1]
+            inp["S0"] = prev["inter_ssm"].cpu()[torch.arange(N), a - 1].contiguous()
+            inp["conv_state"] = prev["conv_snapshots"].cpu()[torch.arange(N), a - 1].contiguous()
+        orc = oracle.verify(inp, "softplus")
+        # the conv_state each verify rolled is overwritten by its commit, so the
+        # rolled windows are checked through the snapshots (bit-exact) instead
+        np.testing.assert_array_equal(outs[i]["conv_snapshots"].double().cpu().numpy(), orc["conv_snapshots"])
+        got = {"o": outs[i]["o"], "inter_ssm": outs[i]["inter_ssm"],
+               "conv_snapshots": outs[i]["conv_snapshots"]}
+        assert_parity(got, torch.from_numpy(orc["conv_state"]), orc)
+    a = accs[-1].long().cpu()
+    assert torch.equal(S.cpu(), outs[-1]["inter_ssm"].cpu()[torch.arange(N), a - 1])
+    assert torch.equal(cs.cpu(), outs[-1]["conv_snapshots"].cpu()[torch.arange(N), a - 1])
