@@ -123,6 +123,36 @@ class L2Flush:
 L2_FLUSH_NOTE = "L2 flushed before every timed launch (258 MB written, then 258 MB read)"
 
 
+# back-to-back figures only where this many sets suffice (calls of >= L2 / 4)
+MAX_ROTATION_SETS = 16
+
+
+def rotation_sets(nbytes):
+    """Independent input/output sets to rotate over when calls of `nbytes` run
+    back to back: enough that together they hold over three times L2, so that
+    the other sets' traffic evicts a set between two of its uses."""
+    return -(-3 * L2_BYTES // max(1, nbytes)) + 1
+
+
+def time_back_to_back(call, R, B, stream, flush):
+    """Mean milliseconds per call of B calls queued back to back on `stream`,
+    call(i % R) for i < B, between one pair of events after an L2 flush (no
+    flush between the calls): each call's launch may overlap the previous
+    call's end, as consecutive calls of a serving loop do."""
+    import torch
+    for r in range(R):
+        call(r)
+    torch.cuda.synchronize()
+    flush(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(B):
+        call(i % R)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / B
+
+
 def measured_hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -446,7 +476,7 @@ def run_ours(args, wl):
         del graph
 
     b2b_line = None
-    if flush_l2 and not args.kernel_only and 4 * alg_bytes >= L2_BYTES:
+    if flush_l2 and not args.kernel_only and rotation_sets(alg_bytes) <= MAX_ROTATION_SETS:
         # A call that fits in L2 is timed above one launch at a time, each between
         # its own events after a flush, so every step also carries the launch's
         # few microseconds between the events.  Here the same call runs back to
@@ -454,7 +484,7 @@ def run_ours(args, wl):
         # and workspace sets that together hold over three times L2: between two
         # uses of one set the other sets' traffic has evicted it.  One event pair
         # around all the calls, no flush between them.
-        R = -(-3 * L2_BYTES // alg_bytes) + 1
+        R = rotation_sets(alg_bytes)
         sets = [(inp, out, ws)]
         for _ in range(R - 1):
             sets.append(({k: (v.clone() if v is not None else None) for k, v in inp.items()},
@@ -467,18 +497,9 @@ def run_ours(args, wl):
                             y["conv_snapshots"], w, stream=stream, variant=args.variant,
                             shape=shape, plan=args.plan or None, validate=False)
 
-        for x, y, w in sets:
-            call(x, y, w)
         B = max(K, 4 * R)
         barrier()
-        flush_buf(0)
-        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        for i in range(B):
-            call(*sets[i % R])
-        b1.record(stream)
-        barrier()
-        b_ms = max_over_ranks(b0.elapsed_time(b1), dev)
+        b_ms = max_over_ranks(B * time_back_to_back(lambda r: call(*sets[r]), R, B, stream, flush_buf), dev)
         b2b_line = {"ms_per_step": b_ms / B, "value": global_head_steps * B / (b_ms / 1e3),
                     "steps": B, "sets": R,
                     "frac": alg_bytes / (b_ms / B / 1e3) / 1e9 / measured_hbm_peak()[0],
@@ -852,9 +873,23 @@ def run_commit(args, wl):
     us = 1e3 * sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
     nbytes = 2 * s.N * (4 * s.HV * s.K * s.V + 3 * s.dim * s.act_bytes) + 4 * s.N
     peak, src = measured_hbm_peak()
+    # back to back over independent copies of everything the call touches
+    R = rotation_sets(nbytes)
+    b2b = None
+    if R <= MAX_ROTATION_SETS:
+        sets = [(out["inter_ssm"], out["conv_snapshots"], S, cs)] + [
+            (out["inter_ssm"].clone(), out["conv_snapshots"].clone(), torch.empty_like(S), torch.empty_like(cs))
+            for _ in range(R - 1)]
+        b_us = 1e3 * time_back_to_back(
+            lambda r: kda.commit(acc, *sets[r], stream=stream, validate=False), R, max(args.steps, 4 * R),
+            stream, flush)
+        del sets
+        b2b = {"us": b_us, "frac": nbytes / (b_us / 1e6) / 1e9 / peak, "sets": R,
+               "timing": "mean of back-to-back calls between one event pair"}
     print(json.dumps({"op": "commit", "workload": wl.name, "us": us, "bytes": nbytes,
                       "GB/s": nbytes / (us / 1e6) / 1e9, "frac": nbytes / (us / 1e6) / 1e9 / peak,
-                      "peak_source": src, "timing": "median of per-launch CUDA events, L2 flushed"}))
+                      "peak_source": src, "timing": "median of per-launch CUDA events, L2 flushed",
+                      "back_to_back": b2b}))
 
 
 def decode_bytes(s) -> int:
@@ -902,10 +937,28 @@ def run_decode(args, wl):
     us = 1e3 * sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
     peak, src = measured_hbm_peak()
     gbs = nbytes / (us / 1e6) / 1e9
+    # back to back over independent copies of everything the call touches
+    R = rotation_sets(nbytes)
+    b2b = None
+    if R <= MAX_ROTATION_SETS:
+        sets = [(inp, o, ws)] + [({k: (v.clone() if v is not None else None) for k, v in inp.items()},
+                                  torch.empty_like(o), kda.alloc_workspace(shape, dev)) for _ in range(R - 1)]
+
+        def call(r):
+            x, y, w = sets[r]
+            kda.conv_decode(x["mixed_qkv"], x["conv_w"], x["conv_state"], x["A_log"], x["dt_bias"], x["a"],
+                            x["b"], x["S0"], wl.gate, y, w, stream=stream, shape=shape, plan=args.plan or None,
+                            validate=False)
+        b_us = 1e3 * time_back_to_back(call, R, max(args.steps, 4 * R), stream, fbuf or L2Flush(dev))
+        del sets
+        b2b = {"us": b_us, "frac": nbytes / (b_us / 1e6) / 1e9 / peak, "sets": R,
+               "head_steps_per_s": s.head_steps / (b_us / 1e6),
+               "timing": "mean of back-to-back calls between one event pair"}
     print(json.dumps({"op": "decode", "workload": wl.name, "us": us, "bytes": nbytes,
                       "head_steps_per_s": s.head_steps / (us / 1e6), "GB/s": gbs,
                       "frac": gbs / peak, "peak_source": src,
-                      "timing": "median of per-launch CUDA events" + (", L2 flushed" if flush else "")}))
+                      "timing": "median of per-launch CUDA events" + (", L2 flushed" if flush else ""),
+                      "back_to_back": b2b}))
 
 
 def main():
