@@ -30,11 +30,10 @@
  * ownership; the library allocates nothing and keeps no pointer after a call
  * returns.  Calls are asynchronous on `stream` (NULL = legacy default
  * stream); no call synchronises except kda_read_status.  Stream order holds
- * as for any launch: the one-item verify and decode kernels and the commit
- * kernel are launched as programmatic dependents of the stream's previous
- * kernel, so their CTAs may become resident while it finishes, but no
- * thread of theirs touches global memory before that kernel has completed
- * and its writes are visible.
+ * as for any launch: every kernel the library launches is a programmatic
+ * dependent of the kernel before it on the stream, so its CTAs may become
+ * resident while that kernel finishes, but no thread of it touches global
+ * memory before that kernel has completed and its writes are visible.
  *
  * Errors: 0 on success; a negative KDA_ERR_* code when the arguments are
  * rejected on the host (nothing is launched, no buffer is touched); a

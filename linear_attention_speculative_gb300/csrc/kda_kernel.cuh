@@ -59,13 +59,15 @@
 // after the barrier that ends the CTA's conv_state reads; the pipelined kernel
 // reads its raw inputs from shared memory and rolls directly.
 //
-// Launch overlap: the one-item kernel is launched as a programmatic dependent
-// of whatever kernel precedes it on the stream.  Its first instruction waits
-// for that kernel (griddepcontrol.wait: completed, writes visible) and only
-// then triggers its own dependents, so its launch and CTA start overlap the
-// previous kernel's last wave while no access of its own, nor of the q/k roll
-// kernel that loads ahead of its own wait, can run before the previous
-// kernel's writes.
+// Launch overlap: every kernel here is launched as a programmatic dependent
+// of whatever kernel precedes it on the stream.  Its first global access
+// comes after a wait for that kernel (griddepcontrol.wait: completed, writes
+// visible), and it triggers its own dependents only after that wait, so its
+// launch and CTA start overlap the previous kernel's last wave while no
+// access of its own, nor of a dependent that loads ahead of its own wait (the
+// q/k roll kernel, the split variant's recurrence kernel), can run before the
+// previous kernel's writes.  The split recurrence kernel waits for its prep
+// kernel instead, which has waited for the kernel before it.
 #pragma once
 
 #include "kda_device.cuh"
@@ -1233,7 +1235,11 @@ __global__ void __launch_bounds__(kPrepThreads) kda_prep_kernel(const Params p) 
   const int NCV = 2 * NQ + G * NVV;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-  // the recurrence kernel may be scheduled once every CTA here has started
+  // launched as a programmatic dependent of the stream's previous kernel:
+  // nothing global is touched before it has completed.  The recurrence
+  // kernel, which issues its state-tile load before its own wait, may then be
+  // scheduled once every CTA here has got past that wait.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const int n = blockIdx.x / p.H;
   const int h = blockIdx.x - n * p.H;
@@ -1541,8 +1547,11 @@ __global__ void __launch_bounds__(pipe_threads(CW), pipe_min_blocks(CW))
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const long long stride = gridDim.x;
-  // a programmatic dependent launched after this grid (the q/k roll kernel)
-  // may be scheduled once every CTA has started; it waits for completion
+  // launched as a programmatic dependent of the stream's previous kernel:
+  // nothing global is touched before it has completed.  Then a programmatic
+  // dependent of this grid (the q/k roll kernel, or the next call) may be
+  // scheduled once every CTA has got here; it waits for this one's end.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;");
   const long long first = next_live_item(p, blockIdx.x, stride);
   if (threadIdx.x == 0) {  // report out-of-range slots of this CTA's items

@@ -142,7 +142,17 @@ int launch_pipe_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& c
   static unsigned long long configured = 0;
   int rc = configure_once(fn, &configured);
   if (rc) return rc;
-  fn<<<cfg.grid, pipe_threads(CW), cfg.smem, st>>>(tmap, p);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3((unsigned)cfg.grid);
+  lc.blockDim = dim3(pipe_threads(CW));
+  lc.dynamicSmemBytes = cfg.smem;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  set_programmatic(attr[0]);
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, fn, tmap, p);
+  if (e != cudaSuccess) return static_cast<int>(e);
   return static_cast<int>(cudaGetLastError());
 }
 
@@ -205,8 +215,17 @@ int launch_split_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& 
   int rc = configure_once(prep, &configured_prep);
   if (!rc) rc = configure_once(rec, &configured_rec);
   if (rc) return rc;
-  prep<<<p.N * p.H, kPrepThreads, prep_smem, st>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t pc = {};
+  pc.gridDim = dim3((unsigned)(p.N * p.H));
+  pc.blockDim = dim3(kPrepThreads);
+  pc.dynamicSmemBytes = prep_smem;
+  pc.stream = st;
+  cudaLaunchAttribute pattr[1];
+  set_programmatic(pattr[0]);
+  pc.attrs = pattr;
+  pc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&pc, prep, p);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return static_cast<int>(e);
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3((unsigned)cfg.grid);
@@ -214,8 +233,7 @@ int launch_split_one(const CUtensorMap& tmap, const Params& p, const LaunchCfg& 
   lc.dynamicSmemBytes = cfg.smem;
   lc.stream = st;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  set_programmatic(attr[0]);
   lc.attrs = attr;
   lc.numAttrs = 1;
   e = cudaLaunchKernelEx(&lc, rec, tmap, p);
