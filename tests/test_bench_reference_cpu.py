@@ -79,3 +79,17 @@ def test_committed_ncu_summaries_match_the_kernel_sources():
     for wl in ("large_bf16_n256_t4_h32", "gva_bf16_n64_t4_h8_hv32_safe", "decode_bf16_n16_t4_h16"):
         total, rd, wr = bench.ncu_traffic(wl, "kda_tile_kernel")
         assert total is not None and total == rd + wr, wl
+
+
+def test_back_to_back_rotation_sets_evict_each_set_between_uses():
+    # between two uses of one set the other R - 1 sets move more than L2 holds
+    # (here at least twice L2), and a call larger than L2 alternates two sets
+    import bench
+    for nbytes in (34_000_000, 88_800_000, 135_000_000, 268_000_000, 1_070_000_000, 2_840_000_000):
+        R = bench.rotation_sets(nbytes)
+        assert R >= 2 and (R - 1) * nbytes >= 2 * bench.L2_BYTES or R == 2, (nbytes, R)
+        assert R * nbytes >= 3 * bench.L2_BYTES
+    assert bench.rotation_sets(88_800_000) == 6
+    assert bench.rotation_sets(3 * bench.L2_BYTES) == 2
+    # tiny calls would need thousands of sets: no back-to-back figure for them
+    assert bench.rotation_sets(1_000_000) > bench.MAX_ROTATION_SETS
