@@ -12,12 +12,13 @@
 // mixed_qkv[n, :, c]] as the verify kernel saw it.  Stream order is the only
 // synchronisation; the verify kernel needs no arrival counters for it.  The
 // launch is a programmatic dependent of the verify kernel: its CTAs may be
-// scheduled once every verify CTA has started.  A thread first loads what it
-// needs -- the new tokens, and for T < 3 the old q/k window, none of which the
-// verify kernel writes -- and only then waits (griddepcontrol.wait, a hardware
-// dependency wait) until the verify grid has completed, every read of the old
-// window included, before it stores: the launch and the loads overlap the
-// verify kernel's last wave.
+// scheduled once every verify CTA has passed its own wait for the kernel
+// before it (so whatever that kernel wrote is visible here too).  A thread
+// first loads what it needs -- the new tokens, and for T < 3 the old q/k
+// window, none of which the verify kernel writes -- and only then waits
+// (griddepcontrol.wait, a hardware dependency wait) until the verify grid has
+// completed, every read of the old window included, before it stores: the
+// launch and the loads overlap the verify kernel's last wave.
 //
 // One thread per 16-byte vector of channels (8 bf16 / 4 fp32): it reads the
 // vector's 3 old values per channel when T < 3 and the last min(T, 3) token
