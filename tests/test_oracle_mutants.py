@@ -64,6 +64,14 @@ MUTANTS = {
                           "const double beta = orc_sigmoid(b[(size_t)t * HV + h]);"),
     "gate_from_first_token": ("const double* at = a + ((size_t)t * HV + hv) * K;",
                               "const double* at = a + (size_t)hv * K;"),
+    "silu_dropped": ("y[t] = orc_silu(acc);", "y[t] = acc;"),
+    "k_not_normalised": ("      orc_l2norm(K, kn, eps);\n", ""),
+    "l2norm_without_eps": ("double inv = 1.0 / sqrt(ss + eps);", "double inv = 1.0 / sqrt(ss);"),
+    "rank1_update_uses_q": ("S[(size_t)r * V + c] += beta * k[r] * u[c];",
+                            "S[(size_t)r * V + c] += beta * q[r] * u[c];"),
+    "dt_bias_from_qk_head": ("dt_bias[(size_t)hv * K + r]", "dt_bias[(size_t)h * K + r]"),
+    "A_log_from_qk_head": ("orc_gate_softplus(A_log[hv],", "orc_gate_softplus(A_log[h],"),
+    "v_from_qk_head": ("const double* vt = yt + 2 * H * K + hv * V;", "const double* vt = yt + 2 * H * K + h * V;"),
     "decay_after_update": (
         "  /* S <- diag(exp g) S */\n"
         "  for (int r = 0; r < K; ++r) {\n"
