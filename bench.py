@@ -302,7 +302,7 @@ def cpu_baseline(wl, inputs_cpu, cpu_seconds=12.0):
     t0 = time.perf_counter()
     oracle.verify(sub, wl.gate, seqs=list(range(n1)), threads=1)
     dt1 = time.perf_counter() - t0
-    bytes_per_head_step = s.algorithmic_bytes() / s.head_steps
+    bytes_per_head_step = s.algorithmic_bytes(wl.gate) / s.head_steps
     return {"value": hs / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
             "gb_per_s": hs / dt * bytes_per_head_step / 1e9,
             "single_core_value": n1 * s.T * s.HV / dt1,
@@ -377,7 +377,7 @@ def run_ours(args, wl):
     ws = kda.alloc_workspace(shape, dev)
     out = {k: v.to(dev) for k, v in wk.empty_outputs(wl).items()}
     stream = torch.cuda.current_stream(dev)
-    alg_bytes = s.algorithmic_bytes()
+    alg_bytes = s.algorithmic_bytes(wl.gate)
     flush_l2 = alg_bytes < 2 * L2_BYTES
     flush_buf = L2Flush(dev) if flush_l2 else None
 
@@ -675,7 +675,7 @@ def run_sweep(args):
         # who rolls the q/k conv_state when several items read it
         shared = (s.HV // s.H) * (s.V // auto_plan.bv) > 1 and auto_plan.variant != kda.VARIANT_SPLIT
         roll_names = {v: k for k, v in kda.QK_ROLL_NAMES.items()}
-        alg = decode_bytes(s) if decode else s.algorithmic_bytes()
+        alg = decode_bytes(s, wl.gate) if decode else s.algorithmic_bytes(wl.gate)
         row = {"workload": wl.name, "op": args.op if decode else "verify", "N": s.N, "T": s.T,
                "H": s.H, "HV": s.HV, "gate": wl.gate, "alg_bytes": alg,
                "head_steps": s.head_steps, "auto": auto,
@@ -892,12 +892,13 @@ def run_commit(args, wl):
                       "back_to_back": b2b}))
 
 
-def decode_bytes(s) -> int:
+def decode_bytes(s, gate="softplus") -> int:
     """Algorithmic bytes of one plain decode call: the state read and written in
-    place, the raw inputs, conv_state read and written, o, the weights."""
+    place, the raw inputs, conv_state read and written, o, the weights (A_log
+    and dt_bias only under the softplus gate)."""
     return (8 * s.N * s.HV * s.K * s.V + s.act_bytes * (
         s.N * s.T * s.dim + 2 * s.N * s.dim * 3 + s.N * s.T * s.HV * s.K + s.N * s.T * s.HV
-        + s.N * s.T * s.HV * s.V + 4 * s.dim) + 4 * s.HV * (1 + s.K))
+        + s.N * s.T * s.HV * s.V + 4 * s.dim) + (4 * s.HV * (1 + s.K) if gate == "softplus" else 0))
 
 
 def run_decode(args, wl):
@@ -917,7 +918,7 @@ def run_decode(args, wl):
         kda.conv_decode(inp["mixed_qkv"], inp["conv_w"], inp["conv_state"], inp["A_log"],
                         inp["dt_bias"], inp["a"], inp["b"], inp["S0"], wl.gate, o, ws,
                         stream=stream, shape=shape, plan=args.plan or None, validate=validate)
-    nbytes = decode_bytes(s)
+    nbytes = decode_bytes(s, wl.gate)
     flush = nbytes < 2 * L2_BYTES
     fbuf = L2Flush(dev) if flush else None
     step(validate=True)  # the first warm-up step

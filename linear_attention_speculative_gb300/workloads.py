@@ -67,19 +67,20 @@ class Shape:
     def torch_act(self) -> torch.dtype:
         return torch.float32 if self.act == "f32" else torch.bfloat16
 
-    def algorithmic_bytes(self) -> int:
+    def algorithmic_bytes(self, gate: str = "softplus") -> int:
         """Bytes the method itself must move once per call.
 
         S0 read once, every per-token state snapshot written once, the packed
         inputs read once, conv_state read and written once, the conv-window
-        snapshots and the output written once, the small parameters read once.
+        snapshots and the output written once, the small parameters read once
+        (A_log and dt_bias only under the softplus gate, which reads them).
         """
         N, T, HV, K, V, W = self.N, self.T, self.HV, self.K, self.V, self.W
         dim, ab = self.dim, self.act_bytes
         state = 4 * N * HV * K * V * (1 + T)
         acts = ab * (N * T * dim + 2 * N * dim * (W - 1) + N * T * dim * (W - 1)
                      + N * T * HV * K + N * T * HV + N * T * HV * V + W * dim)
-        params = 4 * HV * (1 + K)
+        params = 4 * HV * (1 + K) if gate == "softplus" else 0
         return state + acts + params
 
     def label(self) -> str:

@@ -50,3 +50,34 @@ def test_algorithmic_bytes_large():
     state = 5 * 4 * s.N * s.HV * s.K * s.V
     assert s.algorithmic_bytes() > state
     assert state / s.algorithmic_bytes() > 0.94
+
+
+def _tensor_bytes(wl):
+    """Bytes of the tensors one verify call reads and writes, counted from the
+    generated inputs and the outputs: every input read once, conv_state read
+    and written, every output written once."""
+    inp = wk.make_inputs(wl)
+    out = wk.empty_outputs(wl)
+    read = sum(v.numel() * v.element_size() for v in inp.values() if v is not None)
+    cs = inp["conv_state"]
+    written = sum(v.numel() * v.element_size() for v in out.values()) + cs.numel() * cs.element_size()
+    return read, written
+
+
+def test_algorithmic_bytes_equal_the_tensors_a_call_touches():
+    for wl in (wk.TINY, wk.DECODE, wk.custom(3, 5, 2, 8, 64, 128, gate="safe", seed=1),
+               wk.custom(2, 3, 1, 2, 32, 64, act="f32", seed=2)):
+        read, written = _tensor_bytes(wl)
+        assert wl.shape.algorithmic_bytes(wl.gate) == read + written, wl.name
+
+
+def test_algorithmic_bytes_of_the_large_batch():
+    # the figure the large-batch roofline divides by: 589,480,064 B read
+    # (S0 536.9 MB, inputs 52.6 MB) and 2,250,244,096 B written
+    s = wk.LARGE.shape
+    S = 4 * s.N * s.HV * s.K * s.V
+    read = S + 2 * (s.N * s.T * s.dim + s.N * s.dim * 3 + s.dim * 4 + s.N * s.T * s.HV * s.K
+                    + s.N * s.T * s.HV) + 4 * s.HV * (1 + s.K)
+    written = s.T * S + 2 * (s.N * s.T * s.HV * s.V + s.N * s.T * s.dim * 3 + s.N * s.dim * 3)
+    assert (read, written) == (589_480_064, 2_250_244_096)
+    assert s.algorithmic_bytes(wk.LARGE.gate) == read + written == 2_839_724_160
