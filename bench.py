@@ -837,6 +837,13 @@ def sweep_report(path, peak_gbs, peak_src):
     return "\n".join(out)
 
 
+def commit_bytes(s) -> int:
+    """Algorithmic bytes of one commit: per sequence the accepted state and
+    conv-window snapshots read and the state and conv_state written, plus the
+    accepted counts."""
+    return 2 * s.N * (4 * s.HV * s.K * s.V + 3 * s.dim * s.act_bytes) + 4 * s.N
+
+
 def run_commit(args, wl):
     """HBM bandwidth of kda_commit after one verify of the workload."""
     import torch
@@ -871,7 +878,7 @@ def run_commit(args, wl):
         ev.append((e0, e1))
     torch.cuda.synchronize(dev)
     us = 1e3 * sorted(a.elapsed_time(b) for a, b in ev)[len(ev) // 2]
-    nbytes = 2 * s.N * (4 * s.HV * s.K * s.V + 3 * s.dim * s.act_bytes) + 4 * s.N
+    nbytes = commit_bytes(s)
     peak, src = measured_hbm_peak()
     # back to back over independent copies of everything the call touches
     R = rotation_sets(nbytes)

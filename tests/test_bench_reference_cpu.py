@@ -93,3 +93,20 @@ def test_back_to_back_rotation_sets_evict_each_set_between_uses():
     assert bench.rotation_sets(3 * bench.L2_BYTES) == 2
     # tiny calls would need thousands of sets: no back-to-back figure for them
     assert bench.rotation_sets(1_000_000) > bench.MAX_ROTATION_SETS
+
+
+def test_decode_and_commit_bytes_equal_the_tensors_they_touch():
+    import bench
+    from linear_attention_speculative_gb300 import workloads as wk
+    for wl in (wk.TINY, wk.DECODE, wk.custom(3, 2, 2, 4, 64, 32, gate="safe", seed=3)):
+        s = wl.shape
+        inp = wk.make_inputs(wl)
+        nb = lambda t: t.numel() * t.element_size()
+        # plain decode: every input read once, S and conv_state written in place, o written
+        o_bytes = s.N * s.T * s.HV * s.V * s.act_bytes
+        dec = sum(nb(v) for v in inp.values() if v is not None) + nb(inp["S0"]) + nb(inp["conv_state"]) + o_bytes
+        assert bench.decode_bytes(s, wl.gate) == dec, wl.name
+        # commit: one token's state and conv window read, the state and conv_state written, the counts read
+        out = wk.empty_outputs(wl)
+        one = nb(out["inter_ssm"]) // s.T + nb(out["conv_snapshots"]) // s.T
+        assert bench.commit_bytes(s) == 2 * one + 4 * s.N, wl.name
