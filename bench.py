@@ -761,7 +761,7 @@ def sweep_report(path, peak_gbs, peak_src):
     out.append("")
     out.append(f"Peak: {peak_gbs:.1f} GB/s ({peak_src}, MEASURED_PEAKS.json hbm_gbs).  Times are the median of "
                "per-launch CUDA events with L2 flushed before each launch (258 MB written, then 258 MB read); "
-               "GB/s = algorithmic bytes / time.  An explicit plan that resolves to the same launch as an "
+               "GB/s = algorithmic bytes (from the point's shape and gate) / time.  An explicit plan that resolves to the same launch as an "
                "earlier column (e.g. a q/k roll the dispatcher would pick anyway) is timed once and shares "
                "that column's time.")
     out.append("")
@@ -771,7 +771,7 @@ def sweep_report(path, peak_gbs, peak_src):
     for r in rows:
         best = r["best"]
         b_us = r["us"][best]
-        gbs = r["alg_bytes"] / (b_us / 1e6) / 1e9
+        gbs = row_bytes(r) / (b_us / 1e6) / 1e9
         auto = r["auto"] + (f" ({r['auto_roll']})" if r.get("auto_roll") else "")
         out.append(f"| {r['T']} | {r['N']} | {r['H']} | {r['HV']} | {r['gate']} | {auto} | "
                    f"{r['us']['auto']:.1f} | {best} | {b_us:.1f} | {r['us']['auto'] / b_us:.3f} | "
@@ -835,6 +835,14 @@ def sweep_report(path, peak_gbs, peak_src):
                 cells.append(f"{min(q):.2f}-{max(q):.2f}" if len(q) > 1 else f"{q[0]:.2f}")
             out.append(f"| {T} | " + " | ".join(cells) + " |")
     return "\n".join(out)
+
+
+def row_bytes(r) -> int:
+    """Algorithmic bytes of a sweep row's call, from its shape and gate with the
+    current byte count (rows store the count they were timed with)."""
+    from linear_attention_speculative_gb300 import workloads as wk
+    s = wk.custom(r["N"], r["T"], r["H"], r["HV"], r.get("K", 128), r.get("V", 128), gate=r["gate"]).shape
+    return decode_bytes(s, r["gate"]) if r.get("op") == "decode" else s.algorithmic_bytes(r["gate"])
 
 
 def commit_bytes(s) -> int:
