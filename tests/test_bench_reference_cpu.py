@@ -110,3 +110,11 @@ def test_decode_and_commit_bytes_equal_the_tensors_they_touch():
         out = wk.empty_outputs(wl)
         one = nb(out["inter_ssm"]) // s.T + nb(out["conv_snapshots"]) // s.T
         assert bench.commit_bytes(s) == 2 * one + 4 * s.N, wl.name
+
+
+def test_cpu_baseline_reports_the_oracle_on_a_bounded_sample():
+    import bench
+    from linear_attention_speculative_gb300 import workloads as wk
+    d = bench.cpu_baseline(wk.TINY, wk.make_inputs(wk.TINY), cpu_seconds=0.2)
+    assert d["kind"] == "oracle" and d["value"] > 0 and d["cores"] >= 1 and d["gb_per_s"] > 0
+    assert "oracle" in d["sample"]
